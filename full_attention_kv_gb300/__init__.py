@@ -1,0 +1,12 @@
+"""Hybrid-SWA dual-KV-pool attention for GB300 (sm_103a).
+
+The library is ``_build/libhsa.so`` with the C ABI of ``include/hsa.h``; this
+package is its thin Python binding.  Build it with ``__graft_entry__.build()``
+(or ``python -m full_attention_kv_gb300.build``).
+"""
+from .binding import (  # noqa: F401
+    EXPORTS, HSA_CUDA_ERROR, HSA_DEVERR_BAD_BLOCK, HSA_DEVERR_BAD_LEN, HSA_DEVERR_BAD_PAGE,
+    HSA_DEVERR_BAD_RING, HSA_DEVERR_BAD_SEQ, HSA_DEVERR_TIMEOUT, HSA_INVALID_ARG, HSA_OK,
+    HSA_UNSUPPORTED_SHAPE, DualPool, HsaError, HsaPools, decode_workspace, hsa_decode_attn,
+    hsa_decode_workspace_bytes, hsa_kv_append, hsa_prefill_attn, hsa_window_safe_len,
+    hsa_window_safe_len_bitmap, lib, status_string)

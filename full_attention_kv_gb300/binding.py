@@ -1,0 +1,288 @@
+"""Thin ctypes binding of libhsa (include/hsa.h), same entry-point names.
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels.  PyTorch supplies device memory and streams.  If libhsa.so has not been
+built, every call raises; there is no fallback of any kind.
+"""
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libhsa.so")
+
+HSA_OK = 0
+HSA_INVALID_ARG = 1
+HSA_UNSUPPORTED_SHAPE = 2
+HSA_CUDA_ERROR = 3
+
+HSA_DEVERR_BAD_BLOCK = 1
+HSA_DEVERR_BAD_PAGE = 2
+HSA_DEVERR_BAD_SEQ = 4
+HSA_DEVERR_BAD_RING = 8
+HSA_DEVERR_BAD_LEN = 16
+HSA_DEVERR_TIMEOUT = 32
+
+# every symbol include/hsa.h declares
+EXPORTS = ("hsa_kv_append", "hsa_decode_workspace_bytes", "hsa_decode_attn", "hsa_prefill_attn",
+           "hsa_window_safe_len", "hsa_window_safe_len_bitmap", "hsa_status_string")
+
+
+class HsaError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__("%s failed: %s (%d)" % (fn, status_string(status), status))
+
+
+class HsaPools(ctypes.Structure):
+    """Mirror of the C struct hsa_pools."""
+    _fields_ = [
+        ("n_layers", ctypes.c_int32),
+        ("layer_is_full", ctypes.POINTER(ctypes.c_uint8)),
+        ("k", ctypes.POINTER(ctypes.c_void_p)),
+        ("v", ctypes.POINTER(ctypes.c_void_p)),
+        ("num_blocks", ctypes.c_int32),
+        ("page_size", ctypes.c_int32),
+        ("block_tables", ctypes.c_void_p),
+        ("max_blocks", ctypes.c_int32),
+        ("ring_row", ctypes.c_void_p),
+        ("n_ring_rows", ctypes.c_int32),
+        ("batch", ctypes.c_int32),
+        ("W", ctypes.c_int32),
+        ("Hq", ctypes.c_int32),
+        ("Hkv", ctypes.c_int32),
+        ("d", ctypes.c_int32),
+    ]
+
+
+_lib = None
+
+
+def lib():
+    """Load libhsa.so (raises if it was not built: the CUDA path is the only path)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libhsa.so is not built (%s); run __graft_entry__.build()" % LIB_PATH)
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
+        pp = ctypes.POINTER(HsaPools)
+        L.hsa_kv_append.restype = ctypes.c_int
+        L.hsa_kv_append.argtypes = [pp, i32, vp, vp, vp, vp, vp, i32, i32, vp, vp]
+        L.hsa_decode_workspace_bytes.restype = sz
+        L.hsa_decode_workspace_bytes.argtypes = [pp, i32, i32]
+        L.hsa_decode_attn.restype = ctypes.c_int
+        L.hsa_decode_attn.argtypes = [pp, i32, vp, vp, vp, vp, i32, i32, f32, vp, vp, sz, i32,
+                                      vp, vp]
+        L.hsa_prefill_attn.restype = ctypes.c_int
+        L.hsa_prefill_attn.argtypes = [pp, i32, vp, vp, vp, vp, vp, vp, i32, i32, i32, f32, vp,
+                                       vp, vp]
+        L.hsa_window_safe_len.restype = ctypes.c_int
+        L.hsa_window_safe_len.argtypes = [vp, vp, i32, i32, vp, vp]
+        L.hsa_window_safe_len_bitmap.restype = ctypes.c_int
+        L.hsa_window_safe_len_bitmap.argtypes = [vp, vp, vp, i32, i32, vp, vp]
+        L.hsa_status_string.restype = ctypes.c_char_p
+        L.hsa_status_string.argtypes = [ctypes.c_int]
+        _lib = L
+    return _lib
+
+
+def status_string(s):
+    return lib().hsa_status_string(int(s)).decode()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _need(t, name, dtype, device=None, ndim=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError("%s must have %d dims, got %d" % (name, ndim, t.dim()))
+
+
+def _check(fn, status):
+    if status != HSA_OK:
+        raise HsaError(fn, status)
+
+
+class DualPool:
+    """The dual KV pool of one model: the C struct plus the tensors it points at.
+
+    Full layers own K/V tensors [num_blocks, Hkv, page, d]; sliding layers own
+    rings [n_ring_rows, Hkv, W, d]; block_tables [batch, max_blocks] and ring_row
+    [batch] (int32) are shared by every layer of their kind.
+    """
+
+    def __init__(self, layer_is_full, k, v, block_tables, ring_row, Hq, W=128, page=64):
+        self.layer_is_full = [bool(x) for x in layer_is_full]
+        self.k, self.v = list(k), list(v)
+        self.block_tables, self.ring_row = block_tables, ring_row
+        n = len(self.layer_is_full)
+        assert len(self.k) == n and len(self.v) == n
+        _need(block_tables, "block_tables", torch.int32, ndim=2)
+        _need(ring_row, "ring_row", torch.int32, ndim=1)
+        d = Hkv = num_blocks = n_rows = None
+        for l in range(n):
+            _need(self.k[l], "k[%d]" % l, torch.bfloat16, ndim=4)
+            _need(self.v[l], "v[%d]" % l, torch.bfloat16, ndim=4)
+            if self.k[l].shape != self.v[l].shape:
+                raise ValueError("k[%d] and v[%d] differ in shape" % (l, l))
+            nb, hk, rows, dd = self.k[l].shape
+            if self.layer_is_full[l]:
+                if rows != page:
+                    raise ValueError("full layer %d: rows per block %d != page %d" % (l, rows, page))
+                num_blocks = nb if num_blocks is None else num_blocks
+                if nb != num_blocks:
+                    raise ValueError("full layers disagree on num_blocks")
+            else:
+                if rows != W:
+                    raise ValueError("sliding layer %d: ring slots %d != W %d" % (l, rows, W))
+                n_rows = nb if n_rows is None else n_rows
+                if nb != n_rows:
+                    raise ValueError("sliding layers disagree on ring rows")
+            Hkv = hk if Hkv is None else Hkv
+            d = dd if d is None else d
+            if hk != Hkv or dd != d:
+                raise ValueError("layers disagree on Hkv / d")
+        self._full = (ctypes.c_uint8 * n)(*[1 if f else 0 for f in self.layer_is_full])
+        self._k = (ctypes.c_void_p * n)(*[t.data_ptr() for t in self.k])
+        self._v = (ctypes.c_void_p * n)(*[t.data_ptr() for t in self.v])
+        self.c = HsaPools(
+            n_layers=n, layer_is_full=ctypes.cast(self._full, ctypes.POINTER(ctypes.c_uint8)),
+            k=ctypes.cast(self._k, ctypes.POINTER(ctypes.c_void_p)),
+            v=ctypes.cast(self._v, ctypes.POINTER(ctypes.c_void_p)),
+            num_blocks=num_blocks or 0, page_size=page, block_tables=block_tables.data_ptr(),
+            max_blocks=block_tables.shape[1], ring_row=ring_row.data_ptr(),
+            n_ring_rows=n_rows or 0, batch=block_tables.shape[0], W=W, Hq=Hq, Hkv=Hkv or 0,
+            d=d or 0)
+        self.Hq, self.Hkv, self.d, self.W, self.page = Hq, Hkv, d, W, page
+
+    @classmethod
+    def allocate(cls, layer_is_full, num_blocks, n_ring_rows, block_tables, ring_row, Hq, Hkv,
+                 d=128, W=128, page=64, device="cuda"):
+        """Zero-filled pools (rows past a sequence's length must hold finite values)."""
+        k, v = [], []
+        for f in layer_is_full:
+            shape = (num_blocks, Hkv, page, d) if f else (n_ring_rows, Hkv, W, d)
+            k.append(torch.zeros(shape, dtype=torch.bfloat16, device=device))
+            v.append(torch.zeros(shape, dtype=torch.bfloat16, device=device))
+        return cls(layer_is_full, k, v, block_tables, ring_row, Hq, W=W, page=page)
+
+    def ref(self):
+        return ctypes.byref(self.c)
+
+
+def hsa_kv_append(pool, layer, k_new, v_new, cu_tokens, seq_idx, start_pos, dev_err=None,
+                  stream=None):
+    _need(k_new, "k_new", torch.bfloat16, ndim=3)
+    _need(v_new, "v_new", torch.bfloat16, ndim=3)
+    for n, t in (("cu_tokens", cu_tokens), ("seq_idx", seq_idx), ("start_pos", start_pos)):
+        _need(t, n, torch.int32, ndim=1)
+    R = seq_idx.shape[0]
+    if cu_tokens.shape[0] != R + 1 or start_pos.shape[0] != R:
+        raise ValueError("cu_tokens must be [R+1] and start_pos [R]")
+    if dev_err is not None:
+        _need(dev_err, "dev_err", torch.int32)
+    s = lib().hsa_kv_append(pool.ref(), int(layer), _ptr(k_new), _ptr(v_new), _ptr(cu_tokens),
+                            _ptr(seq_idx), _ptr(start_pos), R, k_new.shape[0], _ptr(dev_err),
+                            _stream(stream))
+    _check("hsa_kv_append", s)
+
+
+def hsa_decode_workspace_bytes(pool, B, T):
+    return int(lib().hsa_decode_workspace_bytes(pool.ref(), int(B), int(T)))
+
+
+def decode_workspace(pool, B, T, device="cuda"):
+    """Zero-filled workspace for hsa_decode_attn (allocate once, reuse)."""
+    n = hsa_decode_workspace_bytes(pool, B, T)
+    return torch.zeros(max(n, 16), dtype=torch.uint8, device=device)
+
+
+def hsa_decode_attn(pool, layer, q, k_new, v_new, cached_len, scale, out=None, workspace=None,
+                    max_ctas=0, dev_err=None, stream=None):
+    _need(q, "q", torch.bfloat16, ndim=4)
+    _need(k_new, "k_new", torch.bfloat16, ndim=4)
+    _need(v_new, "v_new", torch.bfloat16, ndim=4)
+    _need(cached_len, "cached_len", torch.int32, ndim=1)
+    B, T = q.shape[0], q.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, ndim=4)
+    if workspace is None:
+        workspace = decode_workspace(pool, B, T, device=q.device)
+    _need(workspace, "workspace", torch.uint8)
+    if dev_err is not None:
+        _need(dev_err, "dev_err", torch.int32)
+    s = lib().hsa_decode_attn(pool.ref(), int(layer), _ptr(q), _ptr(k_new), _ptr(v_new),
+                              _ptr(cached_len), B, T, float(scale), _ptr(out), _ptr(workspace),
+                              workspace.numel(), int(max_ctas), _ptr(dev_err), _stream(stream))
+    _check("hsa_decode_attn", s)
+    return out
+
+
+def hsa_prefill_attn(pool, layer, q, k_new, v_new, cu_rows, prefix_len, seq_idx, max_chunk,
+                     scale, out=None, dev_err=None, stream=None):
+    _need(q, "q", torch.bfloat16, ndim=3)
+    _need(k_new, "k_new", torch.bfloat16, ndim=3)
+    _need(v_new, "v_new", torch.bfloat16, ndim=3)
+    for n, t in (("cu_rows", cu_rows), ("prefix_len", prefix_len), ("seq_idx", seq_idx)):
+        _need(t, n, torch.int32, ndim=1)
+    R = seq_idx.shape[0]
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, ndim=3)
+    if dev_err is not None:
+        _need(dev_err, "dev_err", torch.int32)
+    s = lib().hsa_prefill_attn(pool.ref(), int(layer), _ptr(q), _ptr(k_new), _ptr(v_new),
+                               _ptr(cu_rows), _ptr(prefix_len), _ptr(seq_idx), R, q.shape[0],
+                               int(max_chunk), float(scale), _ptr(out), _ptr(dev_err),
+                               _stream(stream))
+    _check("hsa_prefill_attn", s)
+    return out
+
+
+def hsa_window_safe_len(match_len, swa_slot_pos, W, out=None, stream=None):
+    _need(match_len, "match_len", torch.int32, ndim=1)
+    _need(swa_slot_pos, "swa_slot_pos", torch.int32, ndim=2)
+    n = match_len.shape[0]
+    if swa_slot_pos.shape != (n, W):
+        raise ValueError("swa_slot_pos must be [n, W]")
+    if out is None:
+        out = torch.empty_like(match_len)
+    s = lib().hsa_window_safe_len(_ptr(match_len), _ptr(swa_slot_pos), n, int(W), _ptr(out),
+                                  _stream(stream))
+    _check("hsa_window_safe_len", s)
+    return out
+
+
+def hsa_window_safe_len_bitmap(match_len, live_off, live, W, out=None, stream=None):
+    _need(match_len, "match_len", torch.int32, ndim=1)
+    _need(live_off, "live_off", torch.int64, ndim=1)
+    _need(live, "live", torch.uint8, ndim=1)
+    n = match_len.shape[0]
+    if live_off.shape[0] != n + 1:
+        raise ValueError("live_off must be [n+1]")
+    if out is None:
+        out = torch.empty_like(match_len)
+    s = lib().hsa_window_safe_len_bitmap(_ptr(match_len), _ptr(live_off), _ptr(live), n, int(W),
+                                         _ptr(out), _stream(stream))
+    _check("hsa_window_safe_len_bitmap", s)
+    return out

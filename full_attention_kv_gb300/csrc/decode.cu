@@ -1,0 +1,589 @@
+// decode.cu -- decode / MTP-verify attention over the dual KV pool (sm_103a).
+//
+// What it computes [youleyou.com "小米MiMo首次公开模型推理系统全链路优化降价99%", s1
+// "为什么选择 Hybrid SWA 架构": decode latency tracks the KV bytes read; s2
+// "KVCache系统重构": Full KV Pool paged and growing, SWA KV Pool a W-slot ring; s2
+// "Decode加速与多模态优化": MTP verifies several candidate tokens per step]:
+// for sequence b, KV head h and query row (t, hh) at position c_b + t,
+//   o = softmax(scale * q . K^T) V over the visible keys,
+// full layers: positions 0 .. c_b + t; sliding layers: c_b + t - W + 1 .. c_b + t.
+// Cached keys come from the pool (block table or ring row), the T new keys from
+// k_new / v_new.
+//
+// Design (one kernel per layer, persistent, one CTA per SM):
+//  * Work items are 64-key tiles: one page of the Full KV Pool, or one half of a
+//    128-slot ring row.  Items of all (sequence, KV head) units are laid end to
+//    end and cut into equal contiguous ranges, one per CTA (flash-decoding with
+//    perfect balance whatever the length mix).
+//  * A producer warp streams each tile's K and V (2 x 16 KB) into a 4-stage
+//    shared-memory ring with TMA (128-byte swizzle), mbarrier-tracked.
+//  * Four consumer warps run the tile on tensor cores (mma.sync m16n8k16 bf16,
+//    fp32 accumulate).  GQA packing: the G query heads x T tokens that share a KV
+//    head form the M dimension (row = t * G + hh), so each KV byte is read once
+//    for all of them.  Online softmax in registers (exp2, quad shuffles).
+//  * At the end of a unit the warps merge their softmax states through shared
+//    memory.  A unit covered by one CTA is written straight to `out`; a unit split
+//    across CTAs leaves (m, l, o) partials in the workspace and the last CTA to
+//    finish it (atomic counter, no waiting) merges them and resets the counter.
+#include "hsa_device.cuh"
+#include "hsa_internal.h"
+
+namespace hsa {
+namespace {
+
+constexpr int kTileKeys = 64;
+constexpr int kD = 128;
+constexpr int kStages = 4;
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kTileBytes = kTileKeys * kD * 2;  // 16 KB: one K or V tile
+constexpr int kStageBytes = 2 * kTileBytes;
+constexpr int kMaxRows = 32;                    // G * T
+constexpr int kNewRows = 16;                    // new-token tile (T <= 4 used)
+constexpr int kCombFloats = 16 + 16 + 16 * kD;  // per warp: m, l, o[16][128]
+constexpr int kPartFloats = kMaxRows * (kD + 2);
+
+struct SharedStorage {
+    alignas(1024) uint8_t stage[kStages][kStageBytes];  // [K lo|K hi|V lo|V hi] per stage
+    alignas(16) uint8_t new_k[kNewRows * kD * 2];
+    alignas(16) uint8_t new_v[kNewRows * kD * 2];
+    alignas(16) float comb[kConsumerWarps][kCombFloats];
+    alignas(8) uint64_t full[kStages];
+    alignas(8) uint64_t empty[kStages];
+    int32_t scan[kThreads];
+    int32_t first_b;
+    int32_t first_items_before;  // items of all units of sequences < first_b (per KV head)
+    int32_t total_items;         // per KV head sum
+    int32_t is_last;
+};
+
+struct Walk {
+    // position in the flattened item space: sequence b, head h, tile j of n
+    int b, h, j, n, c;
+};
+
+__device__ __forceinline__ int clamp_len(int c) { return c < 0 ? 0 : c; }
+
+__device__ __forceinline__ int items_of(const DecodeParams &p, int b)
+{
+    int c = clamp_len(__ldg(p.cached_len + b));
+    int keys = p.ring_mode ? min(c, p.W) : c;
+    int n = (keys + kTileKeys - 1) / kTileKeys;
+    return n > 0 ? n : 1;
+}
+
+__device__ __forceinline__ void walk_load(const DecodeParams &p, Walk &w)
+{
+    w.c = clamp_len(__ldg(p.cached_len + w.b));
+    int keys = p.ring_mode ? min(w.c, p.W) : w.c;
+    int n = (keys + kTileKeys - 1) / kTileKeys;
+    w.n = n > 0 ? n : 1;
+}
+
+__device__ __forceinline__ void walk_next(const DecodeParams &p, Walk &w)
+{
+    if (++w.j == w.n) {
+        w.j = 0;
+        if (++w.h == p.Hkv) {
+            w.h = 0;
+            ++w.b;
+            if (w.b < p.B)
+                walk_load(p, w);
+        }
+    }
+}
+
+// TMA row coordinate of tile (b, h, j), or -1 if the tile holds no cached keys or
+// its address is out of range (flagged in dev_err by the producer only).
+__device__ __forceinline__ int64_t tile_row(const DecodeParams &p, const Walk &w, bool report)
+{
+    if (w.c == 0)
+        return -1;
+    if (p.ring_mode) {
+        int rr = __ldg(p.ring_row + w.b);
+        if (rr < 0 || rr >= p.n_ring_rows) {
+            if (report)
+                set_err(p.dev_err, HSA_DEVERR_BAD_RING);
+            return -1;
+        }
+        return ((int64_t)rr * p.Hkv + w.h) * p.W + (int64_t)w.j * kTileKeys;
+    }
+    if (w.j >= p.max_blocks) {
+        if (report)
+            set_err(p.dev_err, HSA_DEVERR_BAD_PAGE);
+        return -1;
+    }
+    int blk = __ldg(p.block_tables + (int64_t)w.b * p.max_blocks + w.j);
+    if (blk < 0 || blk >= p.num_blocks) {
+        if (report)
+            set_err(p.dev_err, HSA_DEVERR_BAD_BLOCK);
+        return -1;
+    }
+    return ((int64_t)blk * p.Hkv + w.h) * kTileKeys;
+}
+
+// Position held by key k (0..63) of tile j, or -1 if that key is not cached.
+__device__ __forceinline__ int key_pos(const DecodeParams &p, int c, int j, int k)
+{
+    int s = j * kTileKeys + k;
+    if (!p.ring_mode)
+        return s < c ? s : -1;
+    // ring: slot s holds the latest position below c congruent to s mod W
+    int back = (c - 1 - s) % p.W;
+    if (back < 0)
+        back += p.W;
+    int pos = c - 1 - back;
+    return pos;  // may be negative: never written
+}
+
+// Per-warp attention state for one m-tile of 16 query rows.
+struct RowState {
+    float o[kD / 8][4];
+    float m[2];
+    float l[2];
+};
+
+// One key tile on tensor cores.  NT = n-tiles of 8 keys this warp owns inside the
+// tile (keys key0 .. key0 + 8 NT - 1), rows = the tile's row count in shared
+// memory (for the swizzle), vis(row, key) = key visible to that query row.
+template <int NT, typename Vis>
+__device__ __forceinline__ void run_tile(RowState &st, const uint32_t (&qa)[kD / 16][4],
+                                         uint32_t sK, uint32_t sV, int tile_rows, int key0,
+                                         float scale_log2, Vis vis)
+{
+    const int lane = threadIdx.x & 31;
+    const int g = lane >> 2, tq = lane & 3;
+    float s[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+        s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+
+    // S = Q K^T: B fragments via ldmatrix (rows = keys, cols = dims)
+    {
+        const int mi = lane >> 3, r = lane & 7;
+#pragma unroll
+        for (int np = 0; np < NT / 2; ++np) {
+            const int key = key0 + np * 16 + (mi >> 1) * 8 + r;
+#pragma unroll
+            for (int ks = 0; ks < kD / 16; ++ks) {
+                const int dim = ks * 16 + (mi & 1) * 8;
+                uint32_t b0, b1, b2, b3;
+                ldmatrix_x4(sK + swz128_offset(key, dim, tile_rows), b0, b1, b2, b3);
+                mma_bf16_16816(s[2 * np], qa[ks], b0, b1);
+                mma_bf16_16816(s[2 * np + 1], qa[ks], b2, b3);
+            }
+        }
+    }
+
+    // mask + online softmax (base-2, scale folded in)
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int key = key0 + nt * 8 + 2 * tq + e;
+            s[nt][e] = vis(g, key) ? s[nt][e] * scale_log2 : -INFINITY;
+            s[nt][2 + e] = vis(g + 8, key) ? s[nt][2 + e] * scale_log2 : -INFINITY;
+            mx0 = fmaxf(mx0, s[nt][e]);
+            mx1 = fmaxf(mx1, s[nt][2 + e]);
+        }
+    }
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+    const float mn0 = fmaxf(st.m[0], mx0), mn1 = fmaxf(st.m[1], mx1);
+    const float base0 = mn0 == -INFINITY ? 0.f : mn0;
+    const float base1 = mn1 == -INFINITY ? 0.f : mn1;
+    const float a0 = fast_exp2(st.m[0] - base0), a1 = fast_exp2(st.m[1] - base1);
+    st.m[0] = mn0;
+    st.m[1] = mn1;
+    float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        s[nt][0] = fast_exp2(s[nt][0] - base0);
+        s[nt][1] = fast_exp2(s[nt][1] - base0);
+        s[nt][2] = fast_exp2(s[nt][2] - base1);
+        s[nt][3] = fast_exp2(s[nt][3] - base1);
+        sum0 += s[nt][0] + s[nt][1];
+        sum1 += s[nt][2] + s[nt][3];
+    }
+    st.l[0] = st.l[0] * a0 + sum0;
+    st.l[1] = st.l[1] * a1 + sum1;
+#pragma unroll
+    for (int n = 0; n < kD / 8; ++n) {
+        st.o[n][0] *= a0;
+        st.o[n][1] *= a0;
+        st.o[n][2] *= a1;
+        st.o[n][3] *= a1;
+    }
+
+    // O += P V: P from the S accumulators, V fragments via ldmatrix.trans
+    const int mi = lane >> 3, r = lane & 7;
+#pragma unroll
+    for (int ks = 0; ks < NT / 2; ++ks) {
+        uint32_t pa[4];
+        pa[0] = pack_bf16(s[2 * ks][0], s[2 * ks][1]);
+        pa[1] = pack_bf16(s[2 * ks][2], s[2 * ks][3]);
+        pa[2] = pack_bf16(s[2 * ks + 1][0], s[2 * ks + 1][1]);
+        pa[3] = pack_bf16(s[2 * ks + 1][2], s[2 * ks + 1][3]);
+        const int key = key0 + ks * 16 + (mi & 1) * 8 + r;
+#pragma unroll
+        for (int np = 0; np < kD / 16; ++np) {
+            const int dim = np * 16 + (mi >> 1) * 8;
+            uint32_t b0, b1, b2, b3;
+            ldmatrix_x4_trans(sV + swz128_offset(key, dim, tile_rows), b0, b1, b2, b3);
+            mma_bf16_16816(st.o[2 * np], pa, b0, b1);
+            mma_bf16_16816(st.o[2 * np + 1], pa, b2, b3);
+        }
+    }
+}
+
+template <int MT>
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                  const DecodeParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    SharedStorage &sh = *reinterpret_cast<SharedStorage *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+
+    // ---- locate this CTA's contiguous range of items ------------------------
+    {
+        const int per = (p.B + kThreads - 1) / kThreads;
+        const int b_lo = min(p.B, tid * per), b_hi = min(p.B, b_lo + per);
+        int local = 0;
+        for (int b = b_lo; b < b_hi; ++b)
+            local += items_of(p, b);
+        sh.scan[tid] = local;
+        if (tid == 0) {
+            for (int s = 0; s < kStages; ++s) {
+                mbar_init(&sh.full[s], 1);
+                mbar_init(&sh.empty[s], kConsumerWarps);
+            }
+            fence_barrier_init();
+        }
+        __syncthreads();
+        if (tid == 0) {
+            int acc = 0;
+            for (int i = 0; i < kThreads; ++i) {
+                int v = sh.scan[i];
+                sh.scan[i] = acc;
+                acc += v;
+            }
+            sh.total_items = acc;
+        }
+        __syncthreads();
+    }
+    const int64_t N = (int64_t)sh.total_items * p.Hkv;
+    const int64_t C = N < (int64_t)gridDim.x ? N : (int64_t)gridDim.x;
+    if ((int64_t)blockIdx.x >= C)
+        return;
+    const int64_t i0 = (int64_t)blockIdx.x * N / C;
+    const int64_t i1 = ((int64_t)blockIdx.x + 1) * N / C;
+    {
+        // the thread whose chunk of sequences holds item i0 records it
+        const int per = (p.B + kThreads - 1) / kThreads;
+        const int b_lo = min(p.B, tid * per), b_hi = min(p.B, b_lo + per);
+        int before = sh.scan[tid];
+        for (int b = b_lo; b < b_hi; ++b) {
+            int n = items_of(p, b);
+            if ((int64_t)(before + n) * p.Hkv > i0 && (int64_t)before * p.Hkv <= i0) {
+                sh.first_b = b;
+                sh.first_items_before = before;
+            }
+            before += n;
+        }
+        __syncthreads();
+    }
+    Walk w0;
+    w0.b = sh.first_b;
+    walk_load(p, w0);
+    {
+        const int64_t off = i0 - (int64_t)sh.first_items_before * p.Hkv;
+        w0.h = (int)(off / w0.n);
+        w0.j = (int)(off % w0.n);
+    }
+    const int64_t w0_unit_start = i0 - w0.j;  // item index of tile 0 of the first unit
+
+    if (warp == kConsumerWarps) {
+        // ---------------------------------------------------------------- producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tmK);
+            tma_prefetch_desc(&tmV);
+            const uint64_t pol = policy_evict_first();
+            Walk w = w0;
+            for (int64_t i = i0, k = 0; i < i1; ++i, ++k) {
+                const int st = (int)(k % kStages);
+                const uint32_t ph = (uint32_t)((k / kStages) & 1);
+                if (!mbar_wait(&sh.empty[st], ph ^ 1)) {
+                    set_err(p.dev_err, HSA_DEVERR_TIMEOUT);
+                    break;
+                }
+                const int64_t row = tile_row(p, w, true);
+                if (row >= 0) {
+                    mbar_arrive_expect_tx(&sh.full[st], kStageBytes);
+                    uint8_t *dst = sh.stage[st];
+                    tma_load_2d(dst, &tmK, &sh.full[st], 0, (int32_t)row, pol);
+                    tma_load_2d(dst + kTileBytes / 2, &tmK, &sh.full[st], 64, (int32_t)row, pol);
+                    tma_load_2d(dst + kTileBytes, &tmV, &sh.full[st], 0, (int32_t)row, pol);
+                    tma_load_2d(dst + kTileBytes + kTileBytes / 2, &tmV, &sh.full[st], 64,
+                                (int32_t)row, pol);
+                } else {
+                    mbar_arrive(&sh.full[st]);
+                }
+                walk_next(p, w);
+            }
+        }
+        return;
+    }
+
+    // -------------------------------------------------------------------- consumers
+    const int mt = warp % MT;
+    const int slice = warp / MT;
+    constexpr int KW = 16 * MT;  // keys per warp per tile
+    const int key0 = slice * KW;
+    const int g = lane >> 2, tq = lane & 3;
+    const int r0 = mt * 16 + g, r1 = r0 + 8;
+    const int t0 = r0 / p.G, t1 = r1 / p.G;
+    const int rows_valid = p.G * p.T;
+
+    RowState st;
+    uint32_t qa[kD / 16][4];
+    Walk w = w0;
+    int64_t unit_start = w0_unit_start;
+    bool fresh = true;
+    bool timed_out = false;
+
+    for (int64_t i = i0, k = 0; i < i1; ++i, ++k) {
+        if (fresh) {
+            fresh = false;
+            st.m[0] = st.m[1] = -INFINITY;
+            st.l[0] = st.l[1] = 0.f;
+#pragma unroll
+            for (int n = 0; n < kD / 8; ++n)
+                st.o[n][0] = st.o[n][1] = st.o[n][2] = st.o[n][3] = 0.f;
+            const __nv_bfloat16 *q0 =
+                p.q + ((int64_t)(w.b * p.T + t0) * p.Hq + w.h * p.G + r0 % p.G) * kD;
+            const __nv_bfloat16 *q1 =
+                p.q + ((int64_t)(w.b * p.T + t1) * p.Hq + w.h * p.G + r1 % p.G) * kD;
+            const bool v0 = t0 < p.T, v1 = t1 < p.T;
+#pragma unroll
+            for (int ks = 0; ks < kD / 16; ++ks) {
+                const int c0 = ks * 16 + 2 * tq;
+                qa[ks][0] = v0 ? __ldg(reinterpret_cast<const uint32_t *>(q0 + c0)) : 0u;
+                qa[ks][1] = v1 ? __ldg(reinterpret_cast<const uint32_t *>(q1 + c0)) : 0u;
+                qa[ks][2] = v0 ? __ldg(reinterpret_cast<const uint32_t *>(q0 + c0 + 8)) : 0u;
+                qa[ks][3] = v1 ? __ldg(reinterpret_cast<const uint32_t *>(q1 + c0 + 8)) : 0u;
+            }
+        }
+        const int stg = (int)(k % kStages);
+        const uint32_t ph = (uint32_t)((k / kStages) & 1);
+        if (!timed_out && !mbar_wait(&sh.full[stg], ph)) {
+            set_err(p.dev_err, HSA_DEVERR_TIMEOUT);
+            timed_out = true;
+        }
+        const bool loaded = !timed_out && tile_row(p, w, false) >= 0;
+        const int c = w.c;
+        const int j = w.j;
+        bool any = loaded;
+        if (loaded && !p.ring_mode)
+            any = key0 < c - j * kTileKeys;  // this warp's keys hold a cached position
+        if (any) {
+            const uint32_t sK = smem_u32(sh.stage[stg]);
+            const uint32_t sV = sK + kTileBytes;
+            const int W = p.W, T = p.T;
+            const bool ring = p.ring_mode != 0;
+            auto vis = [&](int rr, int key) -> bool {
+                const int t = rr == g ? t0 : t1;
+                if (t >= T)
+                    return false;
+                const int pos = key_pos(p, c, j, key);
+                if (pos < 0)
+                    return false;
+                return !ring || pos >= c + t - W + 1;
+            };
+            run_tile<2 * MT>(st, qa, sK, sV, kTileKeys, key0, p.scale_log2, vis);
+        }
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(&sh.empty[stg]);
+
+        const bool unit_last_tile = (j == w.n - 1);
+        const Walk cur = w;
+        walk_next(p, w);
+        if (!(unit_last_tile || i == i1 - 1))
+            continue;
+
+        // ---- end of this CTA's share of unit (cur.b, cur.h) ------------------
+        const int64_t unit_end = unit_start + cur.n;  // one past its last item
+        if (unit_last_tile) {
+            // new tokens: positions c .. c+T-1, causal among themselves
+            named_bar_sync(1, kConsumerWarps * 32);
+            for (int e = tid; e < kNewRows * kD / 8; e += kConsumerWarps * 32) {
+                const int rr = e / (kD / 8), col = (e % (kD / 8)) * 8;
+                uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
+                if (rr < p.T) {
+                    const int64_t src = ((int64_t)(cur.b * p.T + rr) * p.Hkv + cur.h) * kD + col;
+                    kv = __ldg(reinterpret_cast<const uint4 *>(p.k_new + src));
+                    vv = __ldg(reinterpret_cast<const uint4 *>(p.v_new + src));
+                }
+                *reinterpret_cast<uint4 *>(sh.new_k + swz128_offset(rr, col, kNewRows)) = kv;
+                *reinterpret_cast<uint4 *>(sh.new_v + swz128_offset(rr, col, kNewRows)) = vv;
+            }
+            named_bar_sync(1, kConsumerWarps * 32);
+            if (slice == 0) {
+                const int T = p.T;
+                auto vis_new = [&](int rr, int key) -> bool {
+                    const int t = rr == g ? t0 : t1;
+                    return t < T && key <= t;
+                };
+                run_tile<2>(st, qa, smem_u32(sh.new_k), smem_u32(sh.new_v), kNewRows, 0,
+                            p.scale_log2, vis_new);
+            }
+        }
+
+        // merge the warps' states (same m-tile, different key slices)
+        {
+            float l0 = st.l[0], l1 = st.l[1];
+            l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+            l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+            float *cb = sh.comb[warp];
+            if (tq == 0) {
+                cb[g] = st.m[0];
+                cb[g + 8] = st.m[1];
+                cb[16 + g] = l0;
+                cb[16 + g + 8] = l1;
+            }
+            float *co = cb + 32;
+#pragma unroll
+            for (int n = 0; n < kD / 8; ++n) {
+                *reinterpret_cast<float2 *>(co + g * kD + n * 8 + 2 * tq) =
+                    make_float2(st.o[n][0], st.o[n][1]);
+                *reinterpret_cast<float2 *>(co + (g + 8) * kD + n * 8 + 2 * tq) =
+                    make_float2(st.o[n][2], st.o[n][3]);
+            }
+        }
+        named_bar_sync(1, kConsumerWarps * 32);
+
+        const bool whole = unit_start >= i0 && unit_end <= i1;
+        int32_t slot = -1;
+        if (!whole)
+            slot = 2 * (int)blockIdx.x + (i0 < unit_start ? 1 : 0);  // 1 = CTA's last unit
+        constexpr int kSlices = kConsumerWarps / MT;
+        float *part = p.ws_part + (int64_t)(slot < 0 ? 0 : slot) * kPartFloats;
+        for (int e = tid; e < MT * 16 * kD; e += kConsumerWarps * 32) {
+            const int rr = e / kD, dim = e % kD;
+            const int m_t = rr / 16, rl = rr % 16;
+            float M = -INFINITY;
+#pragma unroll
+            for (int s = 0; s < kSlices; ++s)
+                M = fmaxf(M, sh.comb[m_t + MT * s][rl]);
+            const float base = M == -INFINITY ? 0.f : M;
+            float L = 0.f, O = 0.f;
+#pragma unroll
+            for (int s = 0; s < kSlices; ++s) {
+                const float *cb = sh.comb[m_t + MT * s];
+                const float a = fast_exp2(cb[rl] - base);
+                L += cb[16 + rl] * a;
+                O += cb[32 + rl * kD + dim] * a;
+            }
+            if (rr >= rows_valid)
+                continue;
+            if (whole) {
+                const int t = rr / p.G, hh = rr % p.G;
+                const float val = L > 0.f ? O / L : 0.f;
+                p.out[((int64_t)(cur.b * p.T + t) * p.Hq + cur.h * p.G + hh) * kD + dim] =
+                    __float2bfloat16_rn(val);
+            } else {
+                if (dim == 0) {
+                    __stcg(part + rr, M);
+                    __stcg(part + kMaxRows + rr, L);
+                }
+                __stcg(part + 2 * kMaxRows + rr * kD + dim, O);
+            }
+        }
+        if (!whole) {
+            // count this part in; the last CTA of the unit merges every part
+            const int unit = cur.b * p.Hkv + cur.h;
+            const int64_t c_lo = ((unit_start + 1) * C - 1) / N;
+            const int64_t c_hi = (unit_end * C - 1) / N;
+            named_bar_sync(1, kConsumerWarps * 32);
+            if (tid == 0) {
+                __threadfence();
+                const int prev = atomicAdd(p.ws_cnt + unit, 1);
+                sh.is_last = (prev == (int)(c_hi - c_lo));
+            }
+            named_bar_sync(1, kConsumerWarps * 32);
+            if (sh.is_last) {
+                __threadfence();
+                for (int e = tid; e < rows_valid * kD; e += kConsumerWarps * 32) {
+                    const int rr = e / kD, dim = e % kD;
+                    float M = -INFINITY;
+                    for (int64_t cc = c_lo; cc <= c_hi; ++cc) {
+                        const int64_t start_cc = cc * N / C;
+                        const int sl = 2 * (int)cc + (start_cc < unit_start ? 1 : 0);
+                        M = fmaxf(M, __ldcg(p.ws_part + (int64_t)sl * kPartFloats + rr));
+                    }
+                    const float base = M == -INFINITY ? 0.f : M;
+                    float L = 0.f, O = 0.f;
+                    for (int64_t cc = c_lo; cc <= c_hi; ++cc) {
+                        const int64_t start_cc = cc * N / C;
+                        const int sl = 2 * (int)cc + (start_cc < unit_start ? 1 : 0);
+                        const float *pp = p.ws_part + (int64_t)sl * kPartFloats;
+                        const float a = fast_exp2(__ldcg(pp + rr) - base);
+                        L += __ldcg(pp + kMaxRows + rr) * a;
+                        O += __ldcg(pp + 2 * kMaxRows + rr * kD + dim) * a;
+                    }
+                    const int t = rr / p.G, hh = rr % p.G;
+                    p.out[((int64_t)(cur.b * p.T + t) * p.Hq + cur.h * p.G + hh) * kD + dim] =
+                        __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
+                }
+                if (tid == 0)
+                    p.ws_cnt[unit] = 0;
+            }
+        }
+        named_bar_sync(1, kConsumerWarps * 32);  // comb / new-token buffers free again
+        unit_start = unit_end;
+        fresh = true;
+    }
+}
+
+}  // namespace
+
+size_t decode_workspace_bytes(int num_sms, int B, int Hkv)
+{
+    size_t cnt = ((size_t)B * Hkv * sizeof(int32_t) + 255) & ~size_t(255);
+    size_t part = (size_t)2 * num_sms * kPartFloats * sizeof(float);
+    return cnt + part;
+}
+
+size_t decode_smem_bytes() { return sizeof(SharedStorage) + 1024; }
+
+cudaError_t launch_decode(const CUtensorMap &tmK, const CUtensorMap &tmV, const DecodeParams &p,
+                          int ctas, cudaStream_t stream)
+{
+    const size_t smem = decode_smem_bytes();
+    const int MT = (p.G * p.T + 15) / 16;
+    cudaError_t e;
+    if (MT == 1) {
+        e = cudaFuncSetAttribute(decode_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
+        if (e != cudaSuccess)
+            return e;
+        decode_kernel<1><<<ctas, kThreads, smem, stream>>>(tmK, tmV, p);
+    } else {
+        e = cudaFuncSetAttribute(decode_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
+        if (e != cudaSuccess)
+            return e;
+        decode_kernel<2><<<ctas, kThreads, smem, stream>>>(tmK, tmV, p);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace hsa

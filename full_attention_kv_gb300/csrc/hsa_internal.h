@@ -1,0 +1,86 @@
+// hsa_internal.h -- launch interfaces between the C-ABI layer (api.cu) and the
+// kernels.  Host/device shared structs only; no kernel code.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/hsa.h"
+
+struct __nv_bfloat16;
+
+namespace hsa {
+
+struct DecodeParams {
+    const __nv_bfloat16 *q;      // [B, T, Hq, d]
+    const __nv_bfloat16 *k_new;  // [B, T, Hkv, d]
+    const __nv_bfloat16 *v_new;
+    const int32_t *cached_len;   // [B]
+    const int32_t *block_tables; // [batch, max_blocks]
+    int32_t max_blocks;
+    int32_t num_blocks;
+    const int32_t *ring_row;     // [batch]
+    int32_t n_ring_rows;
+    __nv_bfloat16 *out;          // [B, T, Hq, d]
+    float *ws_part;              // partial softmax states, 2 slots per CTA
+    int32_t *ws_cnt;             // per (sequence, KV head) arrival counters
+    int32_t *dev_err;
+    int32_t B, T, Hq, Hkv, G, W;
+    int32_t ring_mode;           // 0: Full KV Pool pages, 1: SWA ring
+    float scale_log2;            // softmax scale * log2(e)
+};
+
+size_t decode_workspace_bytes(int num_sms, int B, int Hkv);
+size_t decode_smem_bytes();
+cudaError_t launch_decode(const CUtensorMap &tmK, const CUtensorMap &tmV, const DecodeParams &p,
+                          int ctas, cudaStream_t stream);
+
+struct AppendParams {
+    const uint4 *k_new;          // [ntok, Hkv, d] as 16-byte chunks
+    const uint4 *v_new;
+    const int32_t *cu_tokens;    // [R+1]
+    const int32_t *seq_idx;      // [R]
+    const int32_t *start_pos;    // [R]
+    uint4 *k_dst;                // layer's K pool / ring
+    uint4 *v_dst;
+    const int32_t *block_tables;
+    const int32_t *ring_row;
+    int32_t *dev_err;
+    int32_t R, ntok, Hkv, chunks_per_row;  // chunks_per_row = d * 2 / 16
+    int32_t batch, max_blocks, num_blocks, page_size, n_ring_rows, W;
+    int32_t ring_mode;
+};
+
+cudaError_t launch_append(const AppendParams &p, cudaStream_t stream);
+
+struct PrefillParams {
+    const __nv_bfloat16 *q;      // [rows, Hq, d]
+    const __nv_bfloat16 *k_new;  // [rows, Hkv, d]
+    const __nv_bfloat16 *v_new;
+    const int32_t *cu_rows;      // [R+1]
+    const int32_t *prefix_len;   // [R]
+    const int32_t *seq_idx;      // [R]
+    const int32_t *block_tables;
+    const int32_t *ring_row;
+    __nv_bfloat16 *out;          // [rows, Hq, d]
+    int32_t *dev_err;
+    int32_t R, rows, Hq, Hkv, G, W;
+    int32_t batch, max_blocks, num_blocks, n_ring_rows;
+    int32_t ring_mode;
+    int32_t tiles_per_req_bound; // host bound on 128-row tiles per request
+    float scale_log2;
+};
+
+cudaError_t launch_prefill(const CUtensorMap &tmPoolK, const CUtensorMap &tmPoolV,
+                           const CUtensorMap &tmNewK, const CUtensorMap &tmNewV,
+                           const CUtensorMap &tmQ, const PrefillParams &p, cudaStream_t stream);
+
+cudaError_t launch_window_safe_ring(const int32_t *match_len, const int32_t *slot_pos, int32_t n,
+                                    int32_t W, int32_t *out, cudaStream_t stream);
+cudaError_t launch_window_safe_bitmap(const int32_t *match_len, const int64_t *live_off,
+                                      const uint8_t *live, int32_t n, int32_t W, int32_t *out,
+                                      cudaStream_t stream);
+
+}  // namespace hsa

@@ -1,0 +1,228 @@
+"""GPU parity of KV append and decode / MTP-verify attention against the oracle.
+
+Every case runs through the C ABI (the ctypes binding) on seeded inputs from
+workload.py; the oracle gets the generator's tensors, never anything the CUDA
+path wrote.  Bars: pools bit-exact; attention max-abs-error <= 1e-2 against the
+float64 oracle (bf16 inputs, fp32 accumulation, unit-scale outputs).
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import harness
+import oracle
+import workload
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-2
+
+
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import full_attention_kv_gb300 as hsa
+    hsa.lib()
+    return hsa
+
+
+def _bits(t):
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def _decode_all(hsa, inst, pool, layers, **kw):
+    outs = []
+    for i, l in enumerate(layers):
+        q, k, v, cl = harness.decode_inputs(inst, l)
+        outs.append(hsa.hsa_decode_attn(pool, i, q, k, v, cl, inst.cfg.scale, **kw))
+    torch.cuda.synchronize()
+    return outs
+
+
+def _oracle_layer(inst, l, seqs=None):
+    seqs = range(inst.R) if seqs is None else seqs
+    c = harness.oracle_case(inst, l, seqs)
+    W = 0 if inst.full[l] else inst.cfg.W
+    return oracle.attention(window=W, scale=inst.cfg.scale, **c)
+
+
+def test_append_pools_bit_exact_tiny():
+    hsa = _cuda()
+    inst = workload.draw(workload.CONFIGS["tiny"])
+    layers = list(range(inst.cfg.n_layers))
+    pool = harness.make_pool(inst, layers)
+    cfg = inst.cfg
+    for i, l in enumerate(layers):
+        k0, v0 = workload.pool_init(inst, l, "cuda")
+        ek, ev = _bits(k0).copy(), _bits(v0).copy()
+        for s in range(inst.R):
+            hk, hv, st = workload.history(inst, l, s, "cuda")
+            kw = dict(block_tables=inst.block_tables) if inst.full[l] else dict(ring_row=inst.ring_row)
+            bad = oracle.append(ek, ev, [0, hk.shape[0]], [s], [st], hk, hv, **kw)
+            assert bad == 0
+        assert np.array_equal(_bits(pool.k[i]), ek), "K pool of layer %d" % l
+        assert np.array_equal(_bits(pool.v[i]), ev), "V pool of layer %d" % l
+    # one decode token per sequence on top, then compare again
+    for i, l in enumerate(layers):
+        _, k, v = workload.new_tokens(inst, l, "cuda")
+        ek, ev = _bits(pool.k[i]).copy(), _bits(pool.v[i]).copy()
+        cu = torch.arange(inst.R + 1, dtype=torch.int32, device="cuda")
+        seq = torch.arange(inst.R, dtype=torch.int32, device="cuda")
+        pos = torch.from_numpy(inst.prefix).cuda()
+        hsa.hsa_kv_append(pool, i, k, v, cu, seq, pos)
+        torch.cuda.synchronize()
+        kw = dict(block_tables=inst.block_tables) if inst.full[l] else dict(ring_row=inst.ring_row)
+        oracle.append(ek, ev, np.arange(inst.R + 1), np.arange(inst.R), inst.prefix, k, v, **kw)
+        assert np.array_equal(_bits(pool.k[i]), ek) and np.array_equal(_bits(pool.v[i]), ev)
+
+
+def test_ring_append_longer_than_window_keeps_last_w():
+    hsa = _cuda()
+    cfg = dataclasses.replace(workload.CONFIGS["tiny"], contexts=(0, 0), B=2)
+    inst = workload.draw(cfg)
+    pool = harness.make_pool(inst, [0])
+    ek, ev = _bits(pool.k[0]).copy(), _bits(pool.v[0]).copy()
+    n = [300, 77]
+    k = workload.randn_bf16((sum(n), cfg.Hkv, cfg.d), 5, "cuda")
+    v = workload.randn_bf16((sum(n), cfg.Hkv, cfg.d), 6, "cuda")
+    cu = torch.tensor([0, n[0], sum(n)], dtype=torch.int32, device="cuda")
+    seq = torch.tensor([1, 0], dtype=torch.int32, device="cuda")
+    pos = torch.tensor([5, 1000], dtype=torch.int32, device="cuda")
+    hsa.hsa_kv_append(pool, 0, k, v, cu, seq, pos)
+    torch.cuda.synchronize()
+    oracle.append(ek, ev, [0, n[0], sum(n)], [1, 0], [5, 1000], k, v, ring_row=inst.ring_row)
+    assert np.array_equal(_bits(pool.k[0]), ek) and np.array_equal(_bits(pool.v[0]), ev)
+
+
+def test_decode_tiny_all_layers():
+    hsa = _cuda()
+    inst = workload.draw(workload.CONFIGS["tiny"])
+    layers = list(range(inst.cfg.n_layers))
+    pool = harness.make_pool(inst, layers)
+    outs = _decode_all(hsa, inst, pool, layers)
+    for i, l in enumerate(layers):
+        ref = _oracle_layer(inst, l)
+        got = outs[i].float().cpu().numpy().reshape(ref.shape)
+        err = np.max(np.abs(got - ref))
+        assert err <= TOL, "layer %d (%s): max abs err %g" % (l, "full" if inst.full[l] else "swa", err)
+
+
+CONTEXTS = (0, 1, 63, 64, 65, 127, 128, 129, 200, 1000, 4097)
+
+
+@pytest.mark.parametrize("T", [1, 2, 3, 4])
+@pytest.mark.parametrize("heads", [(32, 4), (16, 4)])
+def test_decode_ragged_contexts_and_mtp(T, heads):
+    hsa = _cuda()
+    Hq, Hkv = heads
+    cfg = dataclasses.replace(workload.CONFIGS["tiny"], Hq=Hq, Hkv=Hkv, T=T,
+                              contexts=CONTEXTS, B=len(CONTEXTS), index=50 + T)
+    inst = workload.draw(cfg)
+    layers = [6, 0]  # one full, one sliding
+    pool = harness.make_pool(inst, layers)
+    outs = _decode_all(hsa, inst, pool, layers)
+    for i, l in enumerate(layers):
+        ref = _oracle_layer(inst, l)
+        got = outs[i].float().cpu().numpy().reshape(ref.shape)
+        err = np.max(np.abs(got - ref))
+        assert err <= TOL, "T=%d heads=%s layer %d: err %g" % (T, heads, l, err)
+
+
+def test_split_count_and_page_permutation_invariance():
+    hsa = _cuda()
+    cfg = dataclasses.replace(workload.CONFIGS["tiny"], Hq=32, Hkv=4, T=4,
+                              contexts=(3000, 70, 0, 9000, 129), B=5, index=60)
+    inst = workload.draw(cfg)
+    layers = [6, 0]
+    pool = harness.make_pool(inst, layers)
+    base = _decode_all(hsa, inst, pool, layers)
+    for mc in (1, 2, 5, 13):
+        outs = _decode_all(hsa, inst, pool, layers, max_ctas=mc)
+        for a, b in zip(base, outs):
+            assert torch.max(torch.abs(a.float() - b.float())).item() <= TOL
+    # same logical contents under another physical page permutation: identical bits
+    inst2 = workload.draw(cfg, rng_seed=12345)
+    inst2.prefix[:] = inst.prefix
+    pool2 = harness.make_pool(inst2, layers)
+    outs2 = _decode_all(hsa, inst2, pool2, layers)
+    for a, b in zip(base, outs2):
+        assert torch.equal(a, b)
+
+
+def test_device_range_errors_flagged_not_trapped():
+    hsa = _cuda()
+    cfg = dataclasses.replace(workload.CONFIGS["tiny"], contexts=(500, 300), B=2, index=61)
+    inst = workload.draw(cfg)
+    pool = harness.make_pool(inst, [6, 0])
+    good = _decode_all(hsa, inst, pool, [6, 0])
+    bad_bt = pool.block_tables.clone()
+    bad_bt[1, 2] = inst.num_blocks + 7         # sequence 1, page 2: outside the pool
+    pool.block_tables.copy_(bad_bt)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    q, k, v, cl = harness.decode_inputs(inst, 6)
+    out = hsa.hsa_decode_attn(pool, 0, q, k, v, cl, cfg.scale, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & hsa.HSA_DEVERR_BAD_BLOCK
+    assert torch.equal(out[0], good[0][0])     # the other sequence is untouched
+    # append through the bad entry is skipped and flagged as well
+    err.zero_()
+    kk = torch.zeros((1, cfg.Hkv, cfg.d), dtype=torch.bfloat16, device="cuda")
+    hsa.hsa_kv_append(pool, 0, kk, kk, torch.tensor([0, 1], dtype=torch.int32, device="cuda"),
+                      torch.tensor([1], dtype=torch.int32, device="cuda"),
+                      torch.tensor([130], dtype=torch.int32, device="cuda"), dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & hsa.HSA_DEVERR_BAD_BLOCK
+    # a ring row outside the ring
+    err.zero_()
+    pool.ring_row[0] = inst.n_ring_rows + 3
+    q, k, v, cl = harness.decode_inputs(inst, 0)
+    hsa.hsa_decode_attn(pool, 1, q, k, v, cl, cfg.scale, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & hsa.HSA_DEVERR_BAD_RING
+
+
+def test_host_argument_errors():
+    hsa = _cuda()
+    inst = workload.draw(workload.CONFIGS["tiny"])
+    pool = harness.make_pool(inst, [6])
+    q, k, v, cl = harness.decode_inputs(inst, 6)
+    with pytest.raises(hsa.HsaError) as e:
+        hsa.hsa_decode_attn(pool, 3, q, k, v, cl, 0.1)            # layer out of range
+    assert e.value.status == hsa.HSA_INVALID_ARG
+    ws = torch.zeros(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(hsa.HsaError) as e:
+        hsa.hsa_decode_attn(pool, 0, q, k, v, cl, 0.1, workspace=ws)  # workspace too small
+    assert e.value.status == hsa.HSA_INVALID_ARG
+    q5 = torch.zeros((4, 5, 16, 128), dtype=torch.bfloat16, device="cuda")
+    k5 = torch.zeros((4, 5, 2, 128), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(hsa.HsaError) as e:
+        hsa.hsa_decode_attn(pool, 0, q5, k5, k5, cl, 0.1)         # G*T > 32
+    assert e.value.status == hsa.HSA_UNSUPPORTED_SHAPE
+
+
+def test_window_safe_len_matches_oracle_bit_exact():
+    hsa = _cuda()
+    W = 128
+    match, slots, (idx, bm_len, off, live) = workload.window_cases(1000, W, seed=1004)
+    got = hsa.hsa_window_safe_len(torch.from_numpy(match).cuda(), torch.from_numpy(slots).cuda(), W)
+    ref = oracle.window_safe_len_ring(match, slots, W)
+    assert np.array_equal(got.cpu().numpy(), ref)
+    got_b = hsa.hsa_window_safe_len_bitmap(torch.from_numpy(bm_len).cuda(),
+                                           torch.from_numpy(off).cuda(),
+                                           torch.from_numpy(live).cuda(), W)
+    ref_b = oracle.window_safe_len_bitmap(bm_len, off, live, W)
+    assert np.array_equal(got_b.cpu().numpy(), ref_b)
+
+
+@pytest.mark.parametrize("W", [3, 4, 31, 32, 33, 64])
+def test_window_safe_len_small_windows(W):
+    hsa = _cuda()
+    match, slots, (idx, bm_len, off, live) = workload.window_cases(400, W, seed=W, m_hi=300)
+    got = hsa.hsa_window_safe_len(torch.from_numpy(match).cuda(), torch.from_numpy(slots).cuda(), W)
+    assert np.array_equal(got.cpu().numpy(), oracle.window_safe_len_ring(match, slots, W))
+    got_b = hsa.hsa_window_safe_len_bitmap(torch.from_numpy(bm_len).cuda(),
+                                           torch.from_numpy(off).cuda(),
+                                           torch.from_numpy(live).cuda(), W)
+    assert np.array_equal(got_b.cpu().numpy(), oracle.window_safe_len_bitmap(bm_len, off, live, W))
