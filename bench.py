@@ -1,0 +1,544 @@
+#!/usr/bin/env python3
+"""Benchmark of the Hybrid-SWA dual-KV-pool attention path on GB300.
+
+Default workload: decode, 70-layer stack (60 sliding W=128 + 10 full, 6:1),
+32 q / 4 KV heads, d = 128, batch 32, contexts U[8K, 64K], one new token per
+sequence.  A step is the whole hot path for one batch: for every layer the
+decode attention (hsa_decode_attn) and the append of the new token
+(hsa_kv_append), captured once in a CUDA graph and replayed.
+
+Other workloads (--workload): tiny, long (batch 4, 256K-1M), mtp (batch 48,
+mixed buckets, 4 query tokens + 1000 window-safe cases), prefill (8 requests,
+prefix 16K-128K, chunk 2K-8K).  Inputs are seeded synthetic bf16 N(0,1); the KV
+pools (tens of GB) are far larger than L2, so no extra flush is needed.
+
+Prints ONE JSON line (rank 0).  Under torchrun every rank runs an independent
+replica of the workload (sequences are independent: weak scaling, no
+collective on the data path).
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np
+import torch
+
+import workload
+
+METRIC = ("decode attn tokens/s & KV-read GB/s (% HBM peak); prefill attn TFLOP/s (% peak)")
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+# --------------------------------------------------------------------------- helpers
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            j = json.load(f)
+        return dict(hbm=float(j["hbm_gbs"]), bf16=float(j["bf16_tflops"]),
+                    bf16_sustained=float(j.get("bf16_tflops_sustained", j["bf16_tflops"])),
+                    source="measured")
+    except Exception:
+        return dict(hbm=FALLBACK_HBM_GBS, bf16=FALLBACK_BF16_TFLOPS, bf16_sustained=1700.0,
+                    source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms in the background."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[4:]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in rows:
+            for n, v in zip(names, r[3][1:]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        loaded = [r for r in rows if r[2] > 300.0] or rows
+        return {"sm_mhz": statistics.median(r[0] for r in loaded),
+                "sm_max_mhz": max(r[1] for r in rows), "samples": len(rows),
+                "power_w_max": max(r[2] for r in rows), "reasons": sorted(reasons)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x, ws):
+    if ws == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------- accounting
+def decode_bytes(inst, layer_full):
+    """Algorithmic bytes of one decode attention launch on one layer.
+
+    KV: every key some query of the step may see, once (2048 B per token per
+    layer: K and V, 4 KV heads, d = 128, bf16): full layers c + T tokens, sliding
+    layers min(c + T, W + T - 1).  Plus q read and out written.
+    """
+    cfg = inst.cfg
+    per_tok = 2 * cfg.Hkv * cfg.d * 2
+    c = inst.prefix.astype(np.int64)
+    if layer_full:
+        keys = c + cfg.T
+    else:
+        keys = np.minimum(c + cfg.T, cfg.W + cfg.T - 1)
+    qo = 2 * inst.R * cfg.T * cfg.Hq * cfg.d * 2
+    return int(keys.sum()) * per_tok + qo
+
+
+def keys_per_row(inst, layer_full):
+    """Keys each new row attends (int64 [rows])."""
+    cfg = inst.cfg
+    out = np.zeros(inst.rows, np.int64)
+    for r in range(inst.R):
+        a, b = int(inst.cu_new[r]), int(inst.cu_new[r + 1])
+        pos = int(inst.prefix[r]) + np.arange(b - a, dtype=np.int64)
+        out[a:b] = pos + 1 if layer_full else np.minimum(pos + 1, cfg.W)
+    return out
+
+
+def prefill_flops(inst, layer_full):
+    """4 d Hq x (keys attended per row), masked work excluded."""
+    cfg = inst.cfg
+    total = 0
+    for P, C in zip(inst.prefix.astype(np.int64), inst.new.astype(np.int64)):
+        i = np.arange(C, dtype=np.int64)
+        if layer_full:
+            keys = P + i + 1
+        else:
+            keys = np.minimum(P + i + 1, cfg.W)
+        total += int(keys.sum())
+    return 4 * cfg.d * cfg.Hq * total
+
+
+# --------------------------------------------------------------------------- reference arm
+def run_reference(args, inst):
+    """The CPU oracle as it stands on this host's cores, bounded samples."""
+    import oracle
+    import harness  # noqa: F401  (host-only use below)
+    cfg = inst.cfg
+    nthreads = oracle.num_threads()
+    full_layer = next(l for l in range(cfg.n_layers) if inst.full[l])
+    swa_layer = next(l for l in range(cfg.n_layers) if not inst.full[l])
+    rng = np.random.default_rng(7)
+    n_full = sum(inst.full)
+    n_swa = cfg.n_layers - n_full
+    if cfg.kind == "decode":
+        seqs = list(range(inst.R))
+        if inst.prefix.sum() > 3_000_000:  # keep host memory and time bounded
+            seqs = sorted(rng.choice(inst.R, size=max(1, inst.R // 8), replace=False).tolist())
+    else:
+        seqs = [0]
+    times = []
+    cases = {}
+    for l in (full_layer, swa_layer):
+        rows = [r for s in seqs for r in range(int(inst.cu_new[s]), int(inst.cu_new[s + 1]))]
+        if cfg.kind == "prefill":
+            rows = rows[:: max(1, len(rows) // 64)]  # a row subsample
+        items = np.array([(r, h) for r in rows for h in range(cfg.Hq)], np.int32)
+        cases[l] = (_host_case(inst, l, seqs), rows, items)
+    for step in range(args.warmup + args.steps):
+        t_layer = {}
+        for l in (full_layer, swa_layer):
+            c, rows, items = cases[l]
+            t0 = time.perf_counter()
+            oracle.attention(window=0 if inst.full[l] else cfg.W, scale=cfg.scale, items=items,
+                             nthreads=nthreads, **c)
+            dt = time.perf_counter() - t0
+            kpr = keys_per_row(inst, inst.full[l])
+            t_layer[l] = dt * (kpr.sum() / kpr[rows].sum())  # extrapolate by keys attended
+        if step >= args.warmup:
+            times.append(t_layer[full_layer] * n_full + t_layer[swa_layer] * n_swa)
+    step_s = statistics.median(times)
+    if cfg.kind == "decode":
+        value = inst.R * cfg.T / step_s
+        unit = "tokens/s"
+    else:
+        flops = sum(prefill_flops(inst, f) for f in inst.full)
+        value = flops / step_s / 1e12
+        unit = "TFLOP/s"
+    sample = ("%s: 1 full + 1 sliding layer, %d of %d sequences%s, extrapolated x(%d, %d) "
+              "to %d layers and to all rows" % (cfg.name, len(seqs), inst.R,
+                                                 ", row subsample" if cfg.kind == "prefill" else "",
+                                                 n_full, n_swa, cfg.n_layers))
+    return value, unit, step_s, nthreads, sample
+
+
+def _host_case(inst, layer, seqs):
+    """Oracle inputs generated on the host (CPU generator stream)."""
+    cfg = inst.cfg
+    q, k, v = workload.new_tokens(inst, layer, "cpu")
+    hk, hv, off, start = [], [], [0], []
+    want = set(seqs)
+    for s in range(inst.R):
+        if s in want:
+            a, b, st = workload.history(inst, layer, s, "cpu")
+            hk.append(a)
+            hv.append(b)
+            off.append(off[-1] + a.shape[0])
+            start.append(st)
+        else:
+            off.append(off[-1])
+            start.append(int(inst.prefix[s]))
+    empty = torch.zeros((0, cfg.Hkv, cfg.d), dtype=torch.bfloat16)
+    return dict(cu_rows=inst.cu_new, prefix_len=inst.prefix, q=q, k_new=k, v_new=v,
+                hist_k=torch.cat(hk) if hk else empty, hist_v=torch.cat(hv) if hv else empty,
+                hist_off=np.array(off, np.int64), hist_start=np.array(start, np.int32))
+
+
+# --------------------------------------------------------------------------- our arm
+class DecodeStep:
+    """All layers: decode attention then append of the step's new tokens."""
+
+    def __init__(self, inst, device):
+        import full_attention_kv_gb300 as hsa
+        import harness
+        self.hsa = hsa
+        self.inst = inst
+        cfg = inst.cfg
+        self.layers = list(range(cfg.n_layers))
+        self.pool = harness.make_pool(inst, self.layers, device=device, stale="zero")
+        self.q, self.k, self.v = [], [], []
+        for l in self.layers:
+            q, k, v, cl = harness.decode_inputs(inst, l, device)
+            self.q.append(q)
+            self.k.append(k)
+            self.v.append(v)
+        self.cl = cl
+        B, T = inst.R, cfg.T
+        self.out = [torch.empty_like(q) for q in self.q]
+        self.ws = hsa.decode_workspace(self.pool, B, T, device=device)
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        self.cu = torch.arange(0, B * T + 1, T, dtype=torch.int32, device=device)
+        self.seq = torch.arange(B, dtype=torch.int32, device=device)
+        self.window = None
+        if cfg.n_window_cases:
+            m, slots, _ = workload.window_cases(cfg.n_window_cases, cfg.W, seed=cfg.seed)
+            self.window = (torch.from_numpy(m).to(device), torch.from_numpy(slots).to(device),
+                           torch.empty(len(m), dtype=torch.int32, device=device))
+        self.launches_per_step = 2 * len(self.layers) + (1 if self.window else 0)
+
+    def attn(self, l, stream=None):
+        self.hsa.hsa_decode_attn(self.pool, l, self.q[l], self.k[l], self.v[l], self.cl,
+                                 self.inst.cfg.scale, out=self.out[l], workspace=self.ws,
+                                 dev_err=self.err, stream=stream)
+
+    def __call__(self):
+        cfg = self.inst.cfg
+        B, T = self.inst.R, cfg.T
+        for l in self.layers:
+            self.attn(l)
+            self.hsa.hsa_kv_append(self.pool, l, self.k[l].view(B * T, cfg.Hkv, cfg.d),
+                                   self.v[l].view(B * T, cfg.Hkv, cfg.d), self.cu, self.seq,
+                                   self.cl, dev_err=self.err)
+        if self.window is not None:
+            m, s, o = self.window
+            self.hsa.hsa_window_safe_len(m, s, cfg.W, out=o)
+
+    def inputs(self):
+        return self.q + self.k + self.v
+
+    def outputs(self):
+        return self.out
+
+    def dominant(self):
+        """(name, [layers], algorithmic bytes per launch list)."""
+        full = [l for l in self.layers if self.inst.full[l]]
+        return "decode_kernel (full layers)", full, [decode_bytes(self.inst, True)] * len(full)
+
+    def units_per_step(self):
+        return self.inst.R * self.inst.cfg.T
+
+
+def time_dominant(step, iters):
+    """Average duration of the dominant kernel's launches, CUDA events on its stream."""
+    name, layers, nbytes = step.dominant()
+    stream = torch.cuda.current_stream()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in layers]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in layers]
+    total_ms = 0.0
+    n = 0
+    for it in range(iters + 1):
+        for i, l in enumerate(layers):
+            starts[i].record(stream)
+            step.attn(l, stream=stream)
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+        if it == 0:
+            continue  # warm-up pass
+        for i in range(len(layers)):
+            total_ms += starts[i].elapsed_time(ends[i])
+            n += 1
+    avg_s = total_ms / n / 1e3
+    return name, avg_s, float(np.mean(nbytes))
+
+
+def run_ours(args, inst, ws, rank, local):
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    import full_attention_kv_gb300 as hsa
+    hsa.lib()
+    cfg = inst.cfg
+    if cfg.kind != "decode":
+        raise SystemExit("workload %s: only decode workloads are benchmarked by this arm yet"
+                         % cfg.name)
+    step = DecodeStep(inst, device)
+    stream = torch.cuda.Stream(device)
+    if args.profile_step:
+        # one eager step between cudaProfilerStart / Stop (for ncu --profile-from-start off)
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                step()
+        torch.cuda.synchronize()
+        torch.cuda.cudart().cudaProfilerStart()
+        with torch.cuda.stream(stream):
+            step()
+        torch.cuda.synchronize()
+        torch.cuda.cudart().cudaProfilerStop()
+        return {"profile_step": cfg.name, "launches": step.launches_per_step,
+                "dev_err": int(step.err.item())}
+    # warm-up outside and inside the graph
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            step()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    if int(step.err.item()) != 0:
+        raise SystemExit("device error flag set: %d" % int(step.err.item()))
+
+    # ---- timed region: K graph replays ------------------------------------
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier(ws)
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(args.steps):
+            graph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        barrier(ws)
+        step_ms = e0.elapsed_time(e1) / args.steps
+        # dominant kernel, same stream, per-launch events
+        dom_name, dom_s, dom_bytes = time_dominant(step, max(3, min(args.steps, 10)))
+    clocks = clk.summary()
+    step_ms = max_over_ranks(step_ms, ws)
+
+    # ---- end to end through the C ABI with host buffers ----------------------
+    h_in = [t.cpu().pin_memory() for t in step.inputs()]
+    h_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in step.outputs()]
+    d_in = step.inputs()
+    h2d = sum(t.numel() * t.element_size() for t in h_in)
+    d2h = sum(t.numel() * t.element_size() for t in h_out)
+    cur = torch.cuda.current_stream()
+    for _ in range(2):
+        for h, d in zip(h_in, d_in):
+            d.copy_(h, non_blocking=True)
+        graph.replay()
+        for h, d in zip(h_out, step.outputs()):
+            h.copy_(d, non_blocking=True)
+    torch.cuda.synchronize()
+    barrier(ws)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        for h, d in zip(h_in, d_in):
+            d.copy_(h, non_blocking=True)
+        graph.replay()
+        for h, d in zip(h_out, step.outputs()):
+            h.copy_(d, non_blocking=True)
+    cur.synchronize()
+    e2e_s = (time.perf_counter() - t0) / args.steps
+    e2e_s = max_over_ranks(e2e_s, ws)
+
+    units = step.units_per_step()
+    value = units * ws / (step_ms / 1e3)
+    pk = peaks()
+    achieved = dom_bytes / dom_s / 1e9
+    kv_step = sum(decode_bytes(inst, inst.full[l]) for l in range(cfg.n_layers))
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded bf16 N(0,1), drawn lengths, random page permutation)",
+        "config": {"workload": "%s: %d-layer 6:1 Hybrid-SWA stack (W=%d), Hq=%d Hkv=%d d=%d, "
+                               "batch %d, T=%d, contexts %s" % (
+                                   cfg.name, cfg.n_layers, cfg.W, cfg.Hq, cfg.Hkv, cfg.d, inst.R,
+                                   cfg.T, _ctx_desc(cfg)),
+                   "global_batch": inst.R * ws, "T": cfg.T,
+                   "context_total_tokens": int(inst.prefix.sum()),
+                   "parallelism": "replicas x%d" % ws,
+                   "l2": "inputs larger than L2 (KV pools %.1f GB)" % (_pool_bytes(step.pool) / 1e9),
+                   "graph": "one CUDA graph per step (%d launches)" % step.launches_per_step},
+        "kv_read_gbs": kv_step / (step_ms / 1e3) / 1e9,
+        "hbm_frac_step": kv_step / (step_ms / 1e3) / 1e9 / pk["hbm"],
+        "roofline": {"kernel": dom_name, "bound": "hbm", "achieved": achieved, "peak": pk["hbm"],
+                     "unit": "GB/s", "frac": achieved / pk["hbm"], "traffic": _traffic(cfg.name),
+                     "peak_source": pk["source"], "launch_us": dom_s * 1e6,
+                     "bytes_per_launch": dom_bytes},
+        "clocks": clocks,
+        "e2e": {"value": units * ws / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": step.launches_per_step * args.steps,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        v, unit, _, cores, sample = run_reference(
+            argparse.Namespace(steps=1, warmup=0), inst)
+        line["cpu_baseline"] = {"value": v, "unit": unit, "cores": cores, "kind": "oracle",
+                                "sample": sample}
+    return line
+
+
+def _pool_bytes(pool):
+    return sum(t.numel() * t.element_size() for t in pool.k + pool.v)
+
+
+def _ctx_desc(cfg):
+    if cfg.contexts:
+        return "/".join(str(c) for c in cfg.contexts)
+    if cfg.buckets:
+        return "buckets " + ", ".join("%d-%d:%.1f" % b for b in cfg.buckets)
+    if cfg.kind == "prefill":
+        return "prefix U[%d,%d], chunk U[%d,%d]" % (cfg.prefix_lo, cfg.prefix_hi, cfg.chunk_lo,
+                                                     cfg.chunk_hi)
+    return "U[%d,%d]" % (cfg.ctx_lo, cfg.ctx_hi)
+
+
+# DRAM bytes per launch of the dominant kernel from an ncu capture, keyed by the
+# workload and the source digest of the kernel it was taken on (None = not taken
+# on the current kernel).
+TRAFFIC = {
+    # profiles/decode_full_ncu_decode-b4.md: 389.6 MB on 4 sequences, scaled by units
+    "decode": ("716d087b6c293e7c", 2832703286),
+}
+
+
+def _traffic(name):
+    import hashlib
+    src = os.path.join(ROOT, "full_attention_kv_gb300", "csrc", "decode.cu")
+    with open(src, "rb") as f:
+        digest = hashlib.sha256(f.read()).hexdigest()[:16]
+    t = TRAFFIC.get(name)
+    if t and t[0] == digest:
+        return t[1]
+    return None
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode", choices=sorted(workload.CONFIGS))
+    ap.add_argument("--batch", type=int, default=None, help="truncate the draw (profiling)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-step", action="store_true",
+                    help="run one eager step inside cudaProfilerStart/Stop and exit")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    ws, rank, local = dist_env()
+    cfg = workload.CONFIGS[args.workload]
+    inst = workload.draw(cfg, R=args.batch)
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        v, unit, step_s, cores, sample = run_reference(args, inst)
+        line = {"impl": "reference", "metric": METRIC, "value": v, "unit": unit,
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic (seeded bf16 N(0,1))",
+                "config": {"workload": cfg.name, "global_batch": inst.R},
+                "cpu_baseline": {"value": v, "unit": unit, "cores": cores, "kind": "oracle",
+                                 "sample": sample},
+                "e2e": {"value": v, "unit": unit, "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    if ws > 1:
+        torch.distributed.init_process_group("nccl")
+    line = run_ours(args, inst, ws, rank, local)
+    if rank == 0:
+        print(json.dumps(line))
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

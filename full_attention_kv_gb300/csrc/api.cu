@@ -49,6 +49,23 @@ bool encode_2d(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D bf16 tensor map over a packed [d2][d1][d0] tensor (d0 = 128 elements);
+// box = box0 x 1 x box2; 128-byte swizzle.
+bool encode_3d(CUtensorMap *map, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
+               uint32_t box0, uint32_t box2)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn)
+        return false;
+    cuuint64_t dims[3] = {d0, d1, d2};
+    cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+    cuuint32_t box[3] = {box0, 1, box2};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 int device_sms()
@@ -240,10 +257,58 @@ hsa_status hsa_prefill_attn(const hsa_pools *pools, int32_t layer, const void *q
                             int32_t rows, int32_t max_chunk, float scale, void *out,
                             int32_t *dev_err, void *stream)
 {
-    (void)pools; (void)layer; (void)q; (void)k_new; (void)v_new; (void)cu_rows;
-    (void)prefix_len; (void)seq_idx; (void)R; (void)rows; (void)max_chunk; (void)scale;
-    (void)out; (void)dev_err; (void)stream;
-    return HSA_UNSUPPORTED_SHAPE;
+    hsa_status st = check_pools(pools, layer);
+    if (st != HSA_OK)
+        return st;
+    if (R < 0 || rows < 0 || max_chunk < 0)
+        return HSA_INVALID_ARG;
+    if (R == 0 || rows == 0 || max_chunk == 0)
+        return HSA_OK;
+    if (!q || !k_new || !v_new || !cu_rows || !prefix_len || !seq_idx || !out ||
+        !aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(out))
+        return HSA_INVALID_ARG;
+    const bool full = pools->layer_is_full[layer] != 0;
+    const int G = pools->Hq / pools->Hkv;
+    CUtensorMap tmPK, tmPV, tmNK, tmNV, tmQ;
+    const uint64_t prow = full ? (uint64_t)pools->num_blocks * pools->Hkv * pools->page_size
+                               : (uint64_t)pools->n_ring_rows * pools->Hkv * pools->W;
+    if (!encode_2d(&tmPK, pools->k[layer], 128, prow, 128, 64, 64) ||
+        !encode_2d(&tmPV, pools->v[layer], 128, prow, 128, 64, 64) ||
+        !encode_3d(&tmNK, k_new, 128, pools->Hkv, rows, 64, 128) ||
+        !encode_3d(&tmNV, v_new, 128, pools->Hkv, rows, 64, 128) ||
+        !encode_3d(&tmQ, q, 128, pools->Hq, rows, 64, 128))
+        return HSA_CUDA_ERROR;
+    hsa::PrefillParams p{};
+    p.q = static_cast<const __nv_bfloat16 *>(q);
+    p.k_new = static_cast<const __nv_bfloat16 *>(k_new);
+    p.v_new = static_cast<const __nv_bfloat16 *>(v_new);
+    p.cu_rows = cu_rows;
+    p.prefix_len = prefix_len;
+    p.seq_idx = seq_idx;
+    p.block_tables = pools->block_tables;
+    p.ring_row = pools->ring_row;
+    p.out = static_cast<__nv_bfloat16 *>(out);
+    p.dev_err = dev_err;
+    p.R = R;
+    p.rows = rows;
+    p.Hq = pools->Hq;
+    p.Hkv = pools->Hkv;
+    p.G = G;
+    p.W = pools->W;
+    p.batch = pools->batch;
+    p.max_blocks = pools->max_blocks;
+    p.num_blocks = pools->num_blocks;
+    p.n_ring_rows = pools->n_ring_rows;
+    p.ring_mode = full ? 0 : 1;
+    // upper bound on sum_r ceil(C_r / 128): CTAs past the real count exit at once
+    const int64_t b1 = (int64_t)rows / 128 + R;
+    const int64_t b2 = (int64_t)R * ((max_chunk + 127) / 128);
+    p.tiles_per_req_bound = (int32_t)std::min(b1, b2);
+    p.scale_log2 = scale * 1.4426950408889634f;
+    return hsa::launch_prefill(tmPK, tmPV, tmNK, tmNV, tmQ, p, static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? HSA_OK
+               : HSA_CUDA_ERROR;
 }
 
 hsa_status hsa_window_safe_len(const int32_t *match_len, const int32_t *swa_slot_pos, int32_t n,

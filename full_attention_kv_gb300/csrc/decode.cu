@@ -569,20 +569,20 @@ cudaError_t launch_decode(const CUtensorMap &tmK, const CUtensorMap &tmV, const 
 {
     const size_t smem = decode_smem_bytes();
     const int MT = (p.G * p.T + 15) / 16;
-    cudaError_t e;
-    if (MT == 1) {
-        e = cudaFuncSetAttribute(decode_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem);
+    // the opt-in shared-memory size is set once per process (the API is not a stream
+    // operation, but setting it once keeps graph capture free of extra calls)
+    static bool attr_set[2] = {false, false};
+    auto k1 = decode_kernel<1>;
+    auto k2 = decode_kernel<2>;
+    auto kern = MT == 1 ? k1 : k2;
+    if (!attr_set[MT - 1]) {
+        cudaError_t e =
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess)
             return e;
-        decode_kernel<1><<<ctas, kThreads, smem, stream>>>(tmK, tmV, p);
-    } else {
-        e = cudaFuncSetAttribute(decode_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem);
-        if (e != cudaSuccess)
-            return e;
-        decode_kernel<2><<<ctas, kThreads, smem, stream>>>(tmK, tmV, p);
+        attr_set[MT - 1] = true;
     }
+    kern<<<ctas, kThreads, smem, stream>>>(tmK, tmV, p);
     return cudaGetLastError();
 }
 

@@ -69,10 +69,11 @@ struct PrefillParams {
     int32_t R, rows, Hq, Hkv, G, W;
     int32_t batch, max_blocks, num_blocks, n_ring_rows;
     int32_t ring_mode;
-    int32_t tiles_per_req_bound; // host bound on 128-row tiles per request
+    int32_t tiles_per_req_bound; // host upper bound on the total number of 128-row tiles
     float scale_log2;
 };
 
+size_t prefill_smem_bytes();
 cudaError_t launch_prefill(const CUtensorMap &tmPoolK, const CUtensorMap &tmPoolV,
                            const CUtensorMap &tmNewK, const CUtensorMap &tmNewV,
                            const CUtensorMap &tmQ, const PrefillParams &p, cudaStream_t stream);

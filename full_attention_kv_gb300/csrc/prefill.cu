@@ -1,0 +1,485 @@
+// prefill.cu -- chunked prefill attention on a cached prefix (sm_103a, tcgen05).
+//
+// What it computes [youleyou.com "小米MiMo首次公开模型推理系统全链路优化降价99%", s1
+// "为什么选择 Hybrid SWA 架构": SWA layers attend only the last 128 tokens, so their
+// prefill compute falls to the window; hotdry.top "MiMo-V2.5 ultra-speed inference
+// architecture", "PD 分离与长度分桶": chunked prefill]: request r has P cached
+// tokens and C new rows at positions P + i.  Row i attends
+//   full layers:    positions 0 .. P + i
+//   sliding layers: positions P + i - W + 1 .. P + i
+// with positions < P read from the pools (Full KV Pool pages through the block
+// table, or the SWA ring) and positions >= P from the chunk's own k_new / v_new.
+//
+// Design: one CTA per (request, 128-row query tile, query head); keys in tiles of
+// 128.  Six warps:
+//   warp 0   TMA producer: Q once, then K and V tiles into a 2-stage ring
+//            (128-byte swizzle; a prefix tile is two 64-token pages)
+//   warp 1   TMEM owner and MMA issuer (one thread): S = Q K^T into a
+//            double-buffered TMEM tile, O += P V with P read from TMEM
+//   warps 2-5 softmax, one query row per thread (TMEM lane = row): masks,
+//            running max with lazy rescaling (O is rescaled in TMEM only when
+//            the max grows by more than 2^8), P written back to TMEM as bf16
+// While the softmax warps work on tile n, the tensor cores already compute
+// S for tile n+1.  The epilogue divides O by the row sum and writes bf16.
+#include "hsa_device.cuh"
+#include "hsa_internal.h"
+
+namespace hsa {
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBN = 128;
+constexpr int kD = 128;
+constexpr int kHalfBytes = 128 * 128;      // 128 rows x 64 bf16 (one swizzle column block)
+constexpr int kTileBytes = 2 * kHalfBytes; // 32 KB
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColO = 256;            // S buffers at columns 0 and 128
+constexpr float kRescaleSlack = 8.0f;      // log2 units: P may reach 2^8 before a rescale
+
+struct PrefillSmem {
+    alignas(1024) uint8_t q[kTileBytes];
+    alignas(1024) uint8_t k[2][kTileBytes];
+    alignas(1024) uint8_t v[2][kTileBytes];
+    alignas(8) uint64_t q_full;
+    uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
+    uint64_t s_full[2], p_full[2], pv_done[2], o_full;
+    uint32_t tmem_base;
+    int32_t r, qt, P, C, seq, row0;
+};
+
+struct Sched {
+    int nt;          // key tiles
+    int n_fixed;     // prefix tiles (full) or ring tiles (sliding) before the chunk tiles
+    int m_lo;        // first chunk tile
+};
+
+__device__ __forceinline__ Sched make_sched(const PrefillParams &p, int P, int i0)
+{
+    Sched s;
+    if (!p.ring_mode) {
+        s.n_fixed = (P + kBN - 1) / kBN;
+        s.m_lo = 0;
+    } else {
+        s.n_fixed = (P > 0 && i0 < p.W - 1) ? (p.W + kBN - 1) / kBN : 0;
+        const int lo = i0 - p.W + 1;
+        s.m_lo = lo > 0 ? lo / kBN : 0;
+    }
+    s.nt = s.n_fixed + (i0 / kBN - s.m_lo + 1);
+    return s;
+}
+
+__device__ __forceinline__ bool page_ok(const PrefillParams &p, int seq, int page, int *blk)
+{
+    if (page >= p.max_blocks)
+        return false;
+    const int b = __ldg(p.block_tables + (int64_t)seq * p.max_blocks + page);
+    if (b < 0 || b >= p.num_blocks)
+        return false;
+    *blk = b;
+    return true;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap tmPK, const __grid_constant__ CUtensorMap tmPV,
+                   const __grid_constant__ CUtensorMap tmNK, const __grid_constant__ CUtensorMap tmNV,
+                   const __grid_constant__ CUtensorMap tmQ, const PrefillParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    PrefillSmem &sh = *reinterpret_cast<PrefillSmem *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int hq = blockIdx.x % p.Hq;
+    const int h = hq / p.G;
+
+    // ---- which (request, query tile) this CTA owns --------------------------
+    if (tid == 0) {
+        const int tl = blockIdx.x / p.Hq;
+        int acc = 0, found = -1, qt = 0;
+        for (int r = 0; r < p.R; ++r) {
+            const int C = __ldg(p.cu_rows + r + 1) - __ldg(p.cu_rows + r);
+            const int nq = C > 0 ? (C + kBM - 1) / kBM : 0;
+            if (tl < acc + nq) {
+                found = r;
+                qt = tl - acc;
+                break;
+            }
+            acc += nq;
+        }
+        sh.r = found;
+        if (found >= 0) {
+            sh.qt = qt;
+            sh.P = __ldg(p.prefix_len + found);
+            sh.C = __ldg(p.cu_rows + found + 1) - __ldg(p.cu_rows + found);
+            sh.seq = __ldg(p.seq_idx + found);
+            sh.row0 = __ldg(p.cu_rows + found) + qt * kBM;
+            if (sh.seq < 0 || sh.seq >= p.batch) {
+                if (hq == 0)
+                    set_err(p.dev_err, HSA_DEVERR_BAD_SEQ);
+                sh.r = -1;
+            } else if (sh.P < 0) {
+                if (hq == 0)
+                    set_err(p.dev_err, HSA_DEVERR_BAD_LEN);
+                sh.r = -1;
+            }
+        }
+    }
+    __syncthreads();
+    if (sh.r < 0)
+        return;  // past the last tile (grid is an upper bound) or a bad request
+    const int P = sh.P, C = sh.C, seq = sh.seq, i0 = sh.qt * kBM, row0 = sh.row0;
+    const Sched sc = make_sched(p, P, i0);
+
+    if (tid == 0) {
+        mbar_init(&sh.q_full, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&sh.k_full[s], 1);
+            mbar_init(&sh.k_empty[s], 1);
+            mbar_init(&sh.v_full[s], 1);
+            mbar_init(&sh.v_empty[s], 1);
+            mbar_init(&sh.s_full[s], 1);
+            mbar_init(&sh.p_full[s], 4 * 32);
+            mbar_init(&sh.pv_done[s], 1);
+        }
+        mbar_init(&sh.o_full, 1);
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&sh.tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sh.tmem_base;
+
+    if (warp == 0) {
+        // ================================================================ producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tmQ);
+            tma_prefetch_desc(&tmPK);
+            tma_prefetch_desc(&tmPV);
+            tma_prefetch_desc(&tmNK);
+            tma_prefetch_desc(&tmNV);
+            const uint64_t pol_stream = policy_evict_first();
+            const uint64_t pol_keep = policy_evict_last();
+            mbar_arrive_expect_tx(&sh.q_full, kTileBytes);
+            tma_load_3d(sh.q, &tmQ, &sh.q_full, 0, hq, row0, pol_stream);
+            tma_load_3d(sh.q + kHalfBytes, &tmQ, &sh.q_full, 64, hq, row0, pol_stream);
+            int ring_row = 0;
+            if (p.ring_mode) {
+                ring_row = __ldg(p.ring_row + seq);
+                if (ring_row < 0 || ring_row >= p.n_ring_rows) {
+                    if (hq == 0 && sh.qt == 0)
+                        set_err(p.dev_err, HSA_DEVERR_BAD_RING);
+                    ring_row = 0;
+                }
+            }
+            bool ok = true;
+            for (int n = 0; n < sc.nt && ok; ++n) {
+                const int s = n & 1;
+                const uint32_t ph = (n >> 1) & 1;
+                for (int kv = 0; kv < 2 && ok; ++kv) {
+                    uint64_t *empty = kv ? &sh.v_empty[s] : &sh.k_empty[s];
+                    uint64_t *full = kv ? &sh.v_full[s] : &sh.k_full[s];
+                    uint8_t *dst = kv ? sh.v[s] : sh.k[s];
+                    const CUtensorMap *pool = kv ? &tmPV : &tmPK;
+                    const CUtensorMap *nw = kv ? &tmNV : &tmNK;
+                    if (!mbar_wait(empty, ph ^ 1)) {
+                        set_err(p.dev_err, HSA_DEVERR_TIMEOUT);
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(full, kTileBytes);
+                    if (n < sc.n_fixed) {
+                        // two 64-key blocks: pool pages (full) or ring slot blocks (sliding)
+                        for (int pg = 0; pg < 2; ++pg) {
+                            int32_t y;
+                            if (!p.ring_mode) {
+                                int page = 2 * n + pg;
+                                if (page * 64 >= P)
+                                    page = 2 * n;  // past the prefix: reload, masked
+                                int blk = 0;
+                                if (!page_ok(p, seq, page, &blk)) {
+                                    if (kv == 0)
+                                        set_err(p.dev_err, HSA_DEVERR_BAD_BLOCK);
+                                    blk = 0;  // finite stand-in, masked by the softmax warps
+                                }
+                                y = (blk * p.Hkv + h) * 64;
+                            } else {
+                                int sb = 2 * n + pg;
+                                if (sb * 64 >= p.W)
+                                    sb = 2 * n;
+                                y = (ring_row * p.Hkv + h) * p.W + sb * 64;
+                            }
+                            tma_load_2d(dst + pg * 8192, pool, full, 0, y, pol_keep);
+                            tma_load_2d(dst + kHalfBytes + pg * 8192, pool, full, 64, y, pol_keep);
+                        }
+                    } else {
+                        const int m = sc.m_lo + (n - sc.n_fixed);
+                        const int z = row0 - i0 + m * kBN;  // chunk row of key tile m
+                        tma_load_3d(dst, nw, full, 0, h, z, pol_keep);
+                        tma_load_3d(dst + kHalfBytes, nw, full, 64, h, z, pol_keep);
+                    }
+                }
+            }
+            // drain: no TMA write may still be in flight when the CTA exits
+            for (int s = 0; s < 2 && sc.nt > s; ++s) {
+                const int last = s + ((sc.nt - 1 - s) / 2) * 2;
+                const uint32_t ph = (last >> 1) & 1;
+                mbar_wait(&sh.k_full[s], ph);
+                mbar_wait(&sh.v_full[s], ph);
+            }
+        }
+    } else if (warp == 1) {
+        // ================================================================ MMA issuer
+        if (lane == 0) {
+            const uint32_t id_s = idesc_bf16_f32(kBM, kBN, 0, 0);
+            const uint32_t id_pv = idesc_bf16_f32(kBM, kD, 0, 1);
+            const uint32_t sq = smem_u32(sh.q);
+            bool ok = mbar_wait(&sh.q_full, 0);
+            auto issue_pv = [&](int j) -> bool {
+                const int sj = j & 1;
+                const uint32_t phj = (j >> 1) & 1;
+                if (!mbar_wait(&sh.p_full[sj], phj) || !mbar_wait(&sh.v_full[sj], phj))
+                    return false;
+                tc_fence_after();
+                const uint32_t sv = smem_u32(sh.v[sj]);
+#pragma unroll
+                for (int ks = 0; ks < kBN / 16; ++ks) {
+                    const uint64_t b = smem_desc_sw128(sv + ks * 2048, kHalfBytes, 1024);
+                    tc_mma_ts(tmem + kColO, tmem + sj * 128 + ks * 8, b, id_pv,
+                              (j > 0 || ks > 0) ? 1u : 0u);
+                }
+                tc_commit(&sh.pv_done[sj]);
+                tc_commit(&sh.v_empty[sj]);
+                return true;
+            };
+            for (int n = 0; n < sc.nt && ok; ++n) {
+                const int s = n & 1;
+                const uint32_t ph = (n >> 1) & 1;
+                if (!mbar_wait(&sh.k_full[s], ph)) {
+                    ok = false;
+                    break;
+                }
+                if (n >= 2 && !mbar_wait(&sh.pv_done[s], ((n - 2) >> 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t sk = smem_u32(sh.k[s]);
+#pragma unroll
+                for (int ks = 0; ks < kD / 16; ++ks) {
+                    const uint32_t off = (ks >> 2) * kHalfBytes + (ks & 3) * 32;
+                    const uint64_t a = smem_desc_sw128(sq + off, 16, 1024);
+                    const uint64_t b = smem_desc_sw128(sk + off, 16, 1024);
+                    tc_mma_ss(tmem + s * 128, a, b, id_s, ks > 0 ? 1u : 0u);
+                }
+                tc_commit(&sh.s_full[s]);
+                tc_commit(&sh.k_empty[s]);
+                if (n >= 1 && !issue_pv(n - 1)) {
+                    ok = false;
+                    break;
+                }
+            }
+            if (ok)
+                ok = issue_pv(sc.nt - 1);
+            if (ok) {
+                tc_commit(&sh.o_full);
+                mbar_wait(&sh.o_full, 0);  // every MMA done before TMEM is released
+            } else {
+                set_err(p.dev_err, HSA_DEVERR_TIMEOUT);
+            }
+        }
+    } else {
+        // ================================================================ softmax
+        const int wq = warp & 3;
+        const int row = wq * 32 + lane;
+        const int i = i0 + row;
+        const bool row_ok = i < C;
+        const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
+        float m_used = -INFINITY, l = 0.f;
+        int ring_row_ok = 1;
+        if (p.ring_mode) {
+            const int rr = __ldg(p.ring_row + seq);
+            ring_row_ok = rr >= 0 && rr < p.n_ring_rows;
+        }
+        bool ok = true;
+        for (int n = 0; n < sc.nt; ++n) {
+            const int s = n & 1;
+            const uint32_t ph = (n >> 1) & 1;
+            if (!mbar_wait(&sh.s_full[s], ph)) {
+                set_err(p.dev_err, HSA_DEVERR_TIMEOUT);
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            float x[kBN];
+            {
+                uint32_t r32[32];
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    tmem_ld32(lane_addr + s * 128 + c4 * 32, r32);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < 32; ++c)
+                        x[c4 * 32 + c] = __uint_as_float(r32[c]);
+                }
+            }
+            // ---- visibility of the 128 keys of tile n for query row i ----------
+            int lo = 0, hi = 0;
+            bool ok0 = true, ok1 = true, ring = false;
+            if (n < sc.n_fixed) {
+                if (!p.ring_mode) {
+                    hi = min(kBN, P - n * kBN);
+                    int blk;
+                    ok0 = page_ok(p, seq, 2 * n, &blk);
+                    ok1 = (2 * n + 1) * 64 >= P || page_ok(p, seq, 2 * n + 1, &blk);
+                } else {
+                    ring = true;
+                }
+            } else {
+                const int m = sc.m_lo + (n - sc.n_fixed);
+                const int kb = m * kBN;
+                hi = min(kBN, min(i, C - 1) - kb + 1);
+                if (p.ring_mode)
+                    lo = max(0, i - p.W + 1 - kb);
+            }
+            if (!row_ok)
+                hi = 0;
+            float mx = -INFINITY;
+            if (ring) {
+                // slot t holds the latest prefix position below P congruent to t mod W
+                const int lo_pos = max(0, P + i - p.W + 1);
+#pragma unroll
+                for (int c = 0; c < kBN; ++c) {
+                    const int slot = n * kBN + c;
+                    int back = (P - 1 - slot) % p.W;
+                    back += back < 0 ? p.W : 0;
+                    const int pos = P - 1 - back;
+                    const bool vis = row_ok && ring_row_ok && slot < p.W && pos >= lo_pos;
+                    x[c] = vis ? x[c] * p.scale_log2 : -INFINITY;
+                    mx = fmaxf(mx, x[c]);
+                }
+            } else if (lo == 0 && hi == kBN && ok0 && ok1) {
+#pragma unroll
+                for (int c = 0; c < kBN; ++c) {
+                    x[c] *= p.scale_log2;
+                    mx = fmaxf(mx, x[c]);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < kBN; ++c) {
+                    const bool vis = c >= lo && c < hi && (c < 64 ? ok0 : ok1);
+                    x[c] = vis ? x[c] * p.scale_log2 : -INFINITY;
+                    mx = fmaxf(mx, x[c]);
+                }
+            }
+            // ---- running max, lazily raised; O rescaled in TMEM when it moves ------
+            float m_new = m_used;
+            if (mx != -INFINITY && (m_used == -INFINITY || mx > m_used + kRescaleSlack))
+                m_new = mx;
+            const bool resc = m_used != -INFINITY && m_new != m_used;
+            if (__any_sync(0xffffffffu, resc)) {
+                // O holds sum_{j<n} P_j V_j: wait for PV of tile n-1 before touching it
+                if (!mbar_wait(&sh.pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1)) {
+                    set_err(p.dev_err, HSA_DEVERR_TIMEOUT);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const float alpha = resc ? fast_exp2(m_used - m_new) : 1.0f;
+                uint32_t o32[32];
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    tmem_ld32(lane_addr + kColO + c4 * 32, o32);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < 32; ++c)
+                        o32[c] = __float_as_uint(__uint_as_float(o32[c]) * alpha);
+                    tmem_st32(lane_addr + kColO + c4 * 32, o32);
+                }
+                tmem_wait_st();
+                l *= alpha;
+            }
+            m_used = m_new;
+            const float base = m_used == -INFINITY ? 0.f : m_used;
+            float sum = 0.f;
+            uint32_t pk[32];
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    const float p0 = fast_exp2(x[h2 * 64 + 2 * c] - base);
+                    const float p1 = fast_exp2(x[h2 * 64 + 2 * c + 1] - base);
+                    sum += p0 + p1;
+                    pk[c] = pack_bf16(p0, p1);
+                }
+                tmem_st32(lane_addr + s * 128 + h2 * 32, pk);
+            }
+            l += sum;
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&sh.p_full[s]);
+        }
+        // ---- epilogue: O / l -> bf16 ------------------------------------------
+        if (ok && mbar_wait(&sh.o_full, 0)) {
+            tc_fence_after();
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            __nv_bfloat16 *dst = p.out + ((int64_t)(row0 + row) * p.Hq + hq) * kD;
+            uint32_t o32[32];
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) {
+                tmem_ld32(lane_addr + kColO + c4 * 32, o32);
+                tmem_wait_ld();
+                if (row_ok) {
+#pragma unroll
+                    for (int c = 0; c < 32; c += 8) {
+                        uint4 w;
+                        w.x = pack_bf16(__uint_as_float(o32[c + 0]) * inv, __uint_as_float(o32[c + 1]) * inv);
+                        w.y = pack_bf16(__uint_as_float(o32[c + 2]) * inv, __uint_as_float(o32[c + 3]) * inv);
+                        w.z = pack_bf16(__uint_as_float(o32[c + 4]) * inv, __uint_as_float(o32[c + 5]) * inv);
+                        w.w = pack_bf16(__uint_as_float(o32[c + 6]) * inv, __uint_as_float(o32[c + 7]) * inv);
+                        *reinterpret_cast<uint4 *>(dst + c4 * 32 + c) = w;
+                    }
+                }
+            }
+        } else if (ok) {
+            set_err(p.dev_err, HSA_DEVERR_TIMEOUT);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+}  // namespace
+
+size_t prefill_smem_bytes() { return sizeof(PrefillSmem) + 1024; }
+
+cudaError_t launch_prefill(const CUtensorMap &tmPK, const CUtensorMap &tmPV,
+                           const CUtensorMap &tmNK, const CUtensorMap &tmNV,
+                           const CUtensorMap &tmQ, const PrefillParams &p, cudaStream_t stream)
+{
+    const size_t smem = prefill_smem_bytes();
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(prefill_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess)
+            return e;
+        attr_set = true;
+    }
+    const int64_t ctas = (int64_t)p.tiles_per_req_bound * p.Hq;
+    if (ctas <= 0)
+        return cudaSuccess;
+    prefill_kernel<<<(unsigned)ctas, kThreads, smem, stream>>>(tmPK, tmPV, tmNK, tmNV, tmQ, p);
+    return cudaGetLastError();
+}
+
+}  // namespace hsa

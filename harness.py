@@ -84,6 +84,15 @@ def decode_inputs(inst, layer, device="cuda"):
             v.view(B, T, cfg.Hkv, cfg.d), cl)
 
 
+def prefill_inputs(inst, layer, device="cuda"):
+    """(q [rows,Hq,d], k_new [rows,Hkv,d], v_new, cu_rows, prefix_len, seq_idx)."""
+    q, k, v = workload.new_tokens(inst, layer, device)
+    cu = torch.from_numpy(inst.cu_new).to(device)
+    pl = torch.from_numpy(inst.prefix).to(device)
+    seq = torch.arange(inst.R, dtype=torch.int32, device=device)
+    return q, k, v, cu, pl, seq
+
+
 def oracle_case(inst, layer, seqs, device="cuda"):
     """Host copies of everything the oracle needs for `seqs` of one layer.
 

@@ -47,6 +47,8 @@ class Config:
     ctx_hi: int = 0
     buckets: tuple = ()       # ((lo, hi, weight), ...)
     R: int = 0                # prefill: requests
+    prefixes: tuple = ()      # prefill: fixed cached lengths, else drawn
+    chunks: tuple = ()        # prefill: fixed chunk lengths, else drawn
     prefix_lo: int = 0
     prefix_hi: int = 0
     chunk_lo: int = 0
@@ -129,6 +131,9 @@ def draw(cfg: Config, *, R: Optional[int] = None, rng_seed: Optional[int] = None
         else:
             prefix = [rng.randint(cfg.ctx_lo, cfg.ctx_hi) for _ in range(n)]
         new = [cfg.T] * n
+    elif cfg.prefixes:
+        n = len(cfg.prefixes)
+        prefix, new = list(cfg.prefixes), list(cfg.chunks)
     else:
         n = cfg.R
         prefix = [rng.randint(cfg.prefix_lo, cfg.prefix_hi) for _ in range(n)]
