@@ -257,16 +257,17 @@ def _host_case(inst, layer, seqs):
 class DecodeStep:
     """All layers: decode attention then append of the step's new tokens."""
 
-    def __init__(self, inst, device):
+    def __init__(self, inst, device, layers=None):
         import full_attention_kv_gb300 as hsa
         import harness
         self.hsa = hsa
         self.inst = inst
         cfg = inst.cfg
-        self.layers = list(range(cfg.n_layers))
-        self.pool = harness.make_pool(inst, self.layers, device=device, stale="zero")
+        self.model_layers = list(range(cfg.n_layers)) if layers is None else list(layers)
+        self.layers = list(range(len(self.model_layers)))  # pool layer indices
+        self.pool = harness.make_pool(inst, self.model_layers, device=device, stale="zero")
         self.q, self.k, self.v = [], [], []
-        for l in self.layers:
+        for l in self.model_layers:
             q, k, v, cl = harness.decode_inputs(inst, l, device)
             self.q.append(q)
             self.k.append(k)
@@ -310,7 +311,7 @@ class DecodeStep:
 
     def dominant(self):
         """(name, [layers], algorithmic bytes per launch list)."""
-        full = [l for l in self.layers if self.inst.full[l]]
+        full = [i for i, l in enumerate(self.model_layers) if self.inst.full[l]]
         return "decode_kernel (full layers)", full, [decode_bytes(self.inst, True)] * len(full)
 
     def units_per_step(self):
@@ -349,7 +350,8 @@ def run_ours(args, inst, ws, rank, local):
     if cfg.kind != "decode":
         raise SystemExit("workload %s: only decode workloads are benchmarked by this arm yet"
                          % cfg.name)
-    step = DecodeStep(inst, device)
+    layers = None if args.layers is None else [int(x) for x in args.layers.split(",")]
+    step = DecodeStep(inst, device, layers)
     stream = torch.cuda.Stream(device)
     if args.profile_step:
         # one eager step between cudaProfilerStart / Stop (for ncu --profile-from-start off)
@@ -427,7 +429,7 @@ def run_ours(args, inst, ws, rank, local):
     value = units * ws / (step_ms / 1e3)
     pk = peaks()
     achieved = dom_bytes / dom_s / 1e9
-    kv_step = sum(decode_bytes(inst, inst.full[l]) for l in range(cfg.n_layers))
+    kv_step = sum(decode_bytes(inst, inst.full[l]) for l in step.model_layers)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
@@ -505,6 +507,8 @@ def main():
     ap.add_argument("--workload", default="decode", choices=sorted(workload.CONFIGS))
     ap.add_argument("--batch", type=int, default=None, help="truncate the draw (profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", default=None,
+                    help="comma-separated model layers (profiling sub-stack; default all)")
     ap.add_argument("--profile-step", action="store_true",
                     help="run one eager step inside cudaProfilerStart/Stop and exit")
     args = ap.parse_args()
