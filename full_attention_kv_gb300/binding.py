@@ -25,7 +25,8 @@ HSA_DEVERR_BAD_LEN = 16
 HSA_DEVERR_TIMEOUT = 32
 
 # every symbol include/hsa.h declares
-EXPORTS = ("hsa_kv_append", "hsa_decode_workspace_bytes", "hsa_decode_attn", "hsa_prefill_attn",
+EXPORTS = ("hsa_kv_append", "hsa_decode_workspace_bytes", "hsa_decode_attn",
+           "hsa_decode_attn_noalloc", "hsa_prefill_attn",
            "hsa_window_safe_len", "hsa_window_safe_len_bitmap", "hsa_status_string")
 
 
@@ -75,6 +76,9 @@ def lib():
         L.hsa_decode_attn.restype = ctypes.c_int
         L.hsa_decode_attn.argtypes = [pp, i32, vp, vp, vp, vp, i32, i32, f32, vp, vp, sz, i32,
                                       vp, vp]
+        L.hsa_decode_attn_noalloc.restype = ctypes.c_int
+        L.hsa_decode_attn_noalloc.argtypes = [pp, i32, vp, vp, vp, vp, i32, i32, f32, vp, i32,
+                                              vp, vp]
         L.hsa_prefill_attn.restype = ctypes.c_int
         L.hsa_prefill_attn.argtypes = [pp, i32, vp, vp, vp, vp, vp, vp, i32, i32, i32, f32, vp,
                                        vp, vp]
@@ -235,6 +239,28 @@ def hsa_decode_attn(pool, layer, q, k_new, v_new, cached_len, scale, out=None, w
                               _ptr(cached_len), B, T, float(scale), _ptr(out), _ptr(workspace),
                               workspace.numel(), int(max_ctas), _ptr(dev_err), _stream(stream))
     _check("hsa_decode_attn", s)
+    return out
+
+
+def hsa_decode_attn_noalloc(pool, layer, q, k_new, v_new, cached_len, scale, out, max_ctas=0,
+                            dev_err=None, stream=None):
+    """hsa_decode_attn with the library's own fixed device scratch: for callers that
+    cannot allocate device memory where they run decode (no workspace argument).
+    `out` must be supplied; the call itself allocates nothing.  The first call on a
+    device should come before any stream capture; calls that could overlap on the
+    GPU share one scratch array and must be serialised."""
+    _need(q, "q", torch.bfloat16, ndim=4)
+    _need(k_new, "k_new", torch.bfloat16, ndim=4)
+    _need(v_new, "v_new", torch.bfloat16, ndim=4)
+    _need(cached_len, "cached_len", torch.int32, ndim=1)
+    _need(out, "out", torch.bfloat16, ndim=4)
+    if dev_err is not None:
+        _need(dev_err, "dev_err", torch.int32)
+    B, T = q.shape[0], q.shape[1]
+    s = lib().hsa_decode_attn_noalloc(pool.ref(), int(layer), _ptr(q), _ptr(k_new), _ptr(v_new),
+                                      _ptr(cached_len), B, T, float(scale), _ptr(out),
+                                      int(max_ctas), _ptr(dev_err), _stream(stream))
+    _check("hsa_decode_attn_noalloc", s)
     return out
 
 

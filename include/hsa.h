@@ -131,6 +131,27 @@ hsa_status hsa_decode_attn(const hsa_pools *pools, int32_t layer, const void *q,
                            size_t ws_bytes, int32_t max_ctas, int32_t *dev_err, void *stream);
 
 /*
+ * hsa_decode_attn without a caller workspace.  The pages have no counterpart: this
+ * is a convenience of this library for callers that cannot allocate device memory
+ * where they run decode (while a stream is being captured, inside a host runtime
+ * that owns every allocation, or in a loop that must never wait on cudaMalloc).
+ * Same arguments and results as hsa_decode_attn minus `workspace` / `ws_bytes`.
+ * The scratch is a fixed 8 MiB device array inside libhsa, held by every GPU that
+ * loads the library until the process exits; it covers any batch with
+ * B * Hkv <= 4096 (larger returns HSA_UNSUPPORTED_SHAPE) and caps the CTA count
+ * at what fits (about 250).  This call allocates and frees nothing.
+ *  - The first call on a device looks up the array's device address (and may load
+ *    the library's device code): make that first call before any stream capture.
+ *  - Each call zeroes the counter part of the array on `stream`, then launches.
+ *  - All calls share the one array, so calls whose kernels could overlap on the
+ *    GPU (different streams, or different host threads) race; serialise them.
+ */
+hsa_status hsa_decode_attn_noalloc(const hsa_pools *pools, int32_t layer, const void *q,
+                                   const void *k_new, const void *v_new,
+                                   const int32_t *cached_len, int32_t B, int32_t T, float scale,
+                                   void *out, int32_t max_ctas, int32_t *dev_err, void *stream);
+
+/*
  * Chunked prefill on a cached prefix [youleyou s1: SWA cuts prefill compute to
  * the window; hotdry.top "PD 分离与长度分桶": chunked prefill].
  * Request r has prefix_len[r] tokens in the pools of sequence seq_idx[r] and new
