@@ -4,8 +4,8 @@
 Default workload: decode, 70-layer stack (60 sliding W=128 + 10 full, 6:1),
 32 q / 4 KV heads, d = 128, batch 32, contexts U[8K, 64K], one new token per
 sequence.  A step is the whole hot path for one batch: for every layer the
-decode attention (hsa_decode_attn) and the append of the new token
-(hsa_kv_append), captured once in a CUDA graph and replayed.
+decode attention and the append of the new token (hsa_decode_attn_append, one
+fused launch per layer), captured once in a CUDA graph and replayed.
 
 Other workloads (--workload): tiny, long (batch 4, 256K-1M), mtp (batch 48,
 mixed buckets, 4 query tokens + 1000 window-safe cases), prefill (8 requests,
@@ -255,7 +255,8 @@ def _host_case(inst, layer, seqs):
 
 # --------------------------------------------------------------------------- our arm
 class DecodeStep:
-    """All layers: decode attention then append of the step's new tokens."""
+    """All layers: decode attention fused with the append of the step's new tokens
+    (hsa_decode_attn_append, one launch per layer)."""
 
     def __init__(self, inst, device, layers=None):
         import full_attention_kv_gb300 as hsa
@@ -284,24 +285,20 @@ class DecodeStep:
             m, slots, _ = workload.window_cases(cfg.n_window_cases, cfg.W, seed=cfg.seed)
             self.window = (torch.from_numpy(m).to(device), torch.from_numpy(slots).to(device),
                            torch.empty(len(m), dtype=torch.int32, device=device))
-        self.launches_per_step = 2 * len(self.layers) + (1 if self.window else 0)
+        self.launches_per_step = len(self.layers) + (1 if self.window else 0)
 
     def attn(self, l, stream=None):
-        self.hsa.hsa_decode_attn(self.pool, l, self.q[l], self.k[l], self.v[l], self.cl,
-                                 self.inst.cfg.scale, out=self.out[l], workspace=self.ws,
-                                 dev_err=self.err, stream=stream)
+        # attention fused with the append of the step's new rows (accept-all for T > 1)
+        self.hsa.hsa_decode_attn_append(self.pool, l, self.q[l], self.k[l], self.v[l], self.cl,
+                                        self.inst.cfg.scale, out=self.out[l], workspace=self.ws,
+                                        dev_err=self.err, stream=stream)
 
     def __call__(self):
-        cfg = self.inst.cfg
-        B, T = self.inst.R, cfg.T
         for l in self.layers:
             self.attn(l)
-            self.hsa.hsa_kv_append(self.pool, l, self.k[l].view(B * T, cfg.Hkv, cfg.d),
-                                   self.v[l].view(B * T, cfg.Hkv, cfg.d), self.cu, self.seq,
-                                   self.cl, dev_err=self.err)
         if self.window is not None:
             m, s, o = self.window
-            self.hsa.hsa_window_safe_len(m, s, cfg.W, out=o)
+            self.hsa.hsa_window_safe_len(m, s, self.inst.cfg.W, out=o)
 
     def inputs(self):
         return self.q + self.k + self.v
@@ -316,6 +313,61 @@ class DecodeStep:
 
     def units_per_step(self):
         return self.inst.R * self.inst.cfg.T
+
+
+class PrefillStep:
+    """All layers: chunked prefill attention then append of the chunk.
+
+    Replayed steps re-append the same chunk, so after the first step a sliding
+    layer's ring holds the chunk's tail instead of the prefix's: values change, the
+    work (masks depend only on lengths) does not.
+    """
+
+    def __init__(self, inst, device, layers=None):
+        import full_attention_kv_gb300 as hsa
+        import harness
+        self.hsa = hsa
+        self.inst = inst
+        cfg = inst.cfg
+        self.model_layers = list(range(cfg.n_layers)) if layers is None else list(layers)
+        self.layers = list(range(len(self.model_layers)))
+        self.pool = harness.make_pool(inst, self.model_layers, device=device, stale="zero")
+        self.q, self.k, self.v = [], [], []
+        for l in self.model_layers:
+            q, k, v, cu, pl, seq = harness.prefill_inputs(inst, l, device)
+            self.q.append(q)
+            self.k.append(k)
+            self.v.append(v)
+        self.cu, self.pl, self.seq = cu, pl, seq
+        self.max_chunk = int(inst.new.max())
+        self.out = [torch.empty_like(q) for q in self.q]
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        self.launches_per_step = 2 * len(self.layers)
+
+    def attn(self, l, stream=None):
+        self.hsa.hsa_prefill_attn(self.pool, l, self.q[l], self.k[l], self.v[l], self.cu,
+                                  self.pl, self.seq, self.max_chunk, self.inst.cfg.scale,
+                                  out=self.out[l], dev_err=self.err, stream=stream)
+
+    def __call__(self):
+        for l in self.layers:
+            self.attn(l)
+            self.hsa.hsa_kv_append(self.pool, l, self.k[l], self.v[l], self.cu, self.seq,
+                                   self.pl, dev_err=self.err)
+
+    def inputs(self):
+        return self.q + self.k + self.v
+
+    def outputs(self):
+        return self.out
+
+    def dominant(self):
+        full = [i for i, l in enumerate(self.model_layers) if self.inst.full[l]]
+        return ("prefill_kernel (full layers)", full,
+                [prefill_flops(self.inst, True)] * len(full))
+
+    def units_per_step(self):
+        return sum(prefill_flops(self.inst, self.inst.full[l]) for l in self.model_layers)
 
 
 def time_dominant(step, iters):
@@ -347,11 +399,8 @@ def run_ours(args, inst, ws, rank, local):
     import full_attention_kv_gb300 as hsa
     hsa.lib()
     cfg = inst.cfg
-    if cfg.kind != "decode":
-        raise SystemExit("workload %s: only decode workloads are benchmarked by this arm yet"
-                         % cfg.name)
     layers = None if args.layers is None else [int(x) for x in args.layers.split(",")]
-    step = DecodeStep(inst, device, layers)
+    step = (DecodeStep if cfg.kind == "decode" else PrefillStep)(inst, device, layers)
     stream = torch.cuda.Stream(device)
     if args.profile_step:
         # one eager step between cudaProfilerStart / Stop (for ncu --profile-from-start off)
@@ -426,12 +475,32 @@ def run_ours(args, inst, ws, rank, local):
     e2e_s = max_over_ranks(e2e_s, ws)
 
     units = step.units_per_step()
-    value = units * ws / (step_ms / 1e3)
     pk = peaks()
-    achieved = dom_bytes / dom_s / 1e9
-    kv_step = sum(decode_bytes(inst, inst.full[l]) for l in step.model_layers)
+    if cfg.kind == "decode":
+        value = units * ws / (step_ms / 1e3)
+        unit = "tokens/s"
+        e2e_value = units * ws / e2e_s
+        achieved = dom_bytes / dom_s / 1e9
+        roof = {"kernel": dom_name, "bound": "hbm", "achieved": achieved, "peak": pk["hbm"],
+                "unit": "GB/s", "frac": achieved / pk["hbm"], "traffic": _traffic(cfg.name),
+                "peak_source": pk["source"], "launch_us": dom_s * 1e6,
+                "bytes_per_launch": dom_bytes}
+        kv_step = sum(decode_bytes(inst, inst.full[l]) for l in step.model_layers)
+        extra = {"kv_read_gbs": kv_step / (step_ms / 1e3) / 1e9,
+                 "hbm_frac_step": kv_step / (step_ms / 1e3) / 1e9 / pk["hbm"]}
+    else:
+        value = units * ws / (step_ms / 1e3) / 1e12
+        unit = "TFLOP/s"
+        e2e_value = units * ws / e2e_s / 1e12
+        achieved = dom_bytes / dom_s / 1e12
+        roof = {"kernel": dom_name, "bound": "tensor", "achieved": achieved, "peak": pk["bf16"],
+                "unit": "TFLOP/s", "frac": achieved / pk["bf16"], "traffic": _traffic(cfg.name),
+                "peak_source": pk["source"] + " (burst: each launch timed alone)",
+                "launch_us": dom_s * 1e6, "flops_per_launch": dom_bytes}
+        extra = {"step_tflops_frac_sustained": value / ws / pk["bf16_sustained"],
+                 "prefill_rows": inst.rows}
     line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+        "metric": METRIC, "value": value, "unit": unit, "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded bf16 N(0,1), drawn lengths, random page permutation)",
@@ -444,17 +513,13 @@ def run_ours(args, inst, ws, rank, local):
                    "parallelism": "replicas x%d" % ws,
                    "l2": "inputs larger than L2 (KV pools %.1f GB)" % (_pool_bytes(step.pool) / 1e9),
                    "graph": "one CUDA graph per step (%d launches)" % step.launches_per_step},
-        "kv_read_gbs": kv_step / (step_ms / 1e3) / 1e9,
-        "hbm_frac_step": kv_step / (step_ms / 1e3) / 1e9 / pk["hbm"],
-        "roofline": {"kernel": dom_name, "bound": "hbm", "achieved": achieved, "peak": pk["hbm"],
-                     "unit": "GB/s", "frac": achieved / pk["hbm"], "traffic": _traffic(cfg.name),
-                     "peak_source": pk["source"], "launch_us": dom_s * 1e6,
-                     "bytes_per_launch": dom_bytes},
+        "roofline": roof,
         "clocks": clocks,
-        "e2e": {"value": units * ws / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+        "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": step.launches_per_step * args.steps,
     }
+    line.update(extra)
     if rank == 0 and not args.no_cpu_baseline:
         v, unit, _, cores, sample = run_reference(
             argparse.Namespace(steps=1, warmup=0), inst)
@@ -489,7 +554,8 @@ TRAFFIC = {
 
 def _traffic(name):
     import hashlib
-    src = os.path.join(ROOT, "full_attention_kv_gb300", "csrc", "decode.cu")
+    kern = "prefill.cu" if workload.CONFIGS[name].kind == "prefill" else "decode.cu"
+    src = os.path.join(ROOT, "full_attention_kv_gb300", "csrc", kern)
     with open(src, "rb") as f:
         digest = hashlib.sha256(f.read()).hexdigest()[:16]
     t = TRAFFIC.get(name)

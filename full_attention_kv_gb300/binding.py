@@ -26,7 +26,7 @@ HSA_DEVERR_TIMEOUT = 32
 
 # every symbol include/hsa.h declares
 EXPORTS = ("hsa_kv_append", "hsa_decode_workspace_bytes", "hsa_decode_attn",
-           "hsa_decode_attn_noalloc", "hsa_prefill_attn",
+           "hsa_decode_attn_append", "hsa_decode_attn_noalloc", "hsa_prefill_attn",
            "hsa_window_safe_len", "hsa_window_safe_len_bitmap", "hsa_status_string")
 
 
@@ -76,6 +76,9 @@ def lib():
         L.hsa_decode_attn.restype = ctypes.c_int
         L.hsa_decode_attn.argtypes = [pp, i32, vp, vp, vp, vp, i32, i32, f32, vp, vp, sz, i32,
                                       vp, vp]
+        L.hsa_decode_attn_append.restype = ctypes.c_int
+        L.hsa_decode_attn_append.argtypes = [pp, i32, vp, vp, vp, vp, i32, i32, f32, vp, vp, sz,
+                                             i32, vp, vp]
         L.hsa_decode_attn_noalloc.restype = ctypes.c_int
         L.hsa_decode_attn_noalloc.argtypes = [pp, i32, vp, vp, vp, vp, i32, i32, f32, vp, i32,
                                               vp, vp]
@@ -221,7 +224,7 @@ def decode_workspace(pool, B, T, device="cuda"):
 
 
 def hsa_decode_attn(pool, layer, q, k_new, v_new, cached_len, scale, out=None, workspace=None,
-                    max_ctas=0, dev_err=None, stream=None):
+                    max_ctas=0, dev_err=None, stream=None, append=False):
     _need(q, "q", torch.bfloat16, ndim=4)
     _need(k_new, "k_new", torch.bfloat16, ndim=4)
     _need(v_new, "v_new", torch.bfloat16, ndim=4)
@@ -235,11 +238,20 @@ def hsa_decode_attn(pool, layer, q, k_new, v_new, cached_len, scale, out=None, w
     _need(workspace, "workspace", torch.uint8)
     if dev_err is not None:
         _need(dev_err, "dev_err", torch.int32)
-    s = lib().hsa_decode_attn(pool.ref(), int(layer), _ptr(q), _ptr(k_new), _ptr(v_new),
-                              _ptr(cached_len), B, T, float(scale), _ptr(out), _ptr(workspace),
-                              workspace.numel(), int(max_ctas), _ptr(dev_err), _stream(stream))
-    _check("hsa_decode_attn", s)
+    fn = lib().hsa_decode_attn_append if append else lib().hsa_decode_attn
+    s = fn(pool.ref(), int(layer), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(cached_len), B, T,
+           float(scale), _ptr(out), _ptr(workspace), workspace.numel(), int(max_ctas),
+           _ptr(dev_err), _stream(stream))
+    _check("hsa_decode_attn_append" if append else "hsa_decode_attn", s)
     return out
+
+
+def hsa_decode_attn_append(pool, layer, q, k_new, v_new, cached_len, scale, out=None,
+                           workspace=None, max_ctas=0, dev_err=None, stream=None):
+    """Decode attention, then the T new K/V rows of every sequence appended."""
+    return hsa_decode_attn(pool, layer, q, k_new, v_new, cached_len, scale, out=out,
+                           workspace=workspace, max_ctas=max_ctas, dev_err=dev_err,
+                           stream=stream, append=True)
 
 
 def hsa_decode_attn_noalloc(pool, layer, q, k_new, v_new, cached_len, scale, out, max_ctas=0,

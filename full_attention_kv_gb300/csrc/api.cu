@@ -178,10 +178,14 @@ size_t hsa_decode_workspace_bytes(const hsa_pools *pools, int32_t B, int32_t T)
     return hsa::decode_workspace_bytes(std::max(sms > 0 ? sms : 1, B * hkv), B, hkv);
 }
 
-hsa_status hsa_decode_attn(const hsa_pools *pools, int32_t layer, const void *q,
-                           const void *k_new, const void *v_new, const int32_t *cached_len,
-                           int32_t B, int32_t T, float scale, void *out, void *workspace,
-                           size_t ws_bytes, int32_t max_ctas, int32_t *dev_err, void *stream)
+}  // extern "C"
+
+namespace {
+
+hsa_status decode_common(const hsa_pools *pools, int32_t layer, const void *q, const void *k_new,
+                         const void *v_new, const int32_t *cached_len, int32_t B, int32_t T,
+                         float scale, void *out, void *workspace, size_t ws_bytes,
+                         int32_t max_ctas, int32_t *dev_err, void *stream, int append)
 {
     hsa_status st = check_pools(pools, layer);
     if (st != HSA_OK)
@@ -229,26 +233,48 @@ hsa_status hsa_decode_attn(const hsa_pools *pools, int32_t layer, const void *q,
     p.v_new = static_cast<const __nv_bfloat16 *>(v_new);
     p.cached_len = cached_len;
     p.block_tables = pools->block_tables;
+    p.ring_row = pools->ring_row;
+    p.out = static_cast<__nv_bfloat16 *>(out);
+    p.ws = static_cast<uint8_t *>(workspace);
+    p.dev_err = dev_err;
+    p.k_dst = static_cast<uint4 *>(pools->k[layer]);
+    p.v_dst = static_cast<uint4 *>(pools->v[layer]);
     p.max_blocks = pools->max_blocks;
     p.num_blocks = pools->num_blocks;
-    p.ring_row = pools->ring_row;
     p.n_ring_rows = pools->n_ring_rows;
-    p.out = static_cast<__nv_bfloat16 *>(out);
-    const size_t cnt_bytes = ((size_t)B * pools->Hkv * sizeof(int32_t) + 255) & ~size_t(255);
-    p.ws_cnt = static_cast<int32_t *>(workspace);
-    p.ws_part = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + cnt_bytes);
-    p.dev_err = dev_err;
     p.B = B;
-    p.T = T;
-    p.Hq = pools->Hq;
     p.Hkv = pools->Hkv;
-    p.G = G;
     p.W = pools->W;
-    p.ring_mode = full ? 0 : 1;
+    p.T = (int16_t)T;
+    p.G = (int16_t)G;
+    p.flags = (full ? 0 : hsa::kDecodeRing) | (append ? hsa::kDecodeAppend : 0);
     p.scale_log2 = scale * 1.4426950408889634f;
     return hsa::launch_decode(tmK, tmV, p, ctas, static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? HSA_OK
                : HSA_CUDA_ERROR;
+}
+
+}  // namespace
+
+extern "C" {
+
+hsa_status hsa_decode_attn(const hsa_pools *pools, int32_t layer, const void *q,
+                           const void *k_new, const void *v_new, const int32_t *cached_len,
+                           int32_t B, int32_t T, float scale, void *out, void *workspace,
+                           size_t ws_bytes, int32_t max_ctas, int32_t *dev_err, void *stream)
+{
+    return decode_common(pools, layer, q, k_new, v_new, cached_len, B, T, scale, out, workspace,
+                         ws_bytes, max_ctas, dev_err, stream, 0);
+}
+
+hsa_status hsa_decode_attn_append(const hsa_pools *pools, int32_t layer, const void *q,
+                                  const void *k_new, const void *v_new,
+                                  const int32_t *cached_len, int32_t B, int32_t T, float scale,
+                                  void *out, void *workspace, size_t ws_bytes, int32_t max_ctas,
+                                  int32_t *dev_err, void *stream)
+{
+    return decode_common(pools, layer, q, k_new, v_new, cached_len, B, T, scale, out, workspace,
+                         ws_bytes, max_ctas, dev_err, stream, 1);
 }
 
 hsa_status hsa_prefill_attn(const hsa_pools *pools, int32_t layer, const void *q,

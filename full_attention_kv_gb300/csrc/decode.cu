@@ -19,12 +19,19 @@
 //    shared-memory ring with TMA (128-byte swizzle), mbarrier-tracked.
 //  * Four consumer warps run the tile on tensor cores (mma.sync m16n8k16 bf16,
 //    fp32 accumulate).  GQA packing: the G query heads x T tokens that share a KV
-//    head form the M dimension (row = t * G + hh), so each KV byte is read once
-//    for all of them.  Online softmax in registers (exp2, quad shuffles).
+//    head form the M dimension (row = t * G + hh), so each KV byte is read once for
+//    all of them.  16 rows (T <= 2): each warp owns 16 keys of every tile; 32 rows
+//    (T = 3, 4): two warps per 16-row m-tile, 32 keys each.  Online softmax in
+//    registers (exp2, quad shuffles).
 //  * At the end of a unit the warps merge their softmax states through shared
 //    memory.  A unit covered by one CTA is written straight to `out`; a unit split
 //    across CTAs leaves (m, l, o) partials in the workspace and the last CTA to
 //    finish it (atomic counter, no waiting) merges them and resets the counter.
+//  * Optionally (hsa_decode_attn_append) the CTA that completes a unit also appends
+//    the unit's new K/V rows to the pool or ring: every read of that unit is done
+//    by then, so even a T > 1 ring write cannot clobber a slot still being read.
+//  * Launched with programmatic dependent launch: nothing global is read before
+//    griddepcontrol.wait, so the launch and prologue overlap the previous kernel.
 #include "hsa_device.cuh"
 #include "hsa_internal.h"
 
@@ -67,7 +74,7 @@ __device__ __forceinline__ int clamp_len(int c) { return c < 0 ? 0 : c; }
 __device__ __forceinline__ int items_of(const DecodeParams &p, int b)
 {
     int c = clamp_len(__ldg(p.cached_len + b));
-    int keys = p.ring_mode ? min(c, p.W) : c;
+    int keys = (p.flags & kDecodeRing) ? min(c, p.W) : c;
     int n = (keys + kTileKeys - 1) / kTileKeys;
     return n > 0 ? n : 1;
 }
@@ -75,7 +82,7 @@ __device__ __forceinline__ int items_of(const DecodeParams &p, int b)
 __device__ __forceinline__ void walk_load(const DecodeParams &p, Walk &w)
 {
     w.c = clamp_len(__ldg(p.cached_len + w.b));
-    int keys = p.ring_mode ? min(w.c, p.W) : w.c;
+    int keys = (p.flags & kDecodeRing) ? min(w.c, p.W) : w.c;
     int n = (keys + kTileKeys - 1) / kTileKeys;
     w.n = n > 0 ? n : 1;
 }
@@ -99,7 +106,7 @@ __device__ __forceinline__ int64_t tile_row(const DecodeParams &p, const Walk &w
 {
     if (w.c == 0)
         return -1;
-    if (p.ring_mode) {
+    if (p.flags & kDecodeRing) {
         int rr = __ldg(p.ring_row + w.b);
         if (rr < 0 || rr >= p.n_ring_rows) {
             if (report)
@@ -126,7 +133,7 @@ __device__ __forceinline__ int64_t tile_row(const DecodeParams &p, const Walk &w
 __device__ __forceinline__ int key_pos(const DecodeParams &p, int c, int j, int k)
 {
     int s = j * kTileKeys + k;
-    if (!p.ring_mode)
+    if (!(p.flags & kDecodeRing))
         return s < c ? s : -1;
     // ring: slot s holds the latest position below c congruent to s mod W
     int back = (c - 1 - s) % p.W;
@@ -239,6 +246,51 @@ __device__ __forceinline__ void run_tile(RowState &st, const uint32_t (&qa)[kD /
     }
 }
 
+// Append the T new K/V rows of unit (b, h) to this layer's pool or ring.  Called by
+// the CTA that completes the unit, after every read of the unit has finished.
+__device__ __forceinline__ void append_unit(const DecodeParams &p, int b, int h, int c, int tid,
+                                            int nthreads)
+{
+    constexpr int kChunks = kD * 2 / 16;  // 16-byte chunks per row
+    const int total = 2 * p.T * kChunks;
+    const bool ring = (p.flags & kDecodeRing) != 0;
+    int rr = 0;
+    if (ring) {
+        rr = __ldg(p.ring_row + b);
+        if (rr < 0 || rr >= p.n_ring_rows) {
+            if (tid == 0)
+                set_err(p.dev_err, HSA_DEVERR_BAD_RING);
+            return;
+        }
+    }
+    for (int e = tid; e < total; e += nthreads) {
+        const int kv = e / (p.T * kChunks);
+        const int t = (e / kChunks) % p.T;
+        const int ch = e % kChunks;
+        const int64_t pos = (int64_t)c + t;
+        int64_t dst_row;
+        if (ring) {
+            dst_row = ((int64_t)rr * p.Hkv + h) * p.W + pos % p.W;
+        } else {
+            const int64_t page = pos / kTileKeys;
+            if (page >= p.max_blocks) {
+                set_err(p.dev_err, HSA_DEVERR_BAD_PAGE);
+                continue;
+            }
+            const int blk = __ldg(p.block_tables + (int64_t)b * p.max_blocks + page);
+            if (blk < 0 || blk >= p.num_blocks) {
+                set_err(p.dev_err, HSA_DEVERR_BAD_BLOCK);
+                continue;
+            }
+            dst_row = ((int64_t)blk * p.Hkv + h) * kTileKeys + pos % kTileKeys;
+        }
+        const int64_t src = ((int64_t)(b * p.T + t) * p.Hkv + h) * kChunks + ch;
+        const uint4 *from = reinterpret_cast<const uint4 *>(kv ? p.v_new : p.k_new);
+        uint4 *to = kv ? p.v_dst : p.k_dst;
+        to[dst_row * kChunks + ch] = __ldg(from + src);
+    }
+}
+
 template <int MT>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -250,6 +302,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
 
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&sh.full[s], 1);
+            mbar_init(&sh.empty[s], kConsumerWarps);
+        }
+        fence_barrier_init();
+    }
+    if (warp == kConsumerWarps && lane == 0) {
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+    }
+    // Everything above touches no global memory that an earlier kernel writes.
+    grid_dependency_wait();
+    grid_launch_dependents();
+
     // ---- locate this CTA's contiguous range of items ------------------------
     {
         const int per = (p.B + kThreads - 1) / kThreads;
@@ -258,22 +325,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int b = b_lo; b < b_hi; ++b)
             local += items_of(p, b);
         sh.scan[tid] = local;
-        if (tid == 0) {
-            for (int s = 0; s < kStages; ++s) {
-                mbar_init(&sh.full[s], 1);
-                mbar_init(&sh.empty[s], kConsumerWarps);
-            }
-            fence_barrier_init();
-        }
         __syncthreads();
-        if (tid == 0) {
-            int acc = 0;
-            for (int i = 0; i < kThreads; ++i) {
-                int v = sh.scan[i];
-                sh.scan[i] = acc;
-                acc += v;
+        if (warp == 0) {
+            // exclusive scan of kThreads entries: kThreads / 32 consecutive entries per lane
+            constexpr int kPer = kThreads / 32;
+            int v[kPer];
+            int sum = 0;
+#pragma unroll
+            for (int j = 0; j < kPer; ++j) {
+                v[j] = sh.scan[lane * kPer + j];
+                sum += v[j];
             }
-            sh.total_items = acc;
+            int incl = sum;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int u = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o)
+                    incl += u;
+            }
+            int acc = incl - sum;
+#pragma unroll
+            for (int j = 0; j < kPer; ++j) {
+                sh.scan[lane * kPer + j] = acc;
+                acc += v[j];
+            }
+            if (lane == 31)
+                sh.total_items = incl;
         }
         __syncthreads();
     }
@@ -311,11 +388,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kConsumerWarps) {
         // ---------------------------------------------------------------- producer
         if (lane == 0) {
-            tma_prefetch_desc(&tmK);
-            tma_prefetch_desc(&tmV);
             const uint64_t pol = policy_evict_first();
             Walk w = w0;
-            for (int64_t i = i0, k = 0; i < i1; ++i, ++k) {
+            int64_t k = 0;
+            for (int64_t i = i0; i < i1; ++i, ++k) {
                 const int st = (int)(k % kStages);
                 const uint32_t ph = (uint32_t)((k / kStages) & 1);
                 if (!mbar_wait(&sh.empty[st], ph ^ 1)) {
@@ -336,6 +412,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 walk_next(p, w);
             }
+            // drain: no TMA write may still be in flight when the CTA exits
+            for (int64_t s = 0; s < kStages && s < k; ++s) {
+                const int64_t last = s + ((k - 1 - s) / kStages) * kStages;
+                mbar_wait(&sh.full[s], (uint32_t)((last / kStages) & 1));
+            }
         }
         return;
     }
@@ -349,6 +430,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r0 = mt * 16 + g, r1 = r0 + 8;
     const int t0 = r0 / p.G, t1 = r1 / p.G;
     const int rows_valid = p.G * p.T;
+    const int Hq = p.G * p.Hkv;
+    int32_t *const ws_cnt = reinterpret_cast<int32_t *>(p.ws);
+    float *const ws_part = reinterpret_cast<float *>(p.ws + decode_counter_bytes(p.B, p.Hkv));
 
     RowState st;
     uint32_t qa[kD / 16][4];
@@ -366,9 +450,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int n = 0; n < kD / 8; ++n)
                 st.o[n][0] = st.o[n][1] = st.o[n][2] = st.o[n][3] = 0.f;
             const __nv_bfloat16 *q0 =
-                p.q + ((int64_t)(w.b * p.T + t0) * p.Hq + w.h * p.G + r0 % p.G) * kD;
+                p.q + ((int64_t)(w.b * p.T + t0) * Hq + w.h * p.G + r0 % p.G) * kD;
             const __nv_bfloat16 *q1 =
-                p.q + ((int64_t)(w.b * p.T + t1) * p.Hq + w.h * p.G + r1 % p.G) * kD;
+                p.q + ((int64_t)(w.b * p.T + t1) * Hq + w.h * p.G + r1 % p.G) * kD;
             const bool v0 = t0 < p.T, v1 = t1 < p.T;
 #pragma unroll
             for (int ks = 0; ks < kD / 16; ++ks) {
@@ -377,6 +461,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 qa[ks][1] = v1 ? __ldg(reinterpret_cast<const uint32_t *>(q1 + c0)) : 0u;
                 qa[ks][2] = v0 ? __ldg(reinterpret_cast<const uint32_t *>(q0 + c0 + 8)) : 0u;
                 qa[ks][3] = v1 ? __ldg(reinterpret_cast<const uint32_t *>(q1 + c0 + 8)) : 0u;
+            }
+            // stage this unit's new tokens now when this CTA owns the unit's last
+            // tile; rows >= T are zero
+            if (unit_start + w.n <= i1) {
+                for (int e = tid; e < kNewRows * kD / 8; e += kConsumerWarps * 32) {
+                    const int rr = e / (kD / 8), col = (e % (kD / 8)) * 8;
+                    uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
+                    if (rr < p.T) {
+                        const int64_t src =
+                            ((int64_t)(w.b * p.T + rr) * p.Hkv + w.h) * kD + col;
+                        kv = __ldg(reinterpret_cast<const uint4 *>(p.k_new + src));
+                        vv = __ldg(reinterpret_cast<const uint4 *>(p.v_new + src));
+                    }
+                    *reinterpret_cast<uint4 *>(sh.new_k + swz128_offset(rr, col, kNewRows)) = kv;
+                    *reinterpret_cast<uint4 *>(sh.new_v + swz128_offset(rr, col, kNewRows)) = vv;
+                }
             }
         }
         const int stg = (int)(k % kStages);
@@ -389,13 +489,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int c = w.c;
         const int j = w.j;
         bool any = loaded;
-        if (loaded && !p.ring_mode)
+        if (loaded && !(p.flags & kDecodeRing))
             any = key0 < c - j * kTileKeys;  // this warp's keys hold a cached position
         if (any) {
             const uint32_t sK = smem_u32(sh.stage[stg]);
             const uint32_t sV = sK + kTileBytes;
             const int W = p.W, T = p.T;
-            const bool ring = p.ring_mode != 0;
+            const bool ring = (p.flags & kDecodeRing) != 0;
             auto vis = [&](int rr, int key) -> bool {
                 const int t = rr == g ? t0 : t1;
                 if (t >= T)
@@ -420,19 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---- end of this CTA's share of unit (cur.b, cur.h) ------------------
         const int64_t unit_end = unit_start + cur.n;  // one past its last item
         if (unit_last_tile) {
-            // new tokens: positions c .. c+T-1, causal among themselves
-            named_bar_sync(1, kConsumerWarps * 32);
-            for (int e = tid; e < kNewRows * kD / 8; e += kConsumerWarps * 32) {
-                const int rr = e / (kD / 8), col = (e % (kD / 8)) * 8;
-                uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
-                if (rr < p.T) {
-                    const int64_t src = ((int64_t)(cur.b * p.T + rr) * p.Hkv + cur.h) * kD + col;
-                    kv = __ldg(reinterpret_cast<const uint4 *>(p.k_new + src));
-                    vv = __ldg(reinterpret_cast<const uint4 *>(p.v_new + src));
-                }
-                *reinterpret_cast<uint4 *>(sh.new_k + swz128_offset(rr, col, kNewRows)) = kv;
-                *reinterpret_cast<uint4 *>(sh.new_v + swz128_offset(rr, col, kNewRows)) = vv;
-            }
+            // new tokens (staged at unit start): positions c .. c+T-1, causal
             named_bar_sync(1, kConsumerWarps * 32);
             if (slice == 0) {
                 const int T = p.T;
@@ -475,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!whole)
             slot = 2 * (int)blockIdx.x + (i0 < unit_start ? 1 : 0);  // 1 = CTA's last unit
         constexpr int kSlices = kConsumerWarps / MT;
-        float *part = p.ws_part + (int64_t)(slot < 0 ? 0 : slot) * kPartFloats;
+        float *part = ws_part + (int64_t)(slot < 0 ? 0 : slot) * kPartFloats;
         for (int e = tid; e < MT * 16 * kD; e += kConsumerWarps * 32) {
             const int rr = e / kD, dim = e % kD;
             const int m_t = rr / 16, rl = rr % 16;
@@ -497,7 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (whole) {
                 const int t = rr / p.G, hh = rr % p.G;
                 const float val = L > 0.f ? O / L : 0.f;
-                p.out[((int64_t)(cur.b * p.T + t) * p.Hq + cur.h * p.G + hh) * kD + dim] =
+                p.out[((int64_t)(cur.b * p.T + t) * Hq + cur.h * p.G + hh) * kD + dim] =
                     __float2bfloat16_rn(val);
             } else {
                 if (dim == 0) {
@@ -507,6 +595,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __stcg(part + 2 * kMaxRows + rr * kD + dim, O);
             }
         }
+        if (whole && (p.flags & kDecodeAppend))
+            append_unit(p, cur.b, cur.h, cur.c, tid, kConsumerWarps * 32);
         if (!whole) {
             // count this part in; the last CTA of the unit merges every part
             const int unit = cur.b * p.Hkv + cur.h;
@@ -515,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             named_bar_sync(1, kConsumerWarps * 32);
             if (tid == 0) {
                 __threadfence();
-                const int prev = atomicAdd(p.ws_cnt + unit, 1);
+                const int prev = atomicAdd(ws_cnt + unit, 1);
                 sh.is_last = (prev == (int)(c_hi - c_lo));
             }
             named_bar_sync(1, kConsumerWarps * 32);
@@ -527,24 +617,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int64_t cc = c_lo; cc <= c_hi; ++cc) {
                         const int64_t start_cc = cc * N / C;
                         const int sl = 2 * (int)cc + (start_cc < unit_start ? 1 : 0);
-                        M = fmaxf(M, __ldcg(p.ws_part + (int64_t)sl * kPartFloats + rr));
+                        M = fmaxf(M, __ldcg(ws_part + (int64_t)sl * kPartFloats + rr));
                     }
                     const float base = M == -INFINITY ? 0.f : M;
                     float L = 0.f, O = 0.f;
                     for (int64_t cc = c_lo; cc <= c_hi; ++cc) {
                         const int64_t start_cc = cc * N / C;
                         const int sl = 2 * (int)cc + (start_cc < unit_start ? 1 : 0);
-                        const float *pp = p.ws_part + (int64_t)sl * kPartFloats;
+                        const float *pp = ws_part + (int64_t)sl * kPartFloats;
                         const float a = fast_exp2(__ldcg(pp + rr) - base);
                         L += __ldcg(pp + kMaxRows + rr) * a;
                         O += __ldcg(pp + 2 * kMaxRows + rr * kD + dim) * a;
                     }
                     const int t = rr / p.G, hh = rr % p.G;
-                    p.out[((int64_t)(cur.b * p.T + t) * p.Hq + cur.h * p.G + hh) * kD + dim] =
+                    p.out[((int64_t)(cur.b * p.T + t) * Hq + cur.h * p.G + hh) * kD + dim] =
                         __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
                 }
+                if (p.flags & kDecodeAppend)
+                    append_unit(p, cur.b, cur.h, cur.c, tid, kConsumerWarps * 32);
                 if (tid == 0)
-                    p.ws_cnt[unit] = 0;
+                    ws_cnt[unit] = 0;
             }
         }
         named_bar_sync(1, kConsumerWarps * 32);  // comb / new-token buffers free again
@@ -557,17 +649,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 size_t decode_workspace_bytes(int num_sms, int B, int Hkv)
 {
-    size_t cnt = ((size_t)B * Hkv * sizeof(int32_t) + 255) & ~size_t(255);
+    size_t cnt = decode_counter_bytes(B, Hkv);
     size_t part = (size_t)2 * num_sms * kPartFloats * sizeof(float);
     return cnt + part;
 }
 
-size_t decode_smem_bytes() { return sizeof(SharedStorage) + 1024; }
-
 cudaError_t launch_decode(const CUtensorMap &tmK, const CUtensorMap &tmV, const DecodeParams &p,
                           int ctas, cudaStream_t stream)
 {
-    const size_t smem = decode_smem_bytes();
+    const size_t smem = sizeof(SharedStorage) + 1024;
     const int MT = (p.G * p.T + 15) / 16;
     // the opt-in shared-memory size is set once per process (the API is not a stream
     // operation, but setting it once keeps graph capture free of extra calls)
@@ -582,8 +672,17 @@ cudaError_t launch_decode(const CUtensorMap &tmK, const CUtensorMap &tmV, const 
             return e;
         attr_set[MT - 1] = true;
     }
-    kern<<<ctas, kThreads, smem, stream>>>(tmK, tmV, p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)ctas);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, tmK, tmV, p);
 }
 
 }  // namespace hsa

@@ -77,7 +77,7 @@ extern "C" hsa_status hsa_decode_attn_noalloc(const hsa_pools *pools, int32_t la
     if (scratch_address(&scratch) != cudaSuccess)
         return HSA_CUDA_ERROR;
     // the counters must start at zero; the array keeps whatever the last call left
-    const size_t cnt_bytes = ((size_t)B * pools->Hkv * sizeof(int32_t) + 255) & ~size_t(255);
+    const size_t cnt_bytes = hsa::decode_counter_bytes(B, pools->Hkv);
     if (cudaMemsetAsync(scratch, 0, cnt_bytes, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return HSA_CUDA_ERROR;
     return hsa_decode_attn(pools, layer, q, k_new, v_new, cached_len, B, T, scale, out, scratch,

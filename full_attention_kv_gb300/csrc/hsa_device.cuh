@@ -132,6 +132,20 @@ __device__ __forceinline__ uint64_t policy_evict_last()
     return p;
 }
 
+// ---------------------------------------------------------------- dependent launch
+// Programmatic dependent launch: wait until the previous kernel in the stream has
+// completed and its writes are visible (a no-op for a normal launch), and allow
+// the next kernel to be scheduled once every CTA of this grid has said so.
+__device__ __forceinline__ void grid_dependency_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- named barriers
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t threads)
 {

@@ -13,27 +13,38 @@ struct __nv_bfloat16;
 
 namespace hsa {
 
+// The decode parameter struct is passed by value and kept at <= 128 bytes: on
+// sm_103a the decode kernel measured 19% slower with the same code when this
+// struct grew from 128 to 136 bytes (a different code generation of the hot loop).
 struct DecodeParams {
     const __nv_bfloat16 *q;      // [B, T, Hq, d]
     const __nv_bfloat16 *k_new;  // [B, T, Hkv, d]
     const __nv_bfloat16 *v_new;
     const int32_t *cached_len;   // [B]
     const int32_t *block_tables; // [batch, max_blocks]
-    int32_t max_blocks;
-    int32_t num_blocks;
     const int32_t *ring_row;     // [batch]
-    int32_t n_ring_rows;
     __nv_bfloat16 *out;          // [B, T, Hq, d]
-    float *ws_part;              // partial softmax states, 2 slots per CTA
-    int32_t *ws_cnt;             // per (sequence, KV head) arrival counters
+    uint8_t *ws;                 // workspace: arrival counters, then partial softmax states
     int32_t *dev_err;
-    int32_t B, T, Hq, Hkv, G, W;
-    int32_t ring_mode;           // 0: Full KV Pool pages, 1: SWA ring
+    uint4 *k_dst;                // this layer's K pool / ring (append only)
+    uint4 *v_dst;
+    int32_t max_blocks, num_blocks, n_ring_rows;
+    int32_t B, Hkv, W;
+    int16_t T, G;                // query tokens per sequence; query heads per KV head
+    int32_t flags;               // kDecodeRing | kDecodeAppend
     float scale_log2;            // softmax scale * log2(e)
 };
+constexpr int32_t kDecodeRing = 1;    // sliding layer: read the SWA ring
+constexpr int32_t kDecodeAppend = 2;  // append the T new rows (hsa_decode_attn_append)
+static_assert(sizeof(DecodeParams) <= 128, "keep the decode parameter struct <= 128 bytes");
+
+// Bytes of the arrival-counter region at the start of a decode workspace.
+__host__ __device__ inline size_t decode_counter_bytes(int B, int Hkv)
+{
+    return ((size_t)B * Hkv * sizeof(int32_t) + 255) & ~size_t(255);
+}
 
 size_t decode_workspace_bytes(int num_sms, int B, int Hkv);
-size_t decode_smem_bytes();
 cudaError_t launch_decode(const CUtensorMap &tmK, const CUtensorMap &tmV, const DecodeParams &p,
                           int ctas, cudaStream_t stream);
 
@@ -55,6 +66,8 @@ struct AppendParams {
 
 cudaError_t launch_append(const AppendParams &p, cudaStream_t stream);
 
+// Prefill keeps its larger by-value struct: promoted into registers (<= 128
+// bytes) it raised the prefill kernel's spills from 76 to 252 bytes.
 struct PrefillParams {
     const __nv_bfloat16 *q;      // [rows, Hq, d]
     const __nv_bfloat16 *k_new;  // [rows, Hkv, d]

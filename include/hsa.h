@@ -131,6 +131,23 @@ hsa_status hsa_decode_attn(const hsa_pools *pools, int32_t layer, const void *q,
                            size_t ws_bytes, int32_t max_ctas, int32_t *dev_err, void *stream);
 
 /*
+ * Decode attention fused with the append of the step's new tokens (the usual
+ * decode step: attend, then keep the new K/V).  Same arguments and outputs as
+ * hsa_decode_attn; in addition the T new rows of every sequence are written to
+ * this layer's pool at positions cached_len[b] + t (Full KV Pool page through the
+ * block table, or ring slot (cached_len[b] + t) mod W), exactly what hsa_kv_append
+ * with one request per sequence would write.  Each (sequence, KV head) is appended
+ * by the CTA that finishes its attention, after every read of it, so T > 1 on a
+ * sliding layer is safe.  For MTP verify where only some drafts are accepted, use
+ * hsa_decode_attn and then hsa_kv_append with the accepted tokens instead.
+ */
+hsa_status hsa_decode_attn_append(const hsa_pools *pools, int32_t layer, const void *q,
+                                  const void *k_new, const void *v_new,
+                                  const int32_t *cached_len, int32_t B, int32_t T, float scale,
+                                  void *out, void *workspace, size_t ws_bytes, int32_t max_ctas,
+                                  int32_t *dev_err, void *stream);
+
+/*
  * hsa_decode_attn without a caller workspace.  The pages have no counterpart: this
  * is a convenience of this library for callers that cannot allocate device memory
  * where they run decode (while a stream is being captured, inside a host runtime

@@ -226,3 +226,38 @@ def test_window_safe_len_small_windows(W):
                                            torch.from_numpy(off).cuda(),
                                            torch.from_numpy(live).cuda(), W)
     assert np.array_equal(got_b.cpu().numpy(), oracle.window_safe_len_bitmap(bm_len, off, live, W))
+
+
+@pytest.mark.parametrize("T", [1, 4])
+@pytest.mark.parametrize("max_ctas", [0, 3])
+def test_fused_append_matches_attention_then_append(T, max_ctas):
+    """hsa_decode_attn_append = hsa_decode_attn + appending the T new rows.
+
+    max_ctas=3 splits units across CTAs, so the append of a ring whose unit is
+    split is done by the last CTA to finish it (T = 4 would clobber live slots
+    if any CTA were still reading)."""
+    hsa = _cuda()
+    cfg = dataclasses.replace(workload.CONFIGS["tiny"], Hq=32, Hkv=4, T=T,
+                              contexts=(0, 1, 63, 130, 700, 5000), B=6, index=70 + T)
+    inst = workload.draw(cfg)
+    layers = [6, 0]
+    pool = harness.make_pool(inst, layers)
+    for i, l in enumerate(layers):
+        q, k, v, cl = harness.decode_inputs(inst, l)
+        ref = hsa.hsa_decode_attn(pool, i, q, k, v, cl, cfg.scale, max_ctas=max_ctas)
+        ek, ev = _bits(pool.k[i]).copy(), _bits(pool.v[i]).copy()
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        out = hsa.hsa_decode_attn_append(pool, i, q, k, v, cl, cfg.scale, max_ctas=max_ctas,
+                                         dev_err=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        assert torch.equal(out, ref)
+        kw = dict(block_tables=inst.block_tables) if inst.full[l] else dict(ring_row=inst.ring_row)
+        B = inst.R
+        oracle.append(ek, ev, np.arange(0, B * T + 1, T), np.arange(B), inst.prefix,
+                      k.view(B * T, cfg.Hkv, cfg.d), v.view(B * T, cfg.Hkv, cfg.d), **kw)
+        assert np.array_equal(_bits(pool.k[i]), ek) and np.array_equal(_bits(pool.v[i]), ev)
+        # and the attention it computed is the oracle's
+        c = harness.oracle_case(inst, l, range(B))
+        refo = oracle.attention(window=0 if inst.full[l] else cfg.W, scale=cfg.scale, **c)
+        assert np.max(np.abs(out.float().cpu().numpy().reshape(refo.shape) - refo)) <= TOL
