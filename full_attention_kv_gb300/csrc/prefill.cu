@@ -315,18 +315,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
-            float x[kBN];
-            {
-                uint32_t r32[32];
-#pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) {
-                    tmem_ld32(lane_addr + s * 128 + c4 * 32, r32);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int c = 0; c < 32; ++c)
-                        x[c4 * 32 + c] = __uint_as_float(r32[c]);
-                }
-            }
             // ---- visibility of the 128 keys of tile n for query row i ----------
             int lo = 0, hi = 0;
             bool ok0 = true, ok1 = true, ring = false;
@@ -348,34 +336,44 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!row_ok)
                 hi = 0;
-            float mx = -INFINITY;
-            if (ring) {
-                // slot t holds the latest prefix position below P congruent to t mod W
-                const int lo_pos = max(0, P + i - p.W + 1);
-#pragma unroll
-                for (int c = 0; c < kBN; ++c) {
-                    const int slot = n * kBN + c;
+            const bool whole_tile = !ring && lo == 0 && hi == kBN && ok0 && ok1;
+            // ring slot t holds the latest prefix position below P congruent to t mod W
+            const int lo_pos = max(0, P + i - p.W + 1);
+            auto vis = [&](int key) -> bool {
+                if (ring) {
+                    const int slot = n * kBN + key;
                     int back = (P - 1 - slot) % p.W;
                     back += back < 0 ? p.W : 0;
-                    const int pos = P - 1 - back;
-                    const bool vis = row_ok && ring_row_ok && slot < p.W && pos >= lo_pos;
-                    x[c] = vis ? x[c] * p.scale_log2 : -INFINITY;
-                    mx = fmaxf(mx, x[c]);
+                    return row_ok && ring_row_ok && slot < p.W && P - 1 - back >= lo_pos;
                 }
-            } else if (lo == 0 && hi == kBN && ok0 && ok1) {
+                return key >= lo && key < hi && (key < 64 ? ok0 : ok1);
+            };
+            // ---- pass 1: raw-score row max (four loads in flight, four max chains) --
+            float mx = -INFINITY;
+            {
+                uint32_t r32[4][32];
 #pragma unroll
-                for (int c = 0; c < kBN; ++c) {
-                    x[c] *= p.scale_log2;
-                    mx = fmaxf(mx, x[c]);
-                }
-            } else {
+                for (int c4 = 0; c4 < 4; ++c4)
+                    tmem_ld32(lane_addr + s * 128 + c4 * 32, r32[c4]);
+                tmem_wait_ld();
+                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                if (whole_tile) {
 #pragma unroll
-                for (int c = 0; c < kBN; ++c) {
-                    const bool vis = c >= lo && c < hi && (c < 64 ? ok0 : ok1);
-                    x[c] = vis ? x[c] * p.scale_log2 : -INFINITY;
-                    mx = fmaxf(mx, x[c]);
+                    for (int c4 = 0; c4 < 4; ++c4)
+#pragma unroll
+                        for (int c = 0; c < 32; ++c)
+                            m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(r32[c4][c]));
+                } else {
+#pragma unroll
+                    for (int c4 = 0; c4 < 4; ++c4)
+#pragma unroll
+                        for (int c = 0; c < 32; ++c)
+                            if (vis(c4 * 32 + c))
+                                m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(r32[c4][c]));
                 }
+                mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
             }
+            mx *= p.scale_log2;  // the scale is positive
             // ---- running max, lazily raised; O rescaled in TMEM when it moves ------
             float m_new = m_used;
             if (mx != -INFINITY && (m_used == -INFINITY || mx > m_used + kRescaleSlack))
@@ -390,9 +388,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 const float alpha = resc ? fast_exp2(m_used - m_new) : 1.0f;
-                uint32_t o32[32];
-#pragma unroll
+#pragma unroll 1
                 for (int c4 = 0; c4 < 4; ++c4) {
+                    uint32_t o32[32];
                     tmem_ld32(lane_addr + kColO + c4 * 32, o32);
                     tmem_wait_ld();
 #pragma unroll
@@ -405,19 +403,42 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             m_used = m_new;
             const float base = m_used == -INFINITY ? 0.f : m_used;
-            float sum = 0.f;
-            uint32_t pk[32];
+            // ---- pass 2: P = 2^(s scale log2e - m) as bf16 pairs into TMEM --------------
+            // chunks are handled two at a time; chunk c4's 16 P columns land on S
+            // columns 16 c4 .. 16 c4 + 15, which pass 2 has already read
+            float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+            for (int c8 = 0; c8 < 4; c8 += 2) {
+                uint32_t r32[2][32];
+                tmem_ld32(lane_addr + s * 128 + c8 * 32, r32[0]);
+                tmem_ld32(lane_addr + s * 128 + (c8 + 1) * 32, r32[1]);
+                tmem_wait_ld();
+                uint32_t pk[2][16];
 #pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    if (whole_tile) {
 #pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    const float p0 = fast_exp2(x[h2 * 64 + 2 * c] - base);
-                    const float p1 = fast_exp2(x[h2 * 64 + 2 * c + 1] - base);
-                    sum += p0 + p1;
-                    pk[c] = pack_bf16(p0, p1);
+                        for (int c = 0; c < 16; ++c) {
+                            const float p0 = fast_exp2(fmaf(__uint_as_float(r32[h2][2 * c]), p.scale_log2, -base));
+                            const float p1 = fast_exp2(fmaf(__uint_as_float(r32[h2][2 * c + 1]), p.scale_log2, -base));
+                            sum4[c & 3] += p0 + p1;
+                            pk[h2][c] = pack_bf16(p0, p1);
+                        }
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) {
+                            const int k0 = (c8 + h2) * 32 + 2 * c;
+                            const float p0 = vis(k0) ? fast_exp2(fmaf(__uint_as_float(r32[h2][2 * c]), p.scale_log2, -base)) : 0.f;
+                            const float p1 = vis(k0 + 1) ? fast_exp2(fmaf(__uint_as_float(r32[h2][2 * c + 1]), p.scale_log2, -base)) : 0.f;
+                            sum4[c & 3] += p0 + p1;
+                            pk[h2][c] = pack_bf16(p0, p1);
+                        }
+                    }
                 }
-                tmem_st32(lane_addr + s * 128 + h2 * 32, pk);
+                tmem_st16(lane_addr + s * 128 + c8 * 16, pk[0]);
+                tmem_st16(lane_addr + s * 128 + (c8 + 1) * 16, pk[1]);
             }
+            const float sum = (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
             l += sum;
             tmem_wait_st();
             tc_fence_before();
