@@ -126,10 +126,11 @@ def barrier(ws):
         torch.distributed.barrier()
 
 
-def max_over_ranks(x, ws):
+def max_over_ranks(x, ws, device="cuda"):
+    """Slowest rank's value (timings are taken as the max over ranks)."""
     if ws == 1:
         return x
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    t = torch.tensor([x], dtype=torch.float64, device=device)
     torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
     return float(t.item())
 
@@ -547,8 +548,10 @@ def _ctx_desc(cfg):
 # workload and the source digest of the kernel it was taken on (None = not taken
 # on the current kernel).
 TRAFFIC = {
-    # profiles/decode_full_ncu_decode-b4.md: 389.6 MB on 4 sequences, scaled by units
-    "decode": ("716d087b6c293e7c", 2832703286),
+    # profiles/decode_full_ncu_decode-b4.md: 389.5 MB on 4 sequences, scaled by units
+    "decode": ("c30f7c331a4ae7f6", 2832277051),
+    # profiles/prefill_full_ncu_prefill-r2.md: 5.846 GB on 2 requests, scaled by flops
+    "prefill": ("86e2430f370d57d3", 18418300622),
 }
 
 
@@ -581,7 +584,7 @@ def main():
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     ws, rank, local = dist_env()
-    cfg = workload.CONFIGS[args.workload]
+    cfg = workload.shard(workload.CONFIGS[args.workload], rank)
     inst = workload.draw(cfg, R=args.batch)
 
     if args.impl == "reference":

@@ -19,7 +19,7 @@ sample can be regenerated on its own.
 """
 import math
 import random
-from dataclasses import dataclass, field
+from dataclasses import dataclass, field, replace
 from typing import List, Optional
 
 import numpy as np
@@ -158,6 +158,15 @@ def draw(cfg: Config, *, R: Optional[int] = None, rng_seed: Optional[int] = None
     return Instance(cfg, np.array(prefix, np.int32), np.array(new, np.int32), cu, bt,
                     max(total, 1), np.array(rows, np.int32), max(n, 1),
                     layer_is_full(cfg.n_layers))
+
+
+def shard(cfg: Config, rank: int) -> Config:
+    """Rank `rank`'s share of a data-parallel global batch: rank 0 draws exactly the
+    single-GPU workload; every other rank draws its own seeded batch of the same
+    shape (sequences are independent, so ranks never exchange data)."""
+    if rank == 0:
+        return cfg
+    return replace(cfg, index=cfg.index + 1000 * rank)
 
 
 def _seed(cfg: Config, *parts: int) -> int:
