@@ -150,13 +150,21 @@ struct RowState {
     float l[2];
 };
 
+// Running max may lag the true one by up to this much (log2 units) before O is
+// rescaled: P then stays below 2^8, exact enough in bf16, and most tiles skip the
+// 64-register rescale of O.
+constexpr float kRescaleSlack = 8.0f;
+
 // One key tile on tensor cores.  NT = n-tiles of 8 keys this warp owns inside the
 // tile (keys key0 .. key0 + 8 NT - 1), rows = the tile's row count in shared
-// memory (for the swizzle), vis(row, key) = key visible to that query row.
+// memory (for the swizzle), vis(row, key) = key visible to that query row; when
+// all_vis is set every key of the tile is visible to every valid row and only rows
+// past G T (padding) are masked.
 template <int NT, typename Vis>
 __device__ __forceinline__ void run_tile(RowState &st, const uint32_t (&qa)[kD / 16][4],
                                          uint32_t sK, uint32_t sV, int tile_rows, int key0,
-                                         float scale_log2, Vis vis)
+                                         float scale_log2, bool all_vis, bool row0_ok,
+                                         bool row1_ok, Vis vis)
 {
     const int lane = threadIdx.x & 31;
     const int g = lane >> 2, tq = lane & 3;
@@ -182,51 +190,75 @@ __device__ __forceinline__ void run_tile(RowState &st, const uint32_t (&qa)[kD /
         }
     }
 
-    // mask + online softmax (base-2, scale folded in)
+    // mask (raw scores; the scale is positive and folded into the exponent below)
+    if (!all_vis) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int key = key0 + nt * 8 + 2 * tq + e;
+                if (!vis(g, key))
+                    s[nt][e] = -INFINITY;
+                if (!vis(g + 8, key))
+                    s[nt][2 + e] = -INFINITY;
+            }
+        }
+    } else {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            if (!row0_ok)
+                s[nt][0] = s[nt][1] = -INFINITY;
+            if (!row1_ok)
+                s[nt][2] = s[nt][3] = -INFINITY;
+        }
+    }
     float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int key = key0 + nt * 8 + 2 * tq + e;
-            s[nt][e] = vis(g, key) ? s[nt][e] * scale_log2 : -INFINITY;
-            s[nt][2 + e] = vis(g + 8, key) ? s[nt][2 + e] * scale_log2 : -INFINITY;
-            mx0 = fmaxf(mx0, s[nt][e]);
-            mx1 = fmaxf(mx1, s[nt][2 + e]);
-        }
+        mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
+        mx1 = fmaxf(mx1, fmaxf(s[nt][2], s[nt][3]));
     }
     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-    const float mn0 = fmaxf(st.m[0], mx0), mn1 = fmaxf(st.m[1], mx1);
-    const float base0 = mn0 == -INFINITY ? 0.f : mn0;
-    const float base1 = mn1 == -INFINITY ? 0.f : mn1;
-    const float a0 = fast_exp2(st.m[0] - base0), a1 = fast_exp2(st.m[1] - base1);
-    st.m[0] = mn0;
-    st.m[1] = mn1;
-    float sum0 = 0.f, sum1 = 0.f;
+    mx0 *= scale_log2;
+    mx1 *= scale_log2;
+    // running max, raised lazily (the quad shares a row, so its decision is uniform)
+    const bool up0 = mx0 != -INFINITY && (st.m[0] == -INFINITY || mx0 > st.m[0] + kRescaleSlack);
+    const bool up1 = mx1 != -INFINITY && (st.m[1] == -INFINITY || mx1 > st.m[1] + kRescaleSlack);
+    if (__any_sync(0xffffffffu, up0 || up1)) {
+        const float a0 = up0 ? fast_exp2(st.m[0] - mx0) : 1.f;  // m = -inf: O is still 0
+        const float a1 = up1 ? fast_exp2(st.m[1] - mx1) : 1.f;
+        if (up0)
+            st.m[0] = mx0;
+        if (up1)
+            st.m[1] = mx1;
+        st.l[0] *= a0;
+        st.l[1] *= a1;
+#pragma unroll
+        for (int n = 0; n < kD / 8; ++n) {
+            st.o[n][0] *= a0;
+            st.o[n][1] *= a0;
+            st.o[n][2] *= a1;
+            st.o[n][3] *= a1;
+        }
+    }
+    const float base0 = st.m[0] == -INFINITY ? 0.f : st.m[0];
+    const float base1 = st.m[1] == -INFINITY ? 0.f : st.m[1];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-        s[nt][0] = fast_exp2(s[nt][0] - base0);
-        s[nt][1] = fast_exp2(s[nt][1] - base0);
-        s[nt][2] = fast_exp2(s[nt][2] - base1);
-        s[nt][3] = fast_exp2(s[nt][3] - base1);
-        sum0 += s[nt][0] + s[nt][1];
-        sum1 += s[nt][2] + s[nt][3];
-    }
-    st.l[0] = st.l[0] * a0 + sum0;
-    st.l[1] = st.l[1] * a1 + sum1;
-#pragma unroll
-    for (int n = 0; n < kD / 8; ++n) {
-        st.o[n][0] *= a0;
-        st.o[n][1] *= a0;
-        st.o[n][2] *= a1;
-        st.o[n][3] *= a1;
+        s[nt][0] = fast_exp2(fmaf(s[nt][0], scale_log2, -base0));
+        s[nt][1] = fast_exp2(fmaf(s[nt][1], scale_log2, -base0));
+        s[nt][2] = fast_exp2(fmaf(s[nt][2], scale_log2, -base1));
+        s[nt][3] = fast_exp2(fmaf(s[nt][3], scale_log2, -base1));
     }
 
-    // O += P V: P from the S accumulators, V fragments via ldmatrix.trans
+    // O += P V: P from the S accumulators, V fragments via ldmatrix.trans.  The row
+    // sums take the same bf16-rounded P the MMA uses, so O / l is an exact convex
+    // combination of V rows (no scale error proportional to |O|).
     const int mi = lane >> 3, r = lane & 7;
+    float sum0 = 0.f, sum1 = 0.f;
 #pragma unroll
     for (int ks = 0; ks < NT / 2; ++ks) {
         uint32_t pa[4];
@@ -234,6 +266,8 @@ __device__ __forceinline__ void run_tile(RowState &st, const uint32_t (&qa)[kD /
         pa[1] = pack_bf16(s[2 * ks][2], s[2 * ks][3]);
         pa[2] = pack_bf16(s[2 * ks + 1][0], s[2 * ks + 1][1]);
         pa[3] = pack_bf16(s[2 * ks + 1][2], s[2 * ks + 1][3]);
+        sum0 += bf16_lo(pa[0]) + bf16_hi(pa[0]) + bf16_lo(pa[2]) + bf16_hi(pa[2]);
+        sum1 += bf16_lo(pa[1]) + bf16_hi(pa[1]) + bf16_lo(pa[3]) + bf16_hi(pa[3]);
         const int key = key0 + ks * 16 + (mi & 1) * 8 + r;
 #pragma unroll
         for (int np = 0; np < kD / 16; ++np) {
@@ -244,6 +278,8 @@ __device__ __forceinline__ void run_tile(RowState &st, const uint32_t (&qa)[kD /
             mma_bf16_16816(st.o[2 * np + 1], pa, b2, b3);
         }
     }
+    st.l[0] += sum0;
+    st.l[1] += sum1;
 }
 
 // Append the T new K/V rows of unit (b, h) to this layer's pool or ring.  Called by
@@ -505,7 +541,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     return false;
                 return !ring || pos >= c + t - W + 1;
             };
-            run_tile<2 * MT>(st, qa, sK, sV, kTileKeys, key0, p.scale_log2, vis);
+            // full layers: every key of a complete page is visible to every query
+            const bool all_vis = !ring && (j + 1) * kTileKeys <= c;
+            run_tile<2 * MT>(st, qa, sK, sV, kTileKeys, key0, p.scale_log2, all_vis, t0 < T,
+                             t1 < T, vis);
         }
         __syncwarp();
         if (lane == 0)
@@ -529,7 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     return t < T && key <= t;
                 };
                 run_tile<2>(st, qa, smem_u32(sh.new_k), smem_u32(sh.new_v), kNewRows, 0,
-                            p.scale_log2, vis_new);
+                            p.scale_log2, false, t0 < T, t1 < T, vis_new);
             }
         }
 

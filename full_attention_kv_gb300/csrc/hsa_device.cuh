@@ -186,6 +186,10 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// The two bf16 halves of a packed pair, widened exactly to fp32.
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
 // 2^x on the SFU (PTX ex2.approx; relative error ~2^-22, far below bf16 rounding).
 __device__ __forceinline__ float fast_exp2(float x)
 {

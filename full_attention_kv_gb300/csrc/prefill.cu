@@ -404,6 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             m_used = m_new;
             const float base = m_used == -INFINITY ? 0.f : m_used;
             // ---- pass 2: P = 2^(s scale log2e - m) as bf16 pairs into TMEM --------------
+            // (the row sum takes the bf16-rounded P the PV MMA uses)
             // chunks are handled two at a time; chunk c4's 16 P columns land on S
             // columns 16 c4 .. 16 c4 + 15, which pass 2 has already read
             float sum4[4] = {0.f, 0.f, 0.f, 0.f};
@@ -421,8 +422,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int c = 0; c < 16; ++c) {
                             const float p0 = fast_exp2(fmaf(__uint_as_float(r32[h2][2 * c]), p.scale_log2, -base));
                             const float p1 = fast_exp2(fmaf(__uint_as_float(r32[h2][2 * c + 1]), p.scale_log2, -base));
-                            sum4[c & 3] += p0 + p1;
                             pk[h2][c] = pack_bf16(p0, p1);
+                            sum4[c & 3] += bf16_lo(pk[h2][c]) + bf16_hi(pk[h2][c]);
                         }
                     } else {
 #pragma unroll
@@ -430,8 +431,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const int k0 = (c8 + h2) * 32 + 2 * c;
                             const float p0 = vis(k0) ? fast_exp2(fmaf(__uint_as_float(r32[h2][2 * c]), p.scale_log2, -base)) : 0.f;
                             const float p1 = vis(k0 + 1) ? fast_exp2(fmaf(__uint_as_float(r32[h2][2 * c + 1]), p.scale_log2, -base)) : 0.f;
-                            sum4[c & 3] += p0 + p1;
                             pk[h2][c] = pack_bf16(p0, p1);
+                            sum4[c & 3] += bf16_lo(pk[h2][c]) + bf16_hi(pk[h2][c]);
                         }
                     }
                 }
