@@ -27,6 +27,7 @@ HSA_DEVERR_TIMEOUT = 32
 # every symbol include/hsa.h declares
 EXPORTS = ("hsa_kv_append", "hsa_decode_workspace_bytes", "hsa_decode_attn",
            "hsa_decode_attn_append", "hsa_decode_attn_noalloc", "hsa_prefill_attn",
+           "hsa_swa_prefetch",
            "hsa_window_safe_len", "hsa_window_safe_len_bitmap", "hsa_status_string")
 
 
@@ -85,6 +86,8 @@ def lib():
         L.hsa_prefill_attn.restype = ctypes.c_int
         L.hsa_prefill_attn.argtypes = [pp, i32, vp, vp, vp, vp, vp, vp, i32, i32, i32, f32, vp,
                                        vp, vp]
+        L.hsa_swa_prefetch.restype = ctypes.c_int
+        L.hsa_swa_prefetch.argtypes = [pp, i32, vp, vp, i32, vp, vp, i32, vp, vp]
         L.hsa_window_safe_len.restype = ctypes.c_int
         L.hsa_window_safe_len.argtypes = [vp, vp, i32, i32, vp, vp]
         L.hsa_window_safe_len_bitmap.restype = ctypes.c_int
@@ -295,6 +298,29 @@ def hsa_prefill_attn(pool, layer, q, k_new, v_new, cu_rows, prefix_len, seq_idx,
                                _stream(stream))
     _check("hsa_prefill_attn", s)
     return out
+
+
+def hsa_swa_prefetch(pool, layer, host_k, host_v, host_row, seq_idx, dev_err=None, stream=None):
+    """Copy SWA ring rows of one sliding layer from pinned host memory into the
+    device ring pool (row host_row[i] -> ring row of sequence seq_idx[i])."""
+    for n, t in (("host_k", host_k), ("host_v", host_v)):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or t.is_cuda:
+            raise TypeError("%s must be a bf16 host tensor" % n)
+        if not t.is_pinned() or not t.is_contiguous():
+            raise ValueError("%s must be pinned and contiguous" % n)
+    if host_k.shape != host_v.shape or host_k.dim() != 4:
+        raise ValueError("host_k / host_v must be [n_host_rows, Hkv, W, d]")
+    _need(host_row, "host_row", torch.int32, ndim=1)
+    _need(seq_idx, "seq_idx", torch.int32, ndim=1)
+    if host_row.shape != seq_idx.shape:
+        raise ValueError("host_row and seq_idx must have the same length")
+    if dev_err is not None:
+        _need(dev_err, "dev_err", torch.int32)
+    s = lib().hsa_swa_prefetch(pool.ref(), int(layer), ctypes.c_void_p(host_k.data_ptr()),
+                               ctypes.c_void_p(host_v.data_ptr()), host_k.shape[0],
+                               _ptr(host_row), _ptr(seq_idx), host_row.shape[0], _ptr(dev_err),
+                               _stream(stream))
+    _check("hsa_swa_prefetch", s)
 
 
 def hsa_window_safe_len(match_len, swa_slot_pos, W, out=None, stream=None):

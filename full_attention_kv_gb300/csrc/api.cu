@@ -337,6 +337,49 @@ hsa_status hsa_prefill_attn(const hsa_pools *pools, int32_t layer, const void *q
                : HSA_CUDA_ERROR;
 }
 
+hsa_status hsa_swa_prefetch(const hsa_pools *pools, int32_t layer, const void *host_k,
+                            const void *host_v, int32_t n_host_rows, const int32_t *host_row,
+                            const int32_t *seq_idx, int32_t n, int32_t *dev_err, void *stream)
+{
+    hsa_status st = check_pools(pools, layer);
+    if (st != HSA_OK)
+        return st;
+    if (pools->layer_is_full[layer])
+        return HSA_INVALID_ARG;  // only sliding layers have a ring to prefetch
+    if (n < 0 || n_host_rows < 0)
+        return HSA_INVALID_ARG;
+    if (n == 0)
+        return HSA_OK;
+    if (!host_k || !host_v || !host_row || !seq_idx || !aligned16(host_k) || !aligned16(host_v))
+        return HSA_INVALID_ARG;
+    // the host tier must be pinned (page-locked) host memory the GPU can address
+    void *dk = nullptr, *dv = nullptr;
+    if (cudaHostGetDevicePointer(&dk, const_cast<void *>(host_k), 0) != cudaSuccess ||
+        cudaHostGetDevicePointer(&dv, const_cast<void *>(host_v), 0) != cudaSuccess) {
+        cudaGetLastError();  // clear the (non-sticky) error the failed query recorded
+        return HSA_INVALID_ARG;
+    }
+    hsa::SwaPrefetchParams p{};
+    p.host_k = static_cast<const uint4 *>(dk);
+    p.host_v = static_cast<const uint4 *>(dv);
+    p.dev_k = static_cast<uint4 *>(pools->k[layer]);
+    p.dev_v = static_cast<uint4 *>(pools->v[layer]);
+    p.host_row = host_row;
+    p.seq_idx = seq_idx;
+    p.ring_row = pools->ring_row;
+    p.dev_err = dev_err;
+    p.n = n;
+    p.n_host_rows = n_host_rows;
+    p.n_ring_rows = pools->n_ring_rows;
+    p.batch = pools->batch;
+    p.Hkv = pools->Hkv;
+    p.W = pools->W;
+    p.chunks_per_row = pools->d * 2 / 16;
+    return hsa::launch_swa_prefetch(p, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? HSA_OK
+               : HSA_CUDA_ERROR;
+}
+
 hsa_status hsa_window_safe_len(const int32_t *match_len, const int32_t *swa_slot_pos, int32_t n,
                                int32_t W, int32_t *out_len, void *stream)
 {

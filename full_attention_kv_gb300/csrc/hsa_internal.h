@@ -91,6 +91,20 @@ cudaError_t launch_prefill(const CUtensorMap &tmPoolK, const CUtensorMap &tmPool
                            const CUtensorMap &tmNewK, const CUtensorMap &tmNewV,
                            const CUtensorMap &tmQ, const PrefillParams &p, cudaStream_t stream);
 
+struct SwaPrefetchParams {
+    const uint4 *host_k;         // pinned host ring rows [n_host_rows, Hkv, W, d] (device-visible)
+    const uint4 *host_v;
+    uint4 *dev_k;                // the layer's device ring [n_ring_rows, Hkv, W, d]
+    uint4 *dev_v;
+    const int32_t *host_row;     // [n]
+    const int32_t *seq_idx;      // [n]
+    const int32_t *ring_row;     // [batch]
+    int32_t *dev_err;
+    int32_t n, n_host_rows, n_ring_rows, batch, Hkv, W, chunks_per_row;
+};
+
+cudaError_t launch_swa_prefetch(const SwaPrefetchParams &p, cudaStream_t stream);
+
 cudaError_t launch_window_safe_ring(const int32_t *match_len, const int32_t *slot_pos, int32_t n,
                                     int32_t W, int32_t *out, cudaStream_t stream);
 cudaError_t launch_window_safe_bitmap(const int32_t *match_len, const int64_t *live_off,

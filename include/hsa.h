@@ -185,6 +185,22 @@ hsa_status hsa_prefill_attn(const hsa_pools *pools, int32_t layer, const void *q
                             int32_t *dev_err, void *stream);
 
 /*
+ * Layerwise SWA-KV prefetch [youleyou s2 "KVCache系统重构": the SWA layers' KV is
+ * prefetched layer by layer, overlapped with compute, so reading the cache costs
+ * almost nothing; hotdry.top "三层 KVCache 系统": host-to-device KV loads overlap the
+ * compute stream].  Copies ring rows of sliding layer `layer` from a host tier into
+ * the device SWA KV Pool: entry i moves row host_row[i] of host_k / host_v
+ * ([n_host_rows, Hkv, W, d] bf16 in PINNED host memory, which the GPU reads
+ * directly) into ring row ring_row[seq_idx[i]] of the layer.
+ *  host_row, seq_idx: device int32 [n].  Full layers are rejected (HSA_INVALID_ARG),
+ *  as is host memory that is not pinned.  Launch it on a side stream ahead of the
+ *  attention that reads the layer and order the two with an event.
+ */
+hsa_status hsa_swa_prefetch(const hsa_pools *pools, int32_t layer, const void *host_k,
+                            const void *host_v, int32_t n_host_rows, const int32_t *host_row,
+                            const int32_t *seq_idx, int32_t n, int32_t *dev_err, void *stream);
+
+/*
  * Window-safe prefix length [youleyou s2 "KVCache系统重构": a prefix match counts
  * only while the last W tokens still hold valid SWA slots; hotdry.top "Hybrid
  * SWA": the match length is cut back to the window boundary].
