@@ -259,7 +259,7 @@ class DecodeStep:
     """All layers: decode attention fused with the append of the step's new tokens
     (hsa_decode_attn_append, one launch per layer)."""
 
-    def __init__(self, inst, device, layers=None):
+    def __init__(self, inst, device, layers=None, swa_prefetch=False):
         import full_attention_kv_gb300 as hsa
         import harness
         self.hsa = hsa
@@ -268,6 +268,18 @@ class DecodeStep:
         self.model_layers = list(range(cfg.n_layers)) if layers is None else list(layers)
         self.layers = list(range(len(self.model_layers)))  # pool layer indices
         self.pool = harness.make_pool(inst, self.model_layers, device=device, stale="zero")
+        # layerwise SWA prefetch: every sliding layer's rings also live in a pinned
+        # host tier and are brought back each step on a side stream
+        self.prefetch = swa_prefetch
+        self.swa = [i for i, l in enumerate(self.model_layers) if not inst.full[l]]
+        if swa_prefetch:
+            self.host_k = {i: self.pool.k[i].cpu().pin_memory() for i in self.swa}
+            self.host_v = {i: self.pool.v[i].cpu().pin_memory() for i in self.swa}
+            self.host_rows = torch.from_numpy(inst.ring_row).to(device)
+            self.seqs = torch.arange(inst.R, dtype=torch.int32, device=device)
+            self.side = torch.cuda.Stream(device, priority=0)  # below the attention stream
+            self.ready = {i: torch.cuda.Event() for i in self.swa}
+            self.prefetch_bytes = sum(t.numel() * t.element_size() * 2 for t in self.host_k.values())
         self.q, self.k, self.v = [], [], []
         for l in self.model_layers:
             q, k, v, cl = harness.decode_inputs(inst, l, device)
@@ -294,9 +306,26 @@ class DecodeStep:
                                         self.inst.cfg.scale, out=self.out[l], workspace=self.ws,
                                         dev_err=self.err, stream=stream)
 
+    def prefetch_all(self, stream):
+        with torch.cuda.stream(stream):
+            for i in self.swa:
+                self.hsa.hsa_swa_prefetch(self.pool, i, self.host_k[i], self.host_v[i],
+                                          self.host_rows, self.seqs, dev_err=self.err)
+                self.ready[i].record(stream)
+
     def __call__(self):
-        for l in self.layers:
-            self.attn(l)
+        if self.prefetch:
+            cur = torch.cuda.current_stream()
+            self.side.wait_stream(cur)
+            self.prefetch_all(self.side)
+            for l in self.layers:
+                if l in self.ready:
+                    cur.wait_event(self.ready[l])
+                self.attn(l)
+            cur.wait_stream(self.side)
+        else:
+            for l in self.layers:
+                self.attn(l)
         if self.window is not None:
             m, s, o = self.window
             self.hsa.hsa_window_safe_len(m, s, self.inst.cfg.W, out=o)
@@ -394,6 +423,37 @@ def time_dominant(step, iters):
     return name, avg_s, float(np.mean(nbytes))
 
 
+def _prefetch_report(step, args, stream):
+    """Step time without the prefetch, and the prefetch alone, on the same box."""
+    step.prefetch = False
+    g2 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g2, stream=stream):
+        step()
+    for _ in range(3):
+        g2.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        g2.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    plain_ms = e0.elapsed_time(e1) / args.steps
+    step.prefetch = True
+    s = torch.cuda.current_stream()
+    step.prefetch_all(s)
+    torch.cuda.synchronize()
+    e0.record(s)
+    for _ in range(args.steps):
+        step.prefetch_all(s)
+    e1.record(s)
+    torch.cuda.synchronize()
+    alone_ms = e0.elapsed_time(e1) / args.steps
+    return {"bytes_per_step": step.prefetch_bytes, "step_ms_without_prefetch": plain_ms,
+            "prefetch_alone_ms": alone_ms,
+            "prefetch_alone_gbs": step.prefetch_bytes / (alone_ms / 1e3) / 1e9}
+
+
 def run_ours(args, inst, ws, rank, local):
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
@@ -401,8 +461,12 @@ def run_ours(args, inst, ws, rank, local):
     hsa.lib()
     cfg = inst.cfg
     layers = None if args.layers is None else [int(x) for x in args.layers.split(",")]
-    step = (DecodeStep if cfg.kind == "decode" else PrefillStep)(inst, device, layers)
-    stream = torch.cuda.Stream(device)
+    if cfg.kind == "decode":
+        step = DecodeStep(inst, device, layers, swa_prefetch=args.swa_prefetch)
+    else:
+        step = PrefillStep(inst, device, layers)
+    # the attention stream runs at high priority (a side stream, if any, at the default)
+    stream = torch.cuda.Stream(device, priority=-1)
     if args.profile_step:
         # one eager step between cudaProfilerStart / Stop (for ncu --profile-from-start off)
         with torch.cuda.stream(stream):
@@ -446,6 +510,9 @@ def run_ours(args, inst, ws, rank, local):
         step_ms = e0.elapsed_time(e1) / args.steps
         # dominant kernel, same stream, per-launch events
         dom_name, dom_s, dom_bytes = time_dominant(step, max(3, min(args.steps, 10)))
+        prefetch_info = None
+        if getattr(step, "prefetch", False):
+            prefetch_info = _prefetch_report(step, args, stream)
     clocks = clk.summary()
     step_ms = max_over_ranks(step_ms, ws)
 
@@ -521,6 +588,10 @@ def run_ours(args, inst, ws, rank, local):
         "gpu_launches": step.launches_per_step * args.steps,
     }
     line.update(extra)
+    if prefetch_info is not None:
+        line["swa_prefetch"] = prefetch_info
+        line["config"]["swa_prefetch"] = ("every step reloads all sliding layers' rings from a "
+                                          "pinned host tier on a side stream, layer by layer")
     if rank == 0 and not args.no_cpu_baseline:
         v, unit, _, cores, sample = run_reference(
             argparse.Namespace(steps=1, warmup=0), inst)
@@ -576,6 +647,9 @@ def main():
     ap.add_argument("--workload", default="decode", choices=sorted(workload.CONFIGS))
     ap.add_argument("--batch", type=int, default=None, help="truncate the draw (profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--swa-prefetch", action="store_true",
+                    help="decode: reload every sliding layer's rings from pinned host memory "
+                         "each step, layer by layer on a side stream")
     ap.add_argument("--layers", default=None,
                     help="comma-separated model layers (profiling sub-stack; default all)")
     ap.add_argument("--profile-step", action="store_true",

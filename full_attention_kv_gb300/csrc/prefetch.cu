@@ -10,41 +10,60 @@
 // ring row there ([n_host_rows, Hkv, W, d] bf16, pinned).  Bringing it back for
 // layer l is one gather kernel: every thread moves one 16-byte chunk, reading the
 // pinned host row directly over NVLink-C2C (no staging copy) and writing the
-// device ring row of the destination sequence.  The caller launches it on a side
-// stream one or more layers ahead of the attention that needs it; the copy uses
-// no shared memory and few registers, so it runs beside the attention kernels.
+// device ring row of the destination sequence, with four loads in flight per
+// thread.  The caller launches it on a side stream one or more layers ahead of the
+// attention that needs it; it keeps to two CTAs per SM and no shared memory, so it
+// runs beside the attention kernels.
 #include "hsa_device.cuh"
 #include "hsa_internal.h"
 
 namespace hsa {
 namespace {
 
+constexpr int kUnroll = 4;  // independent 16-byte host loads in flight per thread
+
 __global__ void __launch_bounds__(256) swa_prefetch_kernel(const SwaPrefetchParams p)
 {
     const int64_t per_row = (int64_t)p.Hkv * p.W * p.chunks_per_row;  // 16-B chunks per K row
     const int64_t total = (int64_t)p.n * 2 * per_row;
-    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
-         e += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t within = e % per_row;
-        const int kv = (int)((e / per_row) & 1);
-        const int i = (int)(e / (2 * per_row));
-        const int hr = __ldg(p.host_row + i);
-        const int seq = __ldg(p.seq_idx + i);
-        if (hr < 0 || hr >= p.n_host_rows || seq < 0 || seq >= p.batch) {
-            if (within == 0 && kv == 0)
-                set_err(p.dev_err, hr < 0 || hr >= p.n_host_rows ? HSA_DEVERR_BAD_LEN
-                                                                 : HSA_DEVERR_BAD_SEQ);
-            continue;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t e0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e0 < total;
+         e0 += stride * kUnroll) {
+        uint4 v[kUnroll];
+        int64_t dst[kUnroll];
+        bool ok[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t e = e0 + u * stride;
+            ok[u] = false;
+            if (e >= total)
+                continue;
+            const int64_t within = e % per_row;
+            const int kv = (int)((e / per_row) & 1);
+            const int i = (int)(e / (2 * per_row));
+            const int hr = __ldg(p.host_row + i);
+            const int seq = __ldg(p.seq_idx + i);
+            if (hr < 0 || hr >= p.n_host_rows || seq < 0 || seq >= p.batch) {
+                if (within == 0 && kv == 0)
+                    set_err(p.dev_err, hr < 0 || hr >= p.n_host_rows ? HSA_DEVERR_BAD_LEN
+                                                                     : HSA_DEVERR_BAD_SEQ);
+                continue;
+            }
+            const int rr = __ldg(p.ring_row + seq);
+            if (rr < 0 || rr >= p.n_ring_rows) {
+                if (within == 0 && kv == 0)
+                    set_err(p.dev_err, HSA_DEVERR_BAD_RING);
+                continue;
+            }
+            const uint4 *src = kv ? p.host_v : p.host_k;
+            v[u] = src[(int64_t)hr * per_row + within];
+            dst[u] = ((int64_t)rr * per_row + within) * 2 + kv;  // row index, K/V bit
+            ok[u] = true;
         }
-        const int rr = __ldg(p.ring_row + seq);
-        if (rr < 0 || rr >= p.n_ring_rows) {
-            if (within == 0 && kv == 0)
-                set_err(p.dev_err, HSA_DEVERR_BAD_RING);
-            continue;
-        }
-        const uint4 *src = kv ? p.host_v : p.host_k;
-        uint4 *dst = kv ? p.dev_v : p.dev_k;
-        dst[(int64_t)rr * per_row + within] = src[(int64_t)hr * per_row + within];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u)
+            if (ok[u])
+                (dst[u] & 1 ? p.dev_v : p.dev_k)[dst[u] >> 1] = v[u];
     }
 }
 
@@ -58,8 +77,10 @@ cudaError_t launch_swa_prefetch(const SwaPrefetchParams &p, cudaStream_t stream)
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    // a small footprint (two CTAs of 8 warps per SM) so that attention CTAs launched
+    // beside it always find room on every SM
     int64_t blocks = (total + 255) / 256;
-    const int64_t cap = (int64_t)(sms > 0 ? sms : 148) * 8;
+    const int64_t cap = (int64_t)(sms > 0 ? sms : 148) * 2;
     if (blocks > cap)
         blocks = cap;
     swa_prefetch_kernel<<<(unsigned)blocks, 256, 0, stream>>>(p);
