@@ -10,17 +10,22 @@
 // with positions < P read from the pools (Full KV Pool pages through the block
 // table, or the SWA ring) and positions >= P from the chunk's own k_new / v_new.
 //
-// Design: one CTA per (request, 128-row query tile, query head); keys in tiles of
-// 128.  Six warps:
-//   warp 0   TMA producer: Q once, then K and V tiles into a 2-stage ring
-//            (128-byte swizzle; a prefix tile is two 64-token pages)
-//   warp 1   TMEM owner and MMA issuer (one thread): S = Q K^T into a
-//            double-buffered TMEM tile, O += P V with P read from TMEM
-//   warps 2-5 softmax, one query row per thread (TMEM lane = row): masks,
-//            running max with lazy rescaling (O is rescaled in TMEM only when
-//            the max grows by more than 2^8), P written back to TMEM as bf16
-// While the softmax warps work on tile n, the tensor cores already compute
-// S for tile n+1.  The epilogue divides O by the row sum and writes bf16.
+// Design: one CTA per (request, pair of 128-row query tiles A and B, query head);
+// both tiles share every 128-key K / V tile.  Ten warps:
+//   warp 0    TMA producer: Q_A and Q_B once, then K and V tiles into a 2-stage
+//             ring (128-byte swizzle; a prefix tile is two 64-token pages)
+//   warp 1    TMEM owner (S_A, S_B, O_A, O_B: 4 x 128 columns) and MMA issuer
+//             (one thread): S = Q K^T, O += P V with P read from TMEM
+//   warps 2-5 softmax of tile A, warps 6-9 softmax of tile B, one query row per
+//             thread (TMEM lane = row): masks, running max raised lazily (O is
+//             rescaled in TMEM only when the max grows by more than 2^8), P written
+//             back over S as bf16
+// The MMA thread issues PV_A(n), then S_A(n+1), then PV_B(n), then S_B(n+1), so
+// the tensor cores work on one tile while the other tile's warps run softmax, and
+// each SM sub-partition holds two independent softmax warps.  Every key tile is
+// run for both query tiles (a tile a row cannot see is simply masked: at most one
+// extra 128-key tile per CTA).  The epilogue divides O by the row sum and writes
+// bf16.
 #include "hsa_device.cuh"
 #include "hsa_internal.h"
 
@@ -32,30 +37,35 @@ constexpr int kBN = 128;
 constexpr int kD = 128;
 constexpr int kHalfBytes = 128 * 128;      // 128 rows x 64 bf16 (one swizzle column block)
 constexpr int kTileBytes = 2 * kHalfBytes; // 32 KB
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO = 256;            // S buffers at columns 0 and 128
+constexpr uint32_t kColO = 256;            // S_A, S_B at 0 / 128; O_A, O_B at 256 / 384
 constexpr float kRescaleSlack = 8.0f;      // log2 units: P may reach 2^8 before a rescale
 
 struct PrefillSmem {
-    alignas(1024) uint8_t q[kTileBytes];
+    alignas(1024) uint8_t q[2][kTileBytes];
     alignas(1024) uint8_t k[2][kTileBytes];
     alignas(1024) uint8_t v[2][kTileBytes];
     alignas(8) uint64_t q_full;
     uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
-    uint64_t s_full[2], p_full[2], pv_done[2], o_full;
+    uint64_t s_full[2], p_full[2], o_full;  // s_full / p_full per query tile
     uint32_t tmem_base;
-    int32_t r, qt, P, C, seq, row0;
+    int32_t r, qp, P, C, seq, row0;
 };
 
 struct Sched {
-    int nt;          // key tiles
+    int nt;          // key tiles (union over both query tiles)
     int n_fixed;     // prefix tiles (full) or ring tiles (sliding) before the chunk tiles
     int m_lo;        // first chunk tile
 };
 
-__device__ __forceinline__ Sched make_sched(const PrefillParams &p, int P, int i0)
+// Key tiles of the CTA whose query tiles start at rows i0 (A) and i0 + 128 (B, if
+// has_b): full layers read every prefix tile and chunk tiles 0 .. last row / 128;
+// sliding layers read the ring if a row still sees the prefix, and the chunk tiles
+// inside the window.
+__device__ __forceinline__ Sched make_sched(const PrefillParams &p, int P, int i0, bool has_b)
 {
+    const int i_last = i0 + (has_b ? 2 * kBM : kBM) - 1;  // last row of the CTA (may pad)
     Sched s;
     if (!p.ring_mode) {
         s.n_fixed = (P + kBN - 1) / kBN;
@@ -65,7 +75,7 @@ __device__ __forceinline__ Sched make_sched(const PrefillParams &p, int P, int i
         const int lo = i0 - p.W + 1;
         s.m_lo = lo > 0 ? lo / kBN : 0;
     }
-    s.nt = s.n_fixed + (i0 / kBN - s.m_lo + 1);
+    s.nt = s.n_fixed + (i_last / kBN - s.m_lo + 1);
     return s;
 }
 
@@ -93,27 +103,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int hq = blockIdx.x % p.Hq;
     const int h = hq / p.G;
 
-    // ---- which (request, query tile) this CTA owns --------------------------
+    // ---- which (request, pair of query tiles) this CTA owns -----------------
     if (tid == 0) {
         const int tl = blockIdx.x / p.Hq;
-        int acc = 0, found = -1, qt = 0;
+        int acc = 0, found = -1, qp = 0;
         for (int r = 0; r < p.R; ++r) {
             const int C = __ldg(p.cu_rows + r + 1) - __ldg(p.cu_rows + r);
-            const int nq = C > 0 ? (C + kBM - 1) / kBM : 0;
-            if (tl < acc + nq) {
+            const int np = C > 0 ? (C + 2 * kBM - 1) / (2 * kBM) : 0;
+            if (tl < acc + np) {
                 found = r;
-                qt = tl - acc;
+                qp = tl - acc;
                 break;
             }
-            acc += nq;
+            acc += np;
         }
         sh.r = found;
         if (found >= 0) {
-            sh.qt = qt;
+            sh.qp = qp;
             sh.P = __ldg(p.prefix_len + found);
             sh.C = __ldg(p.cu_rows + found + 1) - __ldg(p.cu_rows + found);
             sh.seq = __ldg(p.seq_idx + found);
-            sh.row0 = __ldg(p.cu_rows + found) + qt * kBM;
+            sh.row0 = __ldg(p.cu_rows + found) + qp * 2 * kBM;
             if (sh.seq < 0 || sh.seq >= p.batch) {
                 if (hq == 0)
                     set_err(p.dev_err, HSA_DEVERR_BAD_SEQ);
@@ -127,9 +137,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncthreads();
     if (sh.r < 0)
-        return;  // past the last tile (grid is an upper bound) or a bad request
-    const int P = sh.P, C = sh.C, seq = sh.seq, i0 = sh.qt * kBM, row0 = sh.row0;
-    const Sched sc = make_sched(p, P, i0);
+        return;  // past the last tile pair (grid is an upper bound) or a bad request
+    const int P = sh.P, C = sh.C, seq = sh.seq, i0 = sh.qp * 2 * kBM, row0 = sh.row0;
+    const bool has_b = i0 + kBM < C;
+    const Sched sc = make_sched(p, P, i0, has_b);
 
     if (tid == 0) {
         mbar_init(&sh.q_full, 1);
@@ -140,7 +151,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&sh.v_empty[s], 1);
             mbar_init(&sh.s_full[s], 1);
             mbar_init(&sh.p_full[s], 4 * 32);
-            mbar_init(&sh.pv_done[s], 1);
         }
         mbar_init(&sh.o_full, 1);
         fence_barrier_init();
@@ -164,14 +174,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_prefetch_desc(&tmNV);
             const uint64_t pol_stream = policy_evict_first();
             const uint64_t pol_keep = policy_evict_last();
-            mbar_arrive_expect_tx(&sh.q_full, kTileBytes);
-            tma_load_3d(sh.q, &tmQ, &sh.q_full, 0, hq, row0, pol_stream);
-            tma_load_3d(sh.q + kHalfBytes, &tmQ, &sh.q_full, 64, hq, row0, pol_stream);
+            mbar_arrive_expect_tx(&sh.q_full, (has_b ? 2 : 1) * kTileBytes);
+            for (int t = 0; t < (has_b ? 2 : 1); ++t) {
+                tma_load_3d(sh.q[t], &tmQ, &sh.q_full, 0, hq, row0 + t * kBM, pol_stream);
+                tma_load_3d(sh.q[t] + kHalfBytes, &tmQ, &sh.q_full, 64, hq, row0 + t * kBM,
+                            pol_stream);
+            }
             int ring_row = 0;
             if (p.ring_mode) {
                 ring_row = __ldg(p.ring_row + seq);
                 if (ring_row < 0 || ring_row >= p.n_ring_rows) {
-                    if (hq == 0 && sh.qt == 0)
+                    if (hq == 0 && sh.qp == 0)
                         set_err(p.dev_err, HSA_DEVERR_BAD_RING);
                     ring_row = 0;
                 }
@@ -237,54 +250,62 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             const uint32_t id_s = idesc_bf16_f32(kBM, kBN, 0, 0);
             const uint32_t id_pv = idesc_bf16_f32(kBM, kD, 0, 1);
-            const uint32_t sq = smem_u32(sh.q);
+            const int ntile = has_b ? 2 : 1;
             bool ok = mbar_wait(&sh.q_full, 0);
-            auto issue_pv = [&](int j) -> bool {
-                const int sj = j & 1;
-                const uint32_t phj = (j >> 1) & 1;
-                if (!mbar_wait(&sh.p_full[sj], phj) || !mbar_wait(&sh.v_full[sj], phj))
-                    return false;
-                tc_fence_after();
-                const uint32_t sv = smem_u32(sh.v[sj]);
-#pragma unroll
-                for (int ks = 0; ks < kBN / 16; ++ks) {
-                    const uint64_t b = smem_desc_sw128(sv + ks * 2048, kHalfBytes, 1024);
-                    tc_mma_ts(tmem + kColO, tmem + sj * 128 + ks * 8, b, id_pv,
-                              (j > 0 || ks > 0) ? 1u : 0u);
-                }
-                tc_commit(&sh.pv_done[sj]);
-                tc_commit(&sh.v_empty[sj]);
-                return true;
-            };
-            for (int n = 0; n < sc.nt && ok; ++n) {
-                const int s = n & 1;
-                const uint32_t ph = (n >> 1) & 1;
-                if (!mbar_wait(&sh.k_full[s], ph)) {
-                    ok = false;
-                    break;
-                }
-                if (n >= 2 && !mbar_wait(&sh.pv_done[s], ((n - 2) >> 1) & 1)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t sk = smem_u32(sh.k[s]);
+            // S_t = Q_t K_n^T into TMEM columns t * 128
+            auto issue_s = [&](int t, int n) {
+                const uint32_t sq = smem_u32(sh.q[t]);
+                const uint32_t sk = smem_u32(sh.k[n & 1]);
 #pragma unroll
                 for (int ks = 0; ks < kD / 16; ++ks) {
                     const uint32_t off = (ks >> 2) * kHalfBytes + (ks & 3) * 32;
-                    const uint64_t a = smem_desc_sw128(sq + off, 16, 1024);
-                    const uint64_t b = smem_desc_sw128(sk + off, 16, 1024);
-                    tc_mma_ss(tmem + s * 128, a, b, id_s, ks > 0 ? 1u : 0u);
+                    tc_mma_ss(tmem + t * 128, smem_desc_sw128(sq + off, 16, 1024),
+                              smem_desc_sw128(sk + off, 16, 1024), id_s, ks > 0 ? 1u : 0u);
                 }
-                tc_commit(&sh.s_full[s]);
-                tc_commit(&sh.k_empty[s]);
-                if (n >= 1 && !issue_pv(n - 1)) {
+                tc_commit(&sh.s_full[t]);
+            };
+            // O_t += P_t V_n, P_t read from TMEM over S_t
+            auto issue_pv = [&](int t, int n) {
+                const uint32_t sv = smem_u32(sh.v[n & 1]);
+#pragma unroll
+                for (int ks = 0; ks < kBN / 16; ++ks)
+                    tc_mma_ts(tmem + kColO + t * 128, tmem + t * 128 + ks * 8,
+                              smem_desc_sw128(sv + ks * 2048, kHalfBytes, 1024), id_pv,
+                              (n > 0 || ks > 0) ? 1u : 0u);
+            };
+            if (ok && (ok = mbar_wait(&sh.k_full[0], 0))) {
+                tc_fence_after();
+                for (int t = 0; t < ntile; ++t)
+                    issue_s(t, 0);
+                tc_commit(&sh.k_empty[0]);
+            }
+            for (int n = 0; n < sc.nt && ok; ++n) {
+                const int s = n & 1;
+                const bool more = n + 1 < sc.nt;
+                if (more && !mbar_wait(&sh.k_full[(n + 1) & 1], ((n + 1) >> 1) & 1)) {
                     ok = false;
                     break;
                 }
+                for (int t = 0; t < ntile; ++t) {
+                    // tile t's P of key tile n is in TMEM once its softmax warps arrive;
+                    // S_t(n+1) is issued behind PV_t(n) (tcgen05 MMAs from one thread run
+                    // in issue order, so PV reads P before S overwrites it)
+                    if (!mbar_wait(&sh.p_full[t], n & 1) ||
+                        (t == 0 && !mbar_wait(&sh.v_full[s], (n >> 1) & 1))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    issue_pv(t, n);
+                    if (more)
+                        issue_s(t, n + 1);
+                }
+                if (!ok)
+                    break;
+                if (more)
+                    tc_commit(&sh.k_empty[(n + 1) & 1]);
+                tc_commit(&sh.v_empty[s]);
             }
-            if (ok)
-                ok = issue_pv(sc.nt - 1);
             if (ok) {
                 tc_commit(&sh.o_full);
                 mbar_wait(&sh.o_full, 0);  // every MMA done before TMEM is released
@@ -294,11 +315,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ================================================================ softmax
+        const int t = (warp - 2) >> 2;  // query tile: 0 = A (warps 2-5), 1 = B (warps 6-9)
         const int wq = warp & 3;
         const int row = wq * 32 + lane;
-        const int i = i0 + row;
-        const bool row_ok = i < C;
+        const int i = i0 + t * kBM + row;
+        const bool tile_ok = t == 0 || has_b;
+        const bool row_ok = tile_ok && i < C;
         const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
+        const uint32_t col_s = t * 128, col_o = kColO + t * 128;
         float m_used = -INFINITY, l = 0.f;
         int ring_row_ok = 1;
         if (p.ring_mode) {
@@ -306,14 +330,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             ring_row_ok = rr >= 0 && rr < p.n_ring_rows;
         }
         bool ok = true;
-        for (int n = 0; n < sc.nt; ++n) {
-            const int s = n & 1;
-            const uint32_t ph = (n >> 1) & 1;
-            if (!mbar_wait(&sh.s_full[s], ph)) {
+        for (int n = 0; n < sc.nt && tile_ok; ++n) {
+            if (!mbar_wait(&sh.s_full[t], n & 1)) {
                 set_err(p.dev_err, HSA_DEVERR_TIMEOUT);
                 ok = false;
                 break;
             }
+            // S_t(n) complete implies every earlier MMA (PV_t(n-1) included) completed
             tc_fence_after();
             // ---- visibility of the 128 keys of tile n for query row i ----------
             int lo = 0, hi = 0;
@@ -337,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!row_ok)
                 hi = 0;
             const bool whole_tile = !ring && lo == 0 && hi == kBN && ok0 && ok1;
-            // ring slot t holds the latest prefix position below P congruent to t mod W
+            // ring slot s holds the latest prefix position below P congruent to s mod W
             const int lo_pos = max(0, P + i - p.W + 1);
             auto vis = [&](int key) -> bool {
                 if (ring) {
@@ -354,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t r32[4][32];
 #pragma unroll
                 for (int c4 = 0; c4 < 4; ++c4)
-                    tmem_ld32(lane_addr + s * 128 + c4 * 32, r32[c4]);
+                    tmem_ld32(lane_addr + col_s + c4 * 32, r32[c4]);
                 tmem_wait_ld();
                 float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
                 if (whole_tile) {
@@ -380,23 +403,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m_new = mx;
             const bool resc = m_used != -INFINITY && m_new != m_used;
             if (__any_sync(0xffffffffu, resc)) {
-                // O holds sum_{j<n} P_j V_j: wait for PV of tile n-1 before touching it
-                if (!mbar_wait(&sh.pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1)) {
-                    set_err(p.dev_err, HSA_DEVERR_TIMEOUT);
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
                 const float alpha = resc ? fast_exp2(m_used - m_new) : 1.0f;
 #pragma unroll 1
                 for (int c4 = 0; c4 < 4; ++c4) {
                     uint32_t o32[32];
-                    tmem_ld32(lane_addr + kColO + c4 * 32, o32);
+                    tmem_ld32(lane_addr + col_o + c4 * 32, o32);
                     tmem_wait_ld();
 #pragma unroll
                     for (int c = 0; c < 32; ++c)
                         o32[c] = __float_as_uint(__uint_as_float(o32[c]) * alpha);
-                    tmem_st32(lane_addr + kColO + c4 * 32, o32);
+                    tmem_st32(lane_addr + col_o + c4 * 32, o32);
                 }
                 tmem_wait_st();
                 l *= alpha;
@@ -412,8 +428,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
             for (int c8 = 0; c8 < 4; c8 += 2) {
                 uint32_t r32[2][32];
-                tmem_ld32(lane_addr + s * 128 + c8 * 32, r32[0]);
-                tmem_ld32(lane_addr + s * 128 + (c8 + 1) * 32, r32[1]);
+                tmem_ld32(lane_addr + col_s + c8 * 32, r32[0]);
+                tmem_ld32(lane_addr + col_s + (c8 + 1) * 32, r32[1]);
                 tmem_wait_ld();
                 uint32_t pk[2][16];
 #pragma unroll
@@ -439,24 +455,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
-                tmem_st16(lane_addr + s * 128 + c8 * 16, pk[0]);
-                tmem_st16(lane_addr + s * 128 + (c8 + 1) * 16, pk[1]);
+                tmem_st16(lane_addr + col_s + c8 * 16, pk[0]);
+                tmem_st16(lane_addr + col_s + (c8 + 1) * 16, pk[1]);
             }
             const float sum = (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
             l += sum;
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(&sh.p_full[s]);
+            mbar_arrive(&sh.p_full[t]);
         }
         // ---- epilogue: O / l -> bf16 ------------------------------------------
-        if (ok && mbar_wait(&sh.o_full, 0)) {
+        if (tile_ok && ok && mbar_wait(&sh.o_full, 0)) {
             tc_fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;
-            __nv_bfloat16 *dst = p.out + ((int64_t)(row0 + row) * p.Hq + hq) * kD;
+            __nv_bfloat16 *dst = p.out + ((int64_t)(row0 + t * kBM + row) * p.Hq + hq) * kD;
             uint32_t o32[32];
 #pragma unroll
             for (int c4 = 0; c4 < 4; ++c4) {
-                tmem_ld32(lane_addr + kColO + c4 * 32, o32);
+                tmem_ld32(lane_addr + col_o + c4 * 32, o32);
                 tmem_wait_ld();
                 if (row_ok) {
 #pragma unroll
@@ -470,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-        } else if (ok) {
+        } else if (tile_ok && ok) {
             set_err(p.dev_err, HSA_DEVERR_TIMEOUT);
         }
     }
@@ -500,7 +516,10 @@ cudaError_t launch_prefill(const CUtensorMap &tmPK, const CUtensorMap &tmPV,
             return e;
         attr_set = true;
     }
-    const int64_t ctas = (int64_t)p.tiles_per_req_bound * p.Hq;
+    // tiles_per_req_bound bounds the number of 128-row tiles; a CTA takes a pair of
+    // them, and each request may end on an odd tile
+    const int64_t pairs = ((int64_t)p.tiles_per_req_bound + p.R + 1) / 2;
+    const int64_t ctas = pairs * p.Hq;
     if (ctas <= 0)
         return cudaSuccess;
     prefill_kernel<<<(unsigned)ctas, kThreads, smem, stream>>>(tmPK, tmPV, tmNK, tmNV, tmQ, p);
