@@ -198,6 +198,42 @@ __device__ __forceinline__ float fast_exp2(float x)
     return y;
 }
 
+// ---------------------------------------------------------------- packed fp32 pairs
+// sm_100-family instructions that issue once for two fp32 lanes (f32x2 FMA / add)
+// or fold two comparisons into one (three-input max).
+__device__ __forceinline__ uint64_t f2_make(float lo, float hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ void f2_split(uint64_t v, float &lo, float &hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t d;
+    asm("fma.rn.ftz.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("add.rn.ftz.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c)
+{
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // Byte offset of element (row, col) inside a tile written by TMA with 128-byte
 // swizzle: the tile is stored as boxes of 64 bf16 columns (128 B) x `rows` rows;
 // inside a box the 16-byte chunk index is XOR-ed with (row mod 8).

@@ -371,39 +371,73 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 return key >= lo && key < hi && (key < 64 ? ok0 : ok1);
             };
-            // ---- pass 1: raw-score row max (four loads in flight, four max chains) --
-            float mx = -INFINITY;
-            {
-                uint32_t r32[4][32];
+            // ---- the row's 128 scores: one TMEM read, kept in registers ------------
+            uint32_t r32[4][32];
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4)
+                tmem_ld32(lane_addr + col_s + c4 * 32, r32[c4]);
+            tmem_wait_ld();
+            if (!whole_tile) {
+                // keys the row cannot see become -inf: 2^-inf = 0 in the P pass below
 #pragma unroll
                 for (int c4 = 0; c4 < 4; ++c4)
-                    tmem_ld32(lane_addr + col_s + c4 * 32, r32[c4]);
-                tmem_wait_ld();
-                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-                if (whole_tile) {
 #pragma unroll
-                    for (int c4 = 0; c4 < 4; ++c4)
-#pragma unroll
-                        for (int c = 0; c < 32; ++c)
-                            m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(r32[c4][c]));
-                } else {
-#pragma unroll
-                    for (int c4 = 0; c4 < 4; ++c4)
-#pragma unroll
-                        for (int c = 0; c < 32; ++c)
-                            if (vis(c4 * 32 + c))
-                                m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(r32[c4][c]));
-                }
-                mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                    for (int c = 0; c < 32; ++c)
+                        if (!vis(c4 * 32 + c))
+                            r32[c4][c] = __float_as_uint(-INFINITY);
             }
-            mx *= p.scale_log2;  // the scale is positive
-            // ---- running max, lazily raised; O rescaled in TMEM when it moves ------
+            // ---- row max (three-input max, four chains) ---------------------------
+            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4)
+#pragma unroll
+                for (int c = 0; c < 32; c += 8) {
+                    m4[0] = fmax3(m4[0], __uint_as_float(r32[c4][c + 0]), __uint_as_float(r32[c4][c + 1]));
+                    m4[1] = fmax3(m4[1], __uint_as_float(r32[c4][c + 2]), __uint_as_float(r32[c4][c + 3]));
+                    m4[2] = fmax3(m4[2], __uint_as_float(r32[c4][c + 4]), __uint_as_float(r32[c4][c + 5]));
+                    m4[3] = fmax3(m4[3], __uint_as_float(r32[c4][c + 6]), __uint_as_float(r32[c4][c + 7]));
+                }
+            const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * p.scale_log2;
+            // ---- running max, lazily raised (O is rescaled below when it moves) ----
             float m_new = m_used;
             if (mx != -INFINITY && (m_used == -INFINITY || mx > m_used + kRescaleSlack))
                 m_new = mx;
             const bool resc = m_used != -INFINITY && m_new != m_used;
+            const float alpha = resc ? fast_exp2(m_used - m_new) : 1.0f;
+            m_used = m_new;
+            const float base = m_used == -INFINITY ? 0.f : m_used;
+            // ---- P = 2^(s scale log2e - m) as bf16 pairs, from the registers ------
+            // group c4's 16 P columns land on S columns 16 c4 .. 16 c4 + 15, all read
+            // above.  On whole tiles the row sum takes the unrounded P (128 keys: the
+            // bf16 rounding averages out, relative error ~2^-12.5); on partial tiles
+            // it takes the bf16-rounded P the PV MMA uses, so rows with few keys get
+            // no scale error proportional to |O|.
+            const uint64_t sc2 = f2_make(p.scale_log2, p.scale_log2);
+            const uint64_t nb2 = f2_make(-base, -base);
+            uint64_t acc2[2] = {f2_make(0.f, 0.f), f2_make(0.f, 0.f)};
+            float accr = 0.f;
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    const uint64_t x2 = f2_fma(f2_make(__uint_as_float(r32[c4][2 * c]),
+                                                       __uint_as_float(r32[c4][2 * c + 1])),
+                                               sc2, nb2);
+                    float x0, x1;
+                    f2_split(x2, x0, x1);
+                    const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+                    pk[c] = pack_bf16(p0, p1);
+                    if (whole_tile)
+                        acc2[c & 1] = f2_add(acc2[c & 1], f2_make(p0, p1));
+                    else
+                        accr += bf16_lo(pk[c]) + bf16_hi(pk[c]);
+                }
+                tmem_st16(lane_addr + col_s + c4 * 16, pk);
+            }
+            // O (read by PV_t(n), which waits for this warp) is rescaled after the P
+            // pass, once the score registers are free
             if (__any_sync(0xffffffffu, resc)) {
-                const float alpha = resc ? fast_exp2(m_used - m_new) : 1.0f;
 #pragma unroll 1
                 for (int c4 = 0; c4 < 4; ++c4) {
                     uint32_t o32[32];
@@ -414,52 +448,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         o32[c] = __float_as_uint(__uint_as_float(o32[c]) * alpha);
                     tmem_st32(lane_addr + col_o + c4 * 32, o32);
                 }
-                tmem_wait_st();
-                l *= alpha;
             }
-            m_used = m_new;
-            const float base = m_used == -INFINITY ? 0.f : m_used;
-            // ---- pass 2: P = 2^(s scale log2e - m) as bf16 pairs into TMEM --------------
-            // (on partial tiles the row sum takes the bf16-rounded P the PV MMA uses, so
-            // rows with few keys get no scale error proportional to |O|)
-            // chunks are handled two at a time; chunk c4's 16 P columns land on S
-            // columns 16 c4 .. 16 c4 + 15, which pass 2 has already read
-            float sum4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-            for (int c8 = 0; c8 < 4; c8 += 2) {
-                uint32_t r32[2][32];
-                tmem_ld32(lane_addr + col_s + c8 * 32, r32[0]);
-                tmem_ld32(lane_addr + col_s + (c8 + 1) * 32, r32[1]);
-                tmem_wait_ld();
-                uint32_t pk[2][16];
-#pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2) {
-                    if (whole_tile) {
-                        // 128 visible keys: the bf16 rounding of P averages out in the
-                        // row sum (relative error ~2^-12.5), so the unrounded P is summed
-#pragma unroll
-                        for (int c = 0; c < 16; ++c) {
-                            const float p0 = fast_exp2(fmaf(__uint_as_float(r32[h2][2 * c]), p.scale_log2, -base));
-                            const float p1 = fast_exp2(fmaf(__uint_as_float(r32[h2][2 * c + 1]), p.scale_log2, -base));
-                            pk[h2][c] = pack_bf16(p0, p1);
-                            sum4[c & 3] += p0 + p1;
-                        }
-                    } else {
-#pragma unroll
-                        for (int c = 0; c < 16; ++c) {
-                            const int k0 = (c8 + h2) * 32 + 2 * c;
-                            const float p0 = vis(k0) ? fast_exp2(fmaf(__uint_as_float(r32[h2][2 * c]), p.scale_log2, -base)) : 0.f;
-                            const float p1 = vis(k0 + 1) ? fast_exp2(fmaf(__uint_as_float(r32[h2][2 * c + 1]), p.scale_log2, -base)) : 0.f;
-                            pk[h2][c] = pack_bf16(p0, p1);
-                            sum4[c & 3] += bf16_lo(pk[h2][c]) + bf16_hi(pk[h2][c]);
-                        }
-                    }
-                }
-                tmem_st16(lane_addr + col_s + c8 * 16, pk[0]);
-                tmem_st16(lane_addr + col_s + (c8 + 1) * 16, pk[1]);
+            {
+                float a0, a1;
+                f2_split(f2_add(acc2[0], acc2[1]), a0, a1);
+                l = l * alpha + ((a0 + a1) + accr);
             }
-            const float sum = (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
-            l += sum;
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(&sh.p_full[t]);
