@@ -66,11 +66,42 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may sleep up to `hint_ns` for the phase to
+// complete instead of returning at once (a waiting warp then takes no issue slots
+// from the warps it shares an SM sub-partition with).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns()
 {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
+}
+
+// Bounded wait whose polls sleep (up to 20 us each) until the phase completes.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t *bar, uint32_t parity)
+{
+    if (mbar_try_wait_sleep(bar, parity, 20000u))
+        return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        for (int i = 0; i < 8; ++i)
+            if (mbar_try_wait_sleep(bar, parity, 20000u))
+                return true;
+        if (globaltimer_ns() - t0 > HSA_WAIT_NS)
+            return false;
+    }
 }
 
 // Wait for the phase with the given parity, bounded by HSA_WAIT_NS of wall time;

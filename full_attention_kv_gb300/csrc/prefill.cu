@@ -199,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint8_t *dst = kv ? sh.v[s] : sh.k[s];
                     const CUtensorMap *pool = kv ? &tmPV : &tmPK;
                     const CUtensorMap *nw = kv ? &tmNV : &tmNK;
-                    if (!mbar_wait(empty, ph ^ 1)) {
+                    if (!mbar_wait_sleep(empty, ph ^ 1)) {
                         set_err(p.dev_err, HSA_DEVERR_TIMEOUT);
                         ok = false;
                         break;
@@ -241,8 +241,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int s = 0; s < 2 && sc.nt > s; ++s) {
                 const int last = s + ((sc.nt - 1 - s) / 2) * 2;
                 const uint32_t ph = (last >> 1) & 1;
-                mbar_wait(&sh.k_full[s], ph);
-                mbar_wait(&sh.v_full[s], ph);
+                mbar_wait_sleep(&sh.k_full[s], ph);
+                mbar_wait_sleep(&sh.v_full[s], ph);
             }
         }
     } else if (warp == 1) {
@@ -251,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t id_s = idesc_bf16_f32(kBM, kBN, 0, 0);
             const uint32_t id_pv = idesc_bf16_f32(kBM, kD, 0, 1);
             const int ntile = has_b ? 2 : 1;
-            bool ok = mbar_wait(&sh.q_full, 0);
+            bool ok = mbar_wait_sleep(&sh.q_full, 0);
             // S_t = Q_t K_n^T into TMEM columns t * 128
             auto issue_s = [&](int t, int n) {
                 const uint32_t sq = smem_u32(sh.q[t]);
@@ -273,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                               smem_desc_sw128(sv + ks * 2048, kHalfBytes, 1024), id_pv,
                               (n > 0 || ks > 0) ? 1u : 0u);
             };
-            if (ok && (ok = mbar_wait(&sh.k_full[0], 0))) {
+            if (ok && (ok = mbar_wait_sleep(&sh.k_full[0], 0))) {
                 tc_fence_after();
                 for (int t = 0; t < ntile; ++t)
                     issue_s(t, 0);
@@ -282,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int n = 0; n < sc.nt && ok; ++n) {
                 const int s = n & 1;
                 const bool more = n + 1 < sc.nt;
-                if (more && !mbar_wait(&sh.k_full[(n + 1) & 1], ((n + 1) >> 1) & 1)) {
+                if (more && !mbar_wait_sleep(&sh.k_full[(n + 1) & 1], ((n + 1) >> 1) & 1)) {
                     ok = false;
                     break;
                 }
@@ -290,8 +290,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // tile t's P of key tile n is in TMEM once its softmax warps arrive;
                     // S_t(n+1) is issued behind PV_t(n) (tcgen05 MMAs from one thread run
                     // in issue order, so PV reads P before S overwrites it)
-                    if (!mbar_wait(&sh.p_full[t], n & 1) ||
-                        (t == 0 && !mbar_wait(&sh.v_full[s], (n >> 1) & 1))) {
+                    if (!mbar_wait_sleep(&sh.p_full[t], n & 1) ||
+                        (t == 0 && !mbar_wait_sleep(&sh.v_full[s], (n >> 1) & 1))) {
                         ok = false;
                         break;
                     }
@@ -308,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (ok) {
                 tc_commit(&sh.o_full);
-                mbar_wait(&sh.o_full, 0);  // every MMA done before TMEM is released
+                mbar_wait_sleep(&sh.o_full, 0);  // every MMA done before TMEM is released
             } else {
                 set_err(p.dev_err, HSA_DEVERR_TIMEOUT);
             }
@@ -331,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         bool ok = true;
         for (int n = 0; n < sc.nt && tile_ok; ++n) {
-            if (!mbar_wait(&sh.s_full[t], n & 1)) {
+            if (!mbar_wait_sleep(&sh.s_full[t], n & 1)) {
                 set_err(p.dev_err, HSA_DEVERR_TIMEOUT);
                 ok = false;
                 break;
@@ -459,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(&sh.p_full[t]);
         }
         // ---- epilogue: O / l -> bf16 ------------------------------------------
-        if (tile_ok && ok && mbar_wait(&sh.o_full, 0)) {
+        if (tile_ok && ok && mbar_wait_sleep(&sh.o_full, 0)) {
             tc_fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;
             __nv_bfloat16 *dst = p.out + ((int64_t)(row0 + t * kBM + row) * p.Hq + hq) * kD;
