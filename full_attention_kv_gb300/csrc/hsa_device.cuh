@@ -329,6 +329,25 @@ __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint
         : "memory");
 }
 
+// The same with the accumulate flag fixed at compile time (kAcc 0 or 1): no
+// predicate is computed per MMA, which keeps an issuing thread's instruction count
+// per MMA at its minimum.
+template <int kAcc>
+__device__ __forceinline__ void tc_mma_ss_k(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc)
+{
+    asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, %4;" ::"r"(d_tmem), "l"(a_desc),
+                 "l"(b_desc), "r"(idesc), "n"(kAcc)
+                 : "memory");
+}
+
+template <int kAcc>
+__device__ __forceinline__ void tc_mma_ts_k(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc)
+{
+    asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, %4;" ::"r"(d_tmem), "r"(a_tmem),
+                 "l"(b_desc), "r"(idesc), "n"(kAcc)
+                 : "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
@@ -360,6 +379,24 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 
 // Shared-memory matrix descriptor for tcgen05.mma (128-byte swizzle, version 1):
 // start address, leading and stride byte offsets are encoded in 16-byte units.
+// The two 32-bit halves of smem_desc_sw128, for issuers that keep the high half
+// fixed and step the start address in the low half (start + k is a plain 32-bit
+// add while the address field does not overflow, i.e. below 256 KB).
+__device__ __forceinline__ uint32_t smem_desc_sw128_lo(uint32_t saddr, uint32_t lbo)
+{
+    return ((saddr & 0x3FFFFu) >> 4) | (((lbo >> 4) & 0x3FFFu) << 16);
+}
+
+__host__ __device__ constexpr uint32_t smem_desc_sw128_hi(uint32_t sbo)
+{
+    return ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
+}
+
+__device__ __forceinline__ uint64_t desc_join(uint32_t lo, uint32_t hi)
+{
+    return ((uint64_t)hi << 32) | lo;
+}
+
 __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo)
 {
     return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |

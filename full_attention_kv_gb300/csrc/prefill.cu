@@ -252,26 +252,42 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t id_pv = idesc_bf16_f32(kBM, kD, 0, 1);
             const int ntile = has_b ? 2 : 1;
             bool ok = mbar_wait_sleep(&sh.q_full, 0);
-            // S_t = Q_t K_n^T into TMEM columns t * 128
+            // Descriptor low words of every operand tile (the high word is common:
+            // SBO 1024, version 1, 128-byte swizzle); a k-step adds a constant to the
+            // low word, so each MMA costs the issuing thread one or two integer adds
+            const uint32_t dhi = smem_desc_sw128_hi(1024);
+            const uint32_t q_lo[2] = {smem_desc_sw128_lo(smem_u32(sh.q[0]), 16),
+                                      smem_desc_sw128_lo(smem_u32(sh.q[1]), 16)};
+            const uint32_t k_lo[2] = {smem_desc_sw128_lo(smem_u32(sh.k[0]), 16),
+                                      smem_desc_sw128_lo(smem_u32(sh.k[1]), 16)};
+            const uint32_t v_lo[2] = {smem_desc_sw128_lo(smem_u32(sh.v[0]), kHalfBytes),
+                                      smem_desc_sw128_lo(smem_u32(sh.v[1]), kHalfBytes)};
+            // S_t = Q_t K_n^T into TMEM columns t * 128 (k-step ks: 16 d-columns, i.e.
+            // 32 bytes inside a 128-byte swizzle row, 64 columns per 16 KB block)
             auto issue_s = [&](int t, int n) {
-                const uint32_t sq = smem_u32(sh.q[t]);
-                const uint32_t sk = smem_u32(sh.k[n & 1]);
+                const uint32_t qa = t ? q_lo[1] : q_lo[0];
+                const uint32_t kb = (n & 1) ? k_lo[1] : k_lo[0];
+                const uint32_t d = tmem + t * 128;
+                tc_mma_ss_k<0>(d, desc_join(qa, dhi), desc_join(kb, dhi), id_s);
 #pragma unroll
-                for (int ks = 0; ks < kD / 16; ++ks) {
-                    const uint32_t off = (ks >> 2) * kHalfBytes + (ks & 3) * 32;
-                    tc_mma_ss(tmem + t * 128, smem_desc_sw128(sq + off, 16, 1024),
-                              smem_desc_sw128(sk + off, 16, 1024), id_s, ks > 0 ? 1u : 0u);
+                for (int ks = 1; ks < kD / 16; ++ks) {
+                    const uint32_t off = (ks >> 2) * (kHalfBytes >> 4) + (ks & 3) * 2;
+                    tc_mma_ss_k<1>(d, desc_join(qa + off, dhi), desc_join(kb + off, dhi), id_s);
                 }
                 tc_commit(&sh.s_full[t]);
             };
-            // O_t += P_t V_n, P_t read from TMEM over S_t
+            // O_t += P_t V_n, P_t read from TMEM over S_t (k-step ks: 16 keys = 8 TMEM
+            // columns of bf16 pairs, and 16 rows = 2048 bytes of the MN-major V tile)
             auto issue_pv = [&](int t, int n) {
-                const uint32_t sv = smem_u32(sh.v[n & 1]);
+                const uint32_t vb = (n & 1) ? v_lo[1] : v_lo[0];
+                const uint32_t d = tmem + kColO + t * 128, a = tmem + t * 128;
+                if (n > 0)
+                    tc_mma_ts_k<1>(d, a, desc_join(vb, dhi), id_pv);
+                else
+                    tc_mma_ts_k<0>(d, a, desc_join(vb, dhi), id_pv);
 #pragma unroll
-                for (int ks = 0; ks < kBN / 16; ++ks)
-                    tc_mma_ts(tmem + kColO + t * 128, tmem + t * 128 + ks * 8,
-                              smem_desc_sw128(sv + ks * 2048, kHalfBytes, 1024), id_pv,
-                              (n > 0 || ks > 0) ? 1u : 0u);
+                for (int ks = 1; ks < kBN / 16; ++ks)
+                    tc_mma_ts_k<1>(d, a + ks * 8, desc_join(vb + ks * (2048 >> 4), dhi), id_pv);
             };
             if (ok && (ok = mbar_wait_sleep(&sh.k_full[0], 0))) {
                 tc_fence_after();
