@@ -620,7 +620,7 @@ def _ctx_desc(cfg):
 # on the current kernel).
 TRAFFIC = {
     # profiles/decode_full_ncu_decode-b4.md: 389.5 MB on 4 sequences, scaled by units
-    "decode": ("c30f7c331a4ae7f6", 2832277051),
+    "decode": ("5bb42670f6f357ac", 2831917823),
     # profiles/prefill_full_ncu_prefill-r2.md: 5.846 GB on 2 requests, scaled by flops
     "prefill": ("86e2430f370d57d3", 18418300622),
 }
