@@ -376,14 +376,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!row_ok)
                 hi = 0;
             const bool whole_tile = !ring && lo == 0 && hi == kBN && ok0 && ok1;
-            // ring slot s holds the latest prefix position below P congruent to s mod W
-            const int lo_pos = max(0, P + i - p.W + 1);
+            // ring slot s holds the latest prefix position below P congruent to s mod W,
+            // P - 1 - back(s) with back(s) = (r0 - s) mod W and r0 = (P - 1) mod W; the
+            // row sees it iff that position is >= max(0, P + i - W + 1), i.e. back <= lim
+            const int r0 = ring ? (P - 1) % p.W : 0;
+            const int lim = (row_ok && ring_row_ok) ? P - 1 - max(0, P + i - p.W + 1) : -1;
             auto vis = [&](int key) -> bool {
                 if (ring) {
                     const int slot = n * kBN + key;
-                    int back = (P - 1 - slot) % p.W;
-                    back += back < 0 ? p.W : 0;
-                    return row_ok && ring_row_ok && slot < p.W && P - 1 - back >= lo_pos;
+                    const int back = r0 - slot + (slot > r0 ? p.W : 0);
+                    return slot < p.W && back <= lim;
                 }
                 return key >= lo && key < hi && (key < 64 ? ok0 : ok1);
             };
