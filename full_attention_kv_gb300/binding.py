@@ -16,6 +16,7 @@ HSA_OK = 0
 HSA_INVALID_ARG = 1
 HSA_UNSUPPORTED_SHAPE = 2
 HSA_CUDA_ERROR = 3
+HSA_OUT_OF_RANGE = 4
 
 HSA_DEVERR_BAD_BLOCK = 1
 HSA_DEVERR_BAD_PAGE = 2
@@ -29,6 +30,10 @@ EXPORTS = ("hsa_kv_append", "hsa_decode_workspace_bytes", "hsa_decode_attn",
            "hsa_decode_attn_append", "hsa_decode_attn_noalloc", "hsa_prefill_attn",
            "hsa_swa_prefetch",
            "hsa_window_safe_len", "hsa_window_safe_len_bitmap", "hsa_status_string")
+# every symbol include/hsa_tree.h declares
+TREE_EXPORTS = ("hsa_ptree_create", "hsa_ptree_destroy", "hsa_ptree_match",
+                "hsa_ptree_match_batch", "hsa_ptree_insert", "hsa_ptree_unlock",
+                "hsa_ptree_evict_full", "hsa_ptree_evict_swa", "hsa_ptree_stats")
 
 
 class HsaError(RuntimeError):
@@ -94,6 +99,26 @@ def lib():
         L.hsa_window_safe_len_bitmap.argtypes = [vp, vp, vp, i32, i32, vp, vp]
         L.hsa_status_string.restype = ctypes.c_char_p
         L.hsa_status_string.argtypes = [ctypes.c_int]
+        i64, pi32 = ctypes.c_int64, ctypes.POINTER(ctypes.c_int32)
+        L.hsa_ptree_create.restype = ctypes.c_int
+        L.hsa_ptree_create.argtypes = [i32, i32, ctypes.POINTER(vp)]
+        L.hsa_ptree_destroy.restype = None
+        L.hsa_ptree_destroy.argtypes = [vp]
+        L.hsa_ptree_match.restype = ctypes.c_int
+        L.hsa_ptree_match.argtypes = [vp, vp, i32, i32, i32, pi32, vp, pi32, vp,
+                                      ctypes.POINTER(i64)]
+        L.hsa_ptree_match_batch.restype = ctypes.c_int
+        L.hsa_ptree_match_batch.argtypes = [vp, vp, vp, i32, vp, vp, vp]
+        L.hsa_ptree_insert.restype = ctypes.c_int
+        L.hsa_ptree_insert.argtypes = [vp, vp, vp, i32, i32, vp, vp, pi32, pi32]
+        L.hsa_ptree_unlock.restype = ctypes.c_int
+        L.hsa_ptree_unlock.argtypes = [vp, i64]
+        L.hsa_ptree_evict_full.restype = ctypes.c_int
+        L.hsa_ptree_evict_full.argtypes = [vp, i32, vp, i32, pi32, vp, i32, pi32]
+        L.hsa_ptree_evict_swa.restype = ctypes.c_int
+        L.hsa_ptree_evict_swa.argtypes = [vp, i32, vp, pi32]
+        L.hsa_ptree_stats.restype = ctypes.c_int
+        L.hsa_ptree_stats.argtypes = [vp, ctypes.POINTER(i64), pi32, pi32]
         _lib = L
     return _lib
 
@@ -350,3 +375,123 @@ def hsa_window_safe_len_bitmap(match_len, live_off, live, W, out=None, stream=No
                                          _ptr(out), _stream(stream))
     _check("hsa_window_safe_len_bitmap", s)
     return out
+
+
+def _i32_host(a, name):
+    """A contiguous host int32 tensor view of a sequence of ints (or a tensor)."""
+    t = torch.as_tensor(a, dtype=torch.int32)
+    if t.is_cuda:
+        raise ValueError("%s must be host memory" % name)
+    return t.contiguous().view(-1)
+
+
+class PrefixTree:
+    """Host prefix tree of include/hsa_tree.h (Full index + SWA ring liveness).
+
+    Methods mirror the C calls; token and slot arrays are host int32.
+    ``window_safe(...)`` matches a batch on the host and computes every request's
+    window-safe length on the GPU with hsa_window_safe_len.
+    """
+
+    def __init__(self, W, n_ring_rows):
+        self.W = int(W)
+        h = ctypes.c_void_p()
+        _check("hsa_ptree_create", lib().hsa_ptree_create(self.W, int(n_ring_rows),
+                                                           ctypes.byref(h)))
+        self._h = h
+
+    def close(self):
+        if self._h is not None and self._h.value:
+            lib().hsa_ptree_destroy(self._h)
+        self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def match(self, tokens, lock=False, take_ring=False):
+        """-> (match_len, full_slots[match_len], ring_row, swa_slot_pos[W], lock_handle)."""
+        tok = _i32_host(tokens, "tokens")
+        n = tok.numel()
+        slots = torch.empty(max(n, 1), dtype=torch.int32)
+        pos = torch.empty(self.W, dtype=torch.int32)
+        m, r, hnd = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int64()
+        _check("hsa_ptree_match", lib().hsa_ptree_match(
+            self._h, ctypes.c_void_p(tok.data_ptr()), n, int(bool(lock)), int(bool(take_ring)),
+            ctypes.byref(m), ctypes.c_void_p(slots.data_ptr()), ctypes.byref(r),
+            ctypes.c_void_p(pos.data_ptr()), ctypes.byref(hnd)))
+        return m.value, slots[:m.value].clone(), r.value, pos, hnd.value
+
+    def match_batch(self, seqs):
+        """-> (match_len [n], ring_row [n], swa_slot_pos [n, W]) host int32, read-only."""
+        lens = [len(x) for x in seqs]
+        off = torch.zeros(len(seqs) + 1, dtype=torch.int64)
+        if seqs:
+            off[1:] = torch.cumsum(torch.tensor(lens, dtype=torch.int64), 0)
+        flat = _i32_host([int(v) for x in seqs for v in x], "tokens")
+        n = len(seqs)
+        m = torch.empty(max(n, 1), dtype=torch.int32)
+        r = torch.empty(max(n, 1), dtype=torch.int32)
+        pos = torch.empty(max(n, 1), self.W, dtype=torch.int32)
+        _check("hsa_ptree_match_batch", lib().hsa_ptree_match_batch(
+            self._h, ctypes.c_void_p(flat.data_ptr()) if flat.numel() else None,
+            ctypes.c_void_p(off.data_ptr()), n, ctypes.c_void_p(m.data_ptr()),
+            ctypes.c_void_p(r.data_ptr()), ctypes.c_void_p(pos.data_ptr())))
+        return m[:n], r[:n], pos[:n]
+
+    def window_safe(self, seqs, device="cuda", stream=None):
+        """Window-safe length of each request: host match, one GPU launch."""
+        m, r, pos = self.match_batch(seqs)
+        if m.numel() == 0:
+            return m
+        out = hsa_window_safe_len(m.to(device), pos.to(device), self.W, stream=stream)
+        return out.cpu()
+
+    def insert(self, tokens, full_slots, ring_row=-1, swa_slot_pos=None):
+        """-> (dup_slots to free, ring_kept)."""
+        tok = _i32_host(tokens, "tokens")
+        sl = _i32_host(full_slots, "full_slots")
+        if tok.numel() != sl.numel():
+            raise ValueError("tokens and full_slots differ in length")
+        n = tok.numel()
+        pos = None
+        if ring_row >= 0:
+            pos = _i32_host(swa_slot_pos, "swa_slot_pos")
+            if pos.numel() != self.W:
+                raise ValueError("swa_slot_pos must hold W entries")
+        dup = torch.empty(max(n, 1), dtype=torch.int32)
+        nd, kept = ctypes.c_int32(), ctypes.c_int32()
+        _check("hsa_ptree_insert", lib().hsa_ptree_insert(
+            self._h, ctypes.c_void_p(tok.data_ptr()), ctypes.c_void_p(sl.data_ptr()), n,
+            int(ring_row), None if pos is None else ctypes.c_void_p(pos.data_ptr()),
+            ctypes.c_void_p(dup.data_ptr()), ctypes.byref(nd), ctypes.byref(kept)))
+        return dup[:nd.value].clone(), bool(kept.value)
+
+    def unlock(self, handle):
+        _check("hsa_ptree_unlock", lib().hsa_ptree_unlock(self._h, int(handle)))
+
+    def evict_full(self, n_tokens, slot_cap=1 << 20, row_cap=1 << 16):
+        """-> (freed Full slots, freed ring rows)."""
+        fs = torch.empty(max(slot_cap, 1), dtype=torch.int32)
+        fr = torch.empty(max(row_cap, 1), dtype=torch.int32)
+        ns, nr = ctypes.c_int32(), ctypes.c_int32()
+        _check("hsa_ptree_evict_full", lib().hsa_ptree_evict_full(
+            self._h, int(n_tokens), ctypes.c_void_p(fs.data_ptr()), int(slot_cap),
+            ctypes.byref(ns), ctypes.c_void_p(fr.data_ptr()), int(row_cap), ctypes.byref(nr)))
+        return fs[:ns.value].clone(), fr[:nr.value].clone()
+
+    def evict_swa(self, n_rows):
+        fr = torch.empty(max(int(n_rows), 1), dtype=torch.int32)
+        nf = ctypes.c_int32()
+        _check("hsa_ptree_evict_swa", lib().hsa_ptree_evict_swa(
+            self._h, int(n_rows), ctypes.c_void_p(fr.data_ptr()), ctypes.byref(nf)))
+        return fr[:nf.value].clone()
+
+    def stats(self):
+        """-> (cached tokens, ring rows held, nodes)."""
+        c, rh, nn = ctypes.c_int64(), ctypes.c_int32(), ctypes.c_int32()
+        _check("hsa_ptree_stats", lib().hsa_ptree_stats(self._h, ctypes.byref(c),
+                                                        ctypes.byref(rh), ctypes.byref(nn)))
+        return c.value, rh.value, nn.value

@@ -120,6 +120,8 @@ const char *hsa_status_string(hsa_status s)
         return "unsupported shape";
     case HSA_CUDA_ERROR:
         return "CUDA error";
+    case HSA_OUT_OF_RANGE:
+        return "buffer too small";
     default:
         return "unknown status";
     }

@@ -46,6 +46,7 @@ typedef int hsa_status;
 #define HSA_INVALID_ARG 1        /* null pointer, negative size, bad layer index */
 #define HSA_UNSUPPORTED_SHAPE 2  /* head_dim != 128, page != 64, W not a multiple of 64, ... */
 #define HSA_CUDA_ERROR 3         /* a CUDA runtime call failed (launch, attribute, ...) */
+#define HSA_OUT_OF_RANGE 4       /* a caller buffer is too small for the result (host calls) */
 
 /* bits OR-ed into *dev_err by the kernels */
 #define HSA_DEVERR_BAD_BLOCK 1   /* block-table entry outside [0, num_blocks) */

@@ -7,8 +7,8 @@ import re
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
-def _declared():
-    src = open(os.path.join(ROOT, "include", "hsa.h"), encoding="utf-8").read()
+def _declared(header="hsa.h"):
+    src = open(os.path.join(ROOT, "include", header), encoding="utf-8").read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     return sorted(set(re.findall(r"\b(hsa_[a-z_]+)\s*\(", src)))
 
@@ -21,6 +21,16 @@ def test_library_exports_every_declared_symbol():
     assert "hsa_decode_attn" in names and "hsa_kv_append" in names
     for n in names:
         assert hasattr(L, n), n
+
+
+def test_library_exports_the_tree_header():
+    import full_attention_kv_gb300 as hsa
+    L = ctypes.CDLL(hsa.build.build() if hasattr(hsa, "build") else hsa.binding.LIB_PATH)
+    names = _declared("hsa_tree.h")
+    assert "hsa_ptree_match_batch" in names
+    for n in names:
+        assert hasattr(L, n), n
+    assert sorted(hsa.TREE_EXPORTS) == names
 
 
 def test_binding_covers_the_header():
