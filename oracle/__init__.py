@@ -60,6 +60,18 @@ def lib():
                                    ctypes.c_double]
         L.orc_num_threads.restype = ctypes.c_int
         L.orc_num_threads.argtypes = []
+        fp = ctypes.POINTER(ctypes.c_float)
+        L.orc_e4m3_value.restype = ctypes.c_double
+        L.orc_e4m3_value.argtypes = [ctypes.c_uint8]
+        L.orc_e4m3_encode.restype = ctypes.c_uint8
+        L.orc_e4m3_encode.argtypes = [ctypes.c_float]
+        L.orc_quantize_e4m3.restype = None
+        L.orc_quantize_e4m3.argtypes = [ctypes.c_int64, ctypes.c_int, u16p, u8p, fp]
+        L.orc_attention_fp8hist.restype = ctypes.c_int
+        L.orc_attention_fp8hist.argtypes = [
+            ctypes.c_int, i32p, i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+            u16p, u16p, u16p, u8p, fp, u8p, fp, i64p, ctypes.c_int64, i32p, i32p, dp,
+            ctypes.c_int]
         _lib = L
     return _lib
 
@@ -212,3 +224,75 @@ def kv_ratio(layer_is_full, W, L):
     """KV bytes of the hybrid stack over an all-full stack of the same depth."""
     n = len(layer_is_full)
     return kv_bytes(layer_is_full, W, L, 1.0) / kv_bytes([1] * n, W, L, 1.0)
+
+
+# ---------------------------------------------------------------- FP8 KV (E4M3)
+# hotdry.top "MiMo inference optimization, edge deployment": FP8 KV with
+# quantisation groups aligned to the window; one fp32 scale per (position, KV
+# head) row here.  Arithmetic in hsa_oracle.c.
+
+def e4m3_value(code):
+    """Value of one E4M3 code (OCP 8-bit float, bias 7, no infinities)."""
+    return float(lib().orc_e4m3_value(int(code) & 0xFF))
+
+
+def e4m3_encode(x):
+    """Nearest finite E4M3 code of a float32 value (ties to even, saturating)."""
+    return int(lib().orc_e4m3_encode(float(np.float32(x))))
+
+
+def quantize_e4m3(rows):
+    """bf16 rows [..., d] -> (codes uint8 [..., d], scales float32 [...])."""
+    xb = bf16_bits(rows)
+    shape = xb.shape
+    d = shape[-1]
+    flat = _c(xb.reshape(-1, d), np.uint16)
+    n = flat.shape[0]
+    codes = np.zeros((max(n, 1), d), np.uint8)
+    scales = np.zeros(max(n, 1), np.float32)
+    if n:
+        lib().orc_quantize_e4m3(n, d, _p(flat, ctypes.c_uint16), _p(codes, ctypes.c_uint8),
+                                _p(scales, ctypes.c_float))
+    return codes[:n].reshape(shape), scales[:n].reshape(shape[:-1])
+
+
+def attention_fp8hist(cu_rows, prefix_len, q, k_new, v_new, hk, hks, hv, hvs, hist_off, scale,
+                      items=None, nthreads=None):
+    """Full causal attention of new rows over an FP8 history (codes + scales,
+    dequantised exactly in float64) followed by the bf16 new rows.  History of
+    request r: rows hist_off[r]:hist_off[r+1] = positions 0 .. prefix_len[r]-1."""
+    L = lib()
+    qb, kb, vb = bf16_bits(q), bf16_bits(k_new), bf16_bits(v_new)
+    rows, Hq, d = qb.shape
+    Hkv = kb.shape[1]
+    cu, pl, ho = _c(cu_rows, np.int32), _c(prefix_len, np.int32), _c(hist_off, np.int64)
+    R = len(pl)
+    hk, hv = _c(hk, np.uint8), _c(hv, np.uint8)
+    hks, hvs = _c(hks, np.float32), _c(hvs, np.float32)
+    if hk.size == 0:
+        hk = np.zeros((1, Hkv, d), np.uint8)
+        hv = np.zeros((1, Hkv, d), np.uint8)
+        hks = np.zeros((1, Hkv), np.float32)
+        hvs = np.zeros((1, Hkv), np.float32)
+    if items is None:
+        n = -1
+        out = np.zeros((rows, Hq, d), np.float64)
+        ir = ih = np.zeros(1, np.int32)
+    else:
+        it = _c(items, np.int32).reshape(-1, 2)
+        n = it.shape[0]
+        out = np.zeros((n, d), np.float64)
+        ir, ih = _c(it[:, 0], np.int32), _c(it[:, 1], np.int32)
+        if n == 0:
+            return out
+    nt = num_threads() if nthreads is None else int(nthreads)
+    fp = ctypes.c_float
+    rc = L.orc_attention_fp8hist(
+        R, _p(cu, ctypes.c_int32), _p(pl, ctypes.c_int32), Hq, Hkv, d, float(scale),
+        _p(qb, ctypes.c_uint16), _p(kb, ctypes.c_uint16), _p(vb, ctypes.c_uint16),
+        _p(hk, ctypes.c_uint8), _p(hks, fp), _p(hv, ctypes.c_uint8), _p(hvs, fp),
+        _p(ho, ctypes.c_int64), n, _p(ir, ctypes.c_int32), _p(ih, ctypes.c_int32),
+        _p(out, ctypes.c_double), nt)
+    if rc != 0:
+        raise ValueError("oracle fp8 attention failed: %d" % rc)
+    return out

@@ -338,3 +338,185 @@ double orc_kv_bytes(int n_layers, const uint8_t *is_full, int W, int64_t L,
         tokens += is_full[l] ? (double)L : (double)(L < W ? L : W);
     return tokens * bytes_per_token;
 }
+
+/* ------------------------------------------------------------------------- */
+/* FP8 KV Pool variant.
+ * [P5] hotdry.top "MiMo inference optimization, edge deployment", sections
+ *      "KV Cache 量化策略的技术选型" (quantisation groups aligned to the window so
+ *      that no group straddles a window boundary) and "边缘部署的工程权衡与参数清单"
+ *      (FP8 as a baseline KV format; the newest 128 tokens kept at the original
+ *      precision).
+ * Readings: the Full KV Pool holds E4M3 codes with one fp32 scale per (position,
+ * KV head) row of d values -- a group of one token never crosses a window
+ * boundary; the SWA ring, which holds exactly the newest W = 128 tokens, stays
+ * bf16.  scale = amax / 448 (fp32 division), code = E4M3 of x / scale (fp32
+ * division), all codes 0 and scale 0 for an all-zero row.
+ *
+ * E4M3 (OCP 8-bit floating point): sign bit, 4 exponent bits with bias 7, 3
+ * mantissa bits, subnormals at exponent field 0, no infinities, 0x7F / 0xFF are
+ * NaN; the largest finite magnitude is 448.                                    */
+double orc_e4m3_value(uint8_t c)
+{
+    const int e = (c >> 3) & 15, m = c & 7;
+    if (e == 15 && m == 7)
+        return NAN;
+    double v = e == 0 ? ldexp((double)m / 8.0, -6) : ldexp(1.0 + (double)m / 8.0, e - 7);
+    return (c & 0x80) ? -v : v;
+}
+
+/* The finite code nearest to x, ties to the code with an even mantissa; beyond
+ * the largest finite magnitude the result saturates to +-448.  Plain search over
+ * the 127 non-negative finite codes.                                          */
+uint8_t orc_e4m3_encode(float x)
+{
+    const double a = fabs((double)x);
+    int best = 0;
+    double best_err = INFINITY;
+    for (int c = 0; c <= 126; ++c) {
+        const double err = fabs(orc_e4m3_value((uint8_t)c) - a);
+        if (err < best_err || (err == best_err && (c & 1) == 0 && (best & 1) == 1)) {
+            best = c;
+            best_err = err;
+        }
+    }
+    return (uint8_t)(signbit(x) ? (best | 0x80) : best);
+}
+
+/* Quantise rows of d bf16 values: codes [rows, d], scales [rows].            */
+void orc_quantize_e4m3(int64_t rows, int d, const uint16_t *x, uint8_t *codes, float *scales)
+{
+    for (int64_t r = 0; r < rows; ++r) {
+        float amax = 0.0f;
+        for (int c = 0; c < d; ++c) {
+            const float v = fabsf((float)bf16_to_double(x[r * d + c]));
+            if (v > amax)
+                amax = v;
+        }
+        const float scale = amax / 448.0f;
+        scales[r] = amax > 0.0f ? scale : 0.0f;
+        for (int c = 0; c < d; ++c) {
+            const float v = (float)bf16_to_double(x[r * d + c]);
+            codes[r * d + c] = amax > 0.0f ? orc_e4m3_encode(v / scale) : 0;
+        }
+    }
+}
+
+/* attend_row for an FP8 history: keys / values with index < n_hist are
+ * (codes, scale) rows dequantised exactly to double; the rest are bf16 rows.   */
+static void attend_row_fp8(const double *q, int d, double scale, int nkeys, int n_hist,
+                           const uint8_t *const *kc, const float *ks, const uint8_t *const *vc,
+                           const float *vs, const uint16_t *const *krow,
+                           const uint16_t *const *vrow, double *score, double *out)
+{
+    double mx = -INFINITY;
+    for (int j = 0; j < nkeys; ++j) {
+        double s = 0.0;
+        for (int c = 0; c < d; ++c)
+            s += q[c] * (j < n_hist ? orc_e4m3_value(kc[j][c]) * (double)ks[j]
+                                    : bf16_to_double(krow[j][c]));
+        s *= scale;
+        score[j] = s;
+        if (s > mx)
+            mx = s;
+    }
+    double den = 0.0;
+    for (int j = 0; j < nkeys; ++j) {
+        score[j] = exp(score[j] - mx);
+        den += score[j];
+    }
+    for (int c = 0; c < d; ++c)
+        out[c] = 0.0;
+    for (int j = 0; j < nkeys; ++j) {
+        const double w = score[j] / den;
+        for (int c = 0; c < d; ++c)
+            out[c] += w * (j < n_hist ? orc_e4m3_value(vc[j][c]) * (double)vs[j]
+                                      : bf16_to_double(vrow[j][c]));
+    }
+}
+
+/*
+ * Full causal attention of T new rows per sequence on top of an FP8 history:
+ * decode / MTP verify on an FP8 Full KV Pool.  Sequence r has prefix_len[r]
+ * cached positions, history rows hist_off[r] .. hist_off[r+1]-1 holding positions
+ * 0 .. prefix_len[r]-1 as codes [rows, Hkv, d] with scales [rows, Hkv]; its new
+ * rows cu_rows[r] .. cu_rows[r+1]-1 (bf16) sit at positions prefix_len[r] + i.
+ * Items as in orc_attention.  Returns 0, or -2 on bad arguments.
+ */
+int orc_attention_fp8hist(int R, const int32_t *cu_rows, const int32_t *prefix_len, int Hq,
+                          int Hkv, int d, double scale, const uint16_t *q,
+                          const uint16_t *k_new, const uint16_t *v_new, const uint8_t *hk,
+                          const float *hks, const uint8_t *hv, const float *hvs,
+                          const int64_t *hist_off, int64_t n_items, const int32_t *item_row,
+                          const int32_t *item_head, double *out, int nthreads)
+{
+    if (R < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || d <= 0)
+        return -2;
+    const int group = Hq / Hkv;
+    const int64_t rows = cu_rows[R];
+    const int64_t total = n_items < 0 ? rows * Hq : n_items;
+    int status = 0;
+    int64_t max_keys = 1;
+    for (int r = 0; r < R; ++r) {
+        int64_t k = (int64_t)prefix_len[r] + (cu_rows[r + 1] - cu_rows[r]);
+        if (k > max_keys)
+            max_keys = k;
+        if (hist_off[r + 1] - hist_off[r] != prefix_len[r])
+            return -2;
+    }
+    if (nthreads <= 0)
+        nthreads = 1;
+#pragma omp parallel num_threads(nthreads)
+    {
+        const uint8_t **kc = (const uint8_t **)malloc(sizeof(*kc) * max_keys);
+        const uint8_t **vc = (const uint8_t **)malloc(sizeof(*vc) * max_keys);
+        float *ks = (float *)malloc(sizeof(float) * max_keys);
+        float *vs = (float *)malloc(sizeof(float) * max_keys);
+        const uint16_t **krow = (const uint16_t **)malloc(sizeof(*krow) * max_keys);
+        const uint16_t **vrow = (const uint16_t **)malloc(sizeof(*vrow) * max_keys);
+        double *score = (double *)malloc(sizeof(double) * max_keys);
+        double *qd = (double *)malloc(sizeof(double) * d);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t it = 0; it < total; ++it) {
+            const int64_t row = n_items < 0 ? it / Hq : item_row[it];
+            const int h = n_items < 0 ? (int)(it % Hq) : item_head[it];
+            double *o = out + it * d;
+            if (row < 0 || row >= rows || h < 0 || h >= Hq) {
+#pragma omp atomic write
+                status = -2;
+                continue;
+            }
+            int r = 0;
+            while (r + 1 < R && cu_rows[r + 1] <= row)
+                ++r;
+            const int64_t P = prefix_len[r];
+            const int64_t p = P + (row - cu_rows[r]);
+            const int kv = h / group;
+            int nk = 0;
+            for (int64_t x = 0; x <= p; ++x, ++nk) {
+                if (x < P) {
+                    const int64_t hr = hist_off[r] + x;
+                    kc[nk] = hk + (hr * Hkv + kv) * d;
+                    vc[nk] = hv + (hr * Hkv + kv) * d;
+                    ks[nk] = hks[hr * Hkv + kv];
+                    vs[nk] = hvs[hr * Hkv + kv];
+                } else {
+                    const int64_t nr = cu_rows[r] + (x - P);
+                    krow[nk] = k_new + (nr * Hkv + kv) * d;
+                    vrow[nk] = v_new + (nr * Hkv + kv) * d;
+                }
+            }
+            for (int c = 0; c < d; ++c)
+                qd[c] = bf16_to_double(q[(row * Hq + h) * d + c]);
+            attend_row_fp8(qd, d, scale, nk, (int)P, kc, ks, vc, vs, krow, vrow, score, o);
+        }
+        free(kc);
+        free(vc);
+        free(ks);
+        free(vs);
+        free(krow);
+        free(vrow);
+        free(score);
+        free(qd);
+    }
+    return status;
+}

@@ -406,3 +406,104 @@ def test_kv_ratio_reproduces_the_pages_one_seventh():
         prev = r
     # bytes per token per layer: K and V, 4 KV heads, d = 128, bf16
     assert oracle.kv_bytes([1], W, 1, 2 * 4 * 128 * 2) == 2048.0
+
+
+# ---------------------------------------------------------------- FP8 (E4M3) KV
+# hotdry.top "MiMo inference optimization, edge deployment", "KV Cache 量化策略的技术选型":
+# FP8 KV; the E4M3 values follow the OCP 8-bit floating point definition (bias 7,
+# 3 mantissa bits, no infinities, largest finite 448).
+
+def test_e4m3_hand_values():
+    enc = oracle.e4m3_encode
+    assert enc(448.0) == 0x7E and enc(1.0) == 0x38 and enc(-2.0) == 0xC0
+    assert enc(2.0 ** -9) == 0x01            # smallest subnormal
+    assert enc(2.0 ** -10) == 0x00           # tie with 0 -> even code
+    assert enc(1.0625) == 0x38               # tie between 1 and 1.125 -> even
+    assert enc(1.1875) == 0x3A               # tie between 1.125 and 1.25 -> even
+    assert enc(500.0) == 0x7E and enc(-1e9) == 0xFE   # saturating
+    assert enc(-0.0) == 0x80 and enc(0.0) == 0x00
+    assert oracle.e4m3_value(0x7E) == 448.0 and oracle.e4m3_value(0x01) == 2.0 ** -9
+    assert np.isnan(oracle.e4m3_value(0x7F)) and np.isnan(oracle.e4m3_value(0xFF))
+
+
+def test_e4m3_round_trip_and_order():
+    finite = [c for c in range(256) if c not in (0x7F, 0xFF)]
+    for c in finite:
+        assert oracle.e4m3_encode(oracle.e4m3_value(c)) == c, hex(c)
+    pos = [oracle.e4m3_value(c) for c in range(0x7F)]
+    assert all(a < b for a, b in zip(pos, pos[1:]))   # codes 0..126 are increasing
+
+
+def test_e4m3_matches_torch_cast():
+    """A library routine: torch's float8_e4m3fn cast (round to nearest even)."""
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("no float8 dtype in this torch")
+    rng = np.random.default_rng(8)
+    x = np.concatenate([rng.standard_normal(3000) * 40, rng.standard_normal(1000) * 0.01,
+                        rng.uniform(-448, 448, 1000)]).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.e4m3_encode(v) for v in x], np.uint8)
+    assert np.array_equal(got, ref)
+
+
+def test_quantize_rows_scale_and_extremes():
+    torch = pytest.importorskip("torch")
+    g = torch.Generator().manual_seed(9)
+    x = torch.randn(64, 128, generator=g).to(torch.bfloat16)
+    x[3] = 0
+    codes, scales = oracle.quantize_e4m3(x)
+    xf = x.float().numpy()
+    amax = np.abs(xf).max(axis=1).astype(np.float32)
+    assert np.array_equal(scales, (amax / np.float32(448.0)).astype(np.float32))
+    assert scales[3] == 0 and not codes[3].any()
+    for r in range(64):
+        if r == 3:
+            continue
+        j = int(np.argmax(np.abs(xf[r])))
+        assert codes[r, j] & 0x7F == 0x7E            # the row maximum maps to 448
+        deq = np.array([oracle.e4m3_value(c) for c in codes[r]]) * scales[r]
+        # E4M3 keeps 3 mantissa bits: relative error <= 2^-4 above the subnormals
+        big = np.abs(xf[r]) > scales[r] * 2.0 ** -6
+        assert np.all(np.abs(deq - xf[r])[big] <= np.abs(xf[r])[big] * 2.0 ** -4 + 1e-12)
+
+
+def test_fp8_history_attention_equals_bf16_oracle_on_exact_values():
+    """With unit scales the dequantised history is exactly the E4M3 values, all
+    representable in bf16: orc_attention_fp8hist must equal orc_attention fed
+    those values as bf16 (both float64)."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(10)
+    Hq, Hkv, d, R = 8, 2, 32, 2
+    P = [13, 40]
+    T = [1, 3]
+    hist = sum(P)
+    codes_k = rng.integers(0, 0x7F, (hist, Hkv, d)).astype(np.uint8) | \
+        (rng.integers(0, 2, (hist, Hkv, d)).astype(np.uint8) << 7)
+    codes_k[codes_k == 0xFF] = 0xFE
+    codes_v = rng.integers(0x20, 0x50, (hist, Hkv, d)).astype(np.uint8)
+    ones = np.ones((hist, Hkv), np.float32)
+    val_k = np.vectorize(oracle.e4m3_value)(codes_k).astype(np.float32)
+    val_v = np.vectorize(oracle.e4m3_value)(codes_v).astype(np.float32)
+    bk = torch.from_numpy(val_k).to(torch.bfloat16)
+    bv = torch.from_numpy(val_v).to(torch.bfloat16)
+    assert np.array_equal(bk.float().numpy(), val_k)   # exactly representable
+    rows = sum(T)
+    g = torch.Generator().manual_seed(11)
+    q = (torch.randn(rows, Hq, d, generator=g) * 0.05).to(torch.bfloat16)
+    kn = torch.randn(rows, Hkv, d, generator=g).to(torch.bfloat16)
+    vn = torch.randn(rows, Hkv, d, generator=g).to(torch.bfloat16)
+    cu = np.array([0, T[0], rows], np.int32)
+    pl = np.array(P, np.int32)
+    ho = np.array([0, P[0], hist], np.int64)
+    a = oracle.attention_fp8hist(cu, pl, q, kn, vn, codes_k, ones, codes_v, ones, ho, 0.3)
+    b = oracle.attention(cu, pl, q, kn, vn, bk, bv, ho, np.zeros(R, np.int32), 0, 0.3)
+    assert np.max(np.abs(a - b)) == 0.0
+    # doubling one row's scale doubles that key's dequantised values (exact)
+    two = ones.copy()
+    two[5] = 2.0
+    bk2 = torch.from_numpy(val_k * two[:, :, None]).to(torch.bfloat16)
+    bv2 = torch.from_numpy(val_v * two[:, :, None]).to(torch.bfloat16)
+    a2 = oracle.attention_fp8hist(cu, pl, q, kn, vn, codes_k, two, codes_v, two, ho, 0.3)
+    b2 = oracle.attention(cu, pl, q, kn, vn, bk2, bv2, ho, np.zeros(R, np.int32), 0, 0.3)
+    assert np.max(np.abs(a2 - b2)) == 0.0
