@@ -136,16 +136,21 @@ def max_over_ranks(x, ws, device="cuda"):
 
 
 # --------------------------------------------------------------------------- accounting
-def decode_bytes(inst, layer_full):
+def decode_bytes(inst, layer_full, fp8=False):
     """Algorithmic bytes of one decode attention launch on one layer.
 
     KV: every key some query of the step may see, once (2048 B per token per
     layer: K and V, 4 KV heads, d = 128, bf16): full layers c + T tokens, sliding
-    layers min(c + T, W + T - 1).  Plus q read and out written.
+    layers min(c + T, W + T - 1).  Plus q read and out written.  An FP8 full layer
+    holds its c cached tokens as E4M3 codes plus one fp32 scale per (token, head)
+    row: 2 * Hkv * (d + 4) bytes per token; the T new rows are read as bf16.
     """
     cfg = inst.cfg
     per_tok = 2 * cfg.Hkv * cfg.d * 2
     c = inst.prefix.astype(np.int64)
+    qo = 2 * inst.R * cfg.T * cfg.Hq * cfg.d * 2
+    if layer_full and fp8:
+        return int(c.sum()) * 2 * cfg.Hkv * (cfg.d + 4) + inst.R * cfg.T * per_tok + qo
     if layer_full:
         keys = c + cfg.T
     else:
@@ -259,15 +264,17 @@ class DecodeStep:
     """All layers: decode attention fused with the append of the step's new tokens
     (hsa_decode_attn_append, one launch per layer)."""
 
-    def __init__(self, inst, device, layers=None, swa_prefetch=False):
+    def __init__(self, inst, device, layers=None, swa_prefetch=False, kv_fp8=False):
         import full_attention_kv_gb300 as hsa
         import harness
         self.hsa = hsa
         self.inst = inst
+        self.kv_fp8 = kv_fp8
         cfg = inst.cfg
         self.model_layers = list(range(cfg.n_layers)) if layers is None else list(layers)
         self.layers = list(range(len(self.model_layers)))  # pool layer indices
-        self.pool = harness.make_pool(inst, self.model_layers, device=device, stale="zero")
+        self.pool = harness.make_pool(inst, self.model_layers, device=device, stale="zero",
+                                      fp8=kv_fp8)
         # layerwise SWA prefetch: every sliding layer's rings also live in a pinned
         # host tier and are brought back each step on a side stream
         self.prefetch = swa_prefetch
@@ -339,7 +346,8 @@ class DecodeStep:
     def dominant(self):
         """(name, [layers], algorithmic bytes per launch list)."""
         full = [i for i, l in enumerate(self.model_layers) if self.inst.full[l]]
-        return "decode_kernel (full layers)", full, [decode_bytes(self.inst, True)] * len(full)
+        name = "decode_kernel (full layers%s)" % (", FP8 KV" if self.kv_fp8 else "")
+        return name, full, [decode_bytes(self.inst, True, self.kv_fp8)] * len(full)
 
     def units_per_step(self):
         return self.inst.R * self.inst.cfg.T
@@ -462,7 +470,8 @@ def run_ours(args, inst, ws, rank, local):
     cfg = inst.cfg
     layers = None if args.layers is None else [int(x) for x in args.layers.split(",")]
     if cfg.kind == "decode":
-        step = DecodeStep(inst, device, layers, swa_prefetch=args.swa_prefetch)
+        step = DecodeStep(inst, device, layers, swa_prefetch=args.swa_prefetch,
+                          kv_fp8=args.kv_fp8)
     else:
         step = PrefillStep(inst, device, layers)
     # the attention stream runs at high priority (a side stream, if any, at the default)
@@ -588,11 +597,16 @@ def run_ours(args, inst, ws, rank, local):
         "gpu_launches": step.launches_per_step * args.steps,
     }
     line.update(extra)
+    if getattr(args, "kv_fp8", False):
+        line["dtype"] = "e4m3 Full KV Pool (fp16 MMA, fp32 accumulate), bf16 rings / q / out"
+        line["config"]["kv_fp8"] = ("full layers stored as E4M3 codes + one fp32 scale per "
+                                    "(token, KV head) row; sliding rings bf16")
+        line["roofline"]["traffic"] = None  # the ncu traffic figure is for the bf16 layers
     if prefetch_info is not None:
         line["swa_prefetch"] = prefetch_info
         line["config"]["swa_prefetch"] = ("every step reloads all sliding layers' rings from a "
                                           "pinned host tier on a side stream, layer by layer")
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and not args.no_cpu_baseline and not getattr(args, "kv_fp8", False):
         v, unit, _, cores, sample = run_reference(
             argparse.Namespace(steps=1, warmup=0), inst)
         line["cpu_baseline"] = {"value": v, "unit": unit, "cores": cores, "kind": "oracle",
@@ -650,11 +664,15 @@ def main():
     ap.add_argument("--swa-prefetch", action="store_true",
                     help="decode: reload every sliding layer's rings from pinned host memory "
                          "each step, layer by layer on a side stream")
+    ap.add_argument("--kv-fp8", action="store_true",
+                    help="decode: full layers as an FP8 (E4M3) Full KV Pool (no CPU baseline)")
     ap.add_argument("--layers", default=None,
                     help="comma-separated model layers (profiling sub-stack; default all)")
     ap.add_argument("--profile-step", action="store_true",
                     help="run one eager step inside cudaProfilerStart/Stop and exit")
     args = ap.parse_args()
+    if args.kv_fp8 and workload.CONFIGS[args.workload].kind != "decode":
+        ap.error("--kv-fp8 is a decode variant (prefill reads bf16 pools)")
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     ws, rank, local = dist_env()

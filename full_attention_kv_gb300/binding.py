@@ -60,6 +60,7 @@ class HsaPools(ctypes.Structure):
         ("Hq", ctypes.c_int32),
         ("Hkv", ctypes.c_int32),
         ("d", ctypes.c_int32),
+        ("layer_kv_fp8", ctypes.POINTER(ctypes.c_uint8)),
     ]
 
 
@@ -165,16 +166,32 @@ class DualPool:
     [batch] (int32) are shared by every layer of their kind.
     """
 
-    def __init__(self, layer_is_full, k, v, block_tables, ring_row, Hq, W=128, page=64):
+    def __init__(self, layer_is_full, k, v, block_tables, ring_row, Hq, W=128, page=64,
+                 kv_fp8=None, Hkv=None, d=None, num_blocks=None):
+        """kv_fp8[l] marks an FP8 full layer: k[l], v[l] are then flat uint8 buffers of
+        num_blocks * Hkv * page * (d + 4) bytes (E4M3 codes, then fp32 scales;
+        include/hsa.h gives the layout), and Hkv, d, num_blocks must be passed."""
         self.layer_is_full = [bool(x) for x in layer_is_full]
         self.k, self.v = list(k), list(v)
         self.block_tables, self.ring_row = block_tables, ring_row
         n = len(self.layer_is_full)
         assert len(self.k) == n and len(self.v) == n
+        self.kv_fp8 = [bool(x) for x in kv_fp8] if kv_fp8 is not None else [False] * n
+        assert len(self.kv_fp8) == n
         _need(block_tables, "block_tables", torch.int32, ndim=2)
         _need(ring_row, "ring_row", torch.int32, ndim=1)
-        d = Hkv = num_blocks = n_rows = None
+        n_rows = None
         for l in range(n):
+            if self.kv_fp8[l]:
+                if not self.layer_is_full[l]:
+                    raise ValueError("layer %d: only full layers can be FP8" % l)
+                if Hkv is None or d is None or num_blocks is None:
+                    raise ValueError("FP8 layers need Hkv, d and num_blocks")
+                for t, nm in ((self.k[l], "k"), (self.v[l], "v")):
+                    _need(t, "%s[%d]" % (nm, l), torch.uint8, ndim=1)
+                    if t.numel() != num_blocks * Hkv * page * (d + 4):
+                        raise ValueError("%s[%d]: wrong FP8 layer size" % (nm, l))
+                continue
             _need(self.k[l], "k[%d]" % l, torch.bfloat16, ndim=4)
             _need(self.v[l], "v[%d]" % l, torch.bfloat16, ndim=4)
             if self.k[l].shape != self.v[l].shape:
@@ -197,6 +214,7 @@ class DualPool:
             if hk != Hkv or dd != d:
                 raise ValueError("layers disagree on Hkv / d")
         self._full = (ctypes.c_uint8 * n)(*[1 if f else 0 for f in self.layer_is_full])
+        self._fp8 = (ctypes.c_uint8 * n)(*[1 if f else 0 for f in self.kv_fp8])
         self._k = (ctypes.c_void_p * n)(*[t.data_ptr() for t in self.k])
         self._v = (ctypes.c_void_p * n)(*[t.data_ptr() for t in self.v])
         self.c = HsaPools(
@@ -206,19 +224,42 @@ class DualPool:
             num_blocks=num_blocks or 0, page_size=page, block_tables=block_tables.data_ptr(),
             max_blocks=block_tables.shape[1], ring_row=ring_row.data_ptr(),
             n_ring_rows=n_rows or 0, batch=block_tables.shape[0], W=W, Hq=Hq, Hkv=Hkv or 0,
-            d=d or 0)
+            d=d or 0, layer_kv_fp8=ctypes.cast(self._fp8, ctypes.POINTER(ctypes.c_uint8)))
         self.Hq, self.Hkv, self.d, self.W, self.page = Hq, Hkv, d, W, page
+        self.num_blocks = num_blocks or 0
+
+    def fp8_views(self, layer):
+        """Views of an FP8 layer: (K codes [nb, Hkv, page, d] in stored byte order,
+        K scales [nb, Hkv, page] fp32, V codes [nb, Hkv, d, page] (transposed, stored
+        key order), V scales [nb, Hkv, page] fp32)."""
+        if not self.kv_fp8[layer]:
+            raise ValueError("layer %d is not FP8" % layer)
+        nb, hk, pg, dd = self.num_blocks, self.Hkv, self.page, self.d
+        cb = nb * hk * pg * dd
+        out = []
+        for buf, shape in ((self.k[layer], (nb, hk, pg, dd)), (self.v[layer], (nb, hk, dd, pg))):
+            out.append(buf[:cb].view(shape))
+            out.append(buf[cb:].view(torch.float32).view(nb, hk, pg))
+        return tuple(out)
 
     @classmethod
     def allocate(cls, layer_is_full, num_blocks, n_ring_rows, block_tables, ring_row, Hq, Hkv,
-                 d=128, W=128, page=64, device="cuda"):
-        """Zero-filled pools (rows past a sequence's length must hold finite values)."""
+                 d=128, W=128, page=64, device="cuda", kv_fp8=False):
+        """Zero-filled pools (rows past a sequence's length must hold finite values).
+        kv_fp8=True stores every full layer as an FP8 layer (sliding rings stay bf16)."""
         k, v = [], []
-        for f in layer_is_full:
+        fp8 = [bool(kv_fp8) and bool(f) for f in layer_is_full]
+        for f, q8 in zip(layer_is_full, fp8):
+            if q8:
+                nbytes = num_blocks * Hkv * page * (d + 4)
+                k.append(torch.zeros(nbytes, dtype=torch.uint8, device=device))
+                v.append(torch.zeros(nbytes, dtype=torch.uint8, device=device))
+                continue
             shape = (num_blocks, Hkv, page, d) if f else (n_ring_rows, Hkv, W, d)
             k.append(torch.zeros(shape, dtype=torch.bfloat16, device=device))
             v.append(torch.zeros(shape, dtype=torch.bfloat16, device=device))
-        return cls(layer_is_full, k, v, block_tables, ring_row, Hq, W=W, page=page)
+        return cls(layer_is_full, k, v, block_tables, ring_row, Hq, W=W, page=page, kv_fp8=fp8,
+                   Hkv=Hkv, d=d, num_blocks=num_blocks)
 
     def ref(self):
         return ctypes.byref(self.c)

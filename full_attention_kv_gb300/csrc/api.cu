@@ -66,7 +66,28 @@ bool encode_3d(CUtensorMap *map, const void *base, uint64_t d0, uint64_t d1, uin
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D byte tensor map (E4M3 codes): rows of `cols` bytes, row pitch `cols`.
+bool encode_2d_u8(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows,
+                  uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle swz)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn)
+        return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+bool layer_fp8(const hsa_pools *p, int32_t layer)
+{
+    return p->layer_kv_fp8 && p->layer_kv_fp8[layer];
+}
 
 int device_sms()
 {
@@ -95,6 +116,8 @@ hsa_status check_pools(const hsa_pools *p, int32_t layer)
         return HSA_INVALID_ARG;
     if (!p->k[layer] || !p->v[layer] || !aligned16(p->k[layer]) || !aligned16(p->v[layer]))
         return HSA_INVALID_ARG;
+    if (layer_fp8(p, layer) && !p->layer_is_full[layer])
+        return HSA_UNSUPPORTED_SHAPE;  // the ring (newest W tokens) stays bf16
     if (p->layer_is_full[layer]) {
         if (!p->block_tables || p->num_blocks <= 0 || p->max_blocks <= 0)
             return HSA_INVALID_ARG;
@@ -164,6 +187,7 @@ hsa_status hsa_kv_append(const hsa_pools *pools, int32_t layer, const void *k_ne
     a.n_ring_rows = pools->n_ring_rows;
     a.W = pools->W;
     a.ring_mode = pools->layer_is_full[layer] ? 0 : 1;
+    a.fp8 = layer_fp8(pools, layer) ? 1 : 0;
     return hsa::launch_append(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? HSA_OK
                                                                                   : HSA_CUDA_ERROR;
 }
@@ -223,11 +247,19 @@ hsa_status decode_common(const hsa_pools *pools, int32_t layer, const void *q, c
         return HSA_INVALID_ARG;
 
     CUtensorMap tmK, tmV;
+    const bool fp8 = layer_fp8(pools, layer);
     const uint64_t rows = full ? (uint64_t)pools->num_blocks * pools->Hkv * pools->page_size
                                : (uint64_t)pools->n_ring_rows * pools->Hkv * pools->W;
-    if (!encode_2d(&tmK, pools->k[layer], 128, rows, 128, 64, 64) ||
-        !encode_2d(&tmV, pools->v[layer], 128, rows, 128, 64, 64))
+    if (fp8) {
+        // K codes: rows of 128 bytes, a page = box of 64 rows (128-byte swizzle);
+        // V codes: transposed pages, rows of 64 bytes, box of 128 rows (64-byte swizzle)
+        if (!encode_2d_u8(&tmK, pools->k[layer], 128, rows, 128, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_2d_u8(&tmV, pools->v[layer], 64, rows * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_64B))
+            return HSA_CUDA_ERROR;
+    } else if (!encode_2d(&tmK, pools->k[layer], 128, rows, 128, 64, 64) ||
+               !encode_2d(&tmV, pools->v[layer], 128, rows, 128, 64, 64)) {
         return HSA_CUDA_ERROR;
+    }
 
     DecodeParams p{};
     p.q = static_cast<const __nv_bfloat16 *>(q);
@@ -249,7 +281,8 @@ hsa_status decode_common(const hsa_pools *pools, int32_t layer, const void *q, c
     p.W = pools->W;
     p.T = (int16_t)T;
     p.G = (int16_t)G;
-    p.flags = (full ? 0 : hsa::kDecodeRing) | (append ? hsa::kDecodeAppend : 0);
+    p.flags = (full ? 0 : hsa::kDecodeRing) | (append ? hsa::kDecodeAppend : 0) |
+              (fp8 ? hsa::kDecodeFp8 : 0);
     p.scale_log2 = scale * 1.4426950408889634f;
     return hsa::launch_decode(tmK, tmV, p, ctas, static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? HSA_OK
@@ -288,6 +321,8 @@ hsa_status hsa_prefill_attn(const hsa_pools *pools, int32_t layer, const void *q
     hsa_status st = check_pools(pools, layer);
     if (st != HSA_OK)
         return st;
+    if (layer_fp8(pools, layer))
+        return HSA_UNSUPPORTED_SHAPE;  // FP8 pool layers are a decode variant
     if (R < 0 || rows < 0 || max_chunk < 0)
         return HSA_INVALID_ARG;
     if (R == 0 || rows == 0 || max_chunk == 0)

@@ -10,6 +10,7 @@
 // For the ring only a request's last W tokens are written, so every slot is
 // written once per call (deterministic, race-free) and the result equals
 // appending the tokens one by one in position order.
+#include "fp8_kv.cuh"
 #include "hsa_device.cuh"
 #include "hsa_internal.h"
 
@@ -81,16 +82,80 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendParams p)
     }
 }
 
+// FP8 Full KV Pool layer: one warp per (token, KV head, K or V) row, quantised
+// into the layer's E4M3 layout (fp8_kv.cuh).
+__global__ void __launch_bounds__(256) append_fp8_kernel(const AppendParams p)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    const int64_t total = (int64_t)p.ntok * p.Hkv * 2;
+    uint8_t *const kc = reinterpret_cast<uint8_t *>(p.k_dst);
+    uint8_t *const vc = reinterpret_cast<uint8_t *>(p.v_dst);
+    const int64_t cb = fp8_codes_bytes(p.num_blocks, p.Hkv);
+    float *const ks = reinterpret_cast<float *>(kc + cb);
+    float *const vs = reinterpret_cast<float *>(vc + cb);
+    for (int64_t e = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); e < total;
+         e += warps) {
+        const int kv = (int)(e & 1);
+        const int64_t th = e >> 1;
+        const int h = (int)(th % p.Hkv);
+        const int tok = (int)(th / p.Hkv);
+        int lo = 0, hi = p.R;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (__ldg(p.cu_tokens + mid) <= tok)
+                lo = mid;
+            else
+                hi = mid;
+        }
+        const int first = __ldg(p.cu_tokens + lo), last = __ldg(p.cu_tokens + lo + 1);
+        const int seq = __ldg(p.seq_idx + lo);
+        const int64_t pos = (int64_t)__ldg(p.start_pos + lo) + (tok - first);
+        int err = 0, blk = 0;
+        if (tok < first || tok >= last || pos < 0) {
+            err = HSA_DEVERR_BAD_LEN;
+        } else if (seq < 0 || seq >= p.batch) {
+            err = HSA_DEVERR_BAD_SEQ;
+        } else if (pos / p.page_size >= p.max_blocks) {
+            err = HSA_DEVERR_BAD_PAGE;
+        } else {
+            blk = __ldg(p.block_tables + (int64_t)seq * p.max_blocks + pos / p.page_size);
+            if (blk < 0 || blk >= p.num_blocks)
+                err = HSA_DEVERR_BAD_BLOCK;
+        }
+        if (err) {  // uniform across the warp
+            if (lane == 0)
+                set_err(p.dev_err, err);
+            continue;
+        }
+        const __nv_bfloat16 *src =
+            reinterpret_cast<const __nv_bfloat16 *>(kv ? p.v_new : p.k_new) + ((int64_t)tok * p.Hkv + h) * 128;
+        fp8_store_row(src, kv ? vc : kc, kv ? vs : ks, blk, h, p.Hkv, (int)(pos % p.page_size), kv,
+                      lane);
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_append(const AppendParams &p, cudaStream_t stream)
 {
-    const int64_t total = (int64_t)p.ntok * p.Hkv * p.chunks_per_row;
-    if (total == 0)
-        return cudaSuccess;
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (p.fp8) {
+        const int64_t warps = (int64_t)p.ntok * p.Hkv * 2;
+        if (warps == 0)
+            return cudaSuccess;
+        int64_t blocks = (warps + 7) / 8;
+        const int64_t cap = (int64_t)(sms > 0 ? sms : 148) * 8;
+        if (blocks > cap)
+            blocks = cap;
+        append_fp8_kernel<<<(unsigned)blocks, 256, 0, stream>>>(p);
+        return cudaGetLastError();
+    }
+    const int64_t total = (int64_t)p.ntok * p.Hkv * p.chunks_per_row;
+    if (total == 0)
+        return cudaSuccess;
     int64_t blocks = (total + 255) / 256;
     const int64_t cap = (int64_t)(sms > 0 ? sms : 148) * 8;
     if (blocks > cap)

@@ -32,6 +32,7 @@
 //    by then, so even a T > 1 ring write cannot clobber a slot still being read.
 //  * Launched with programmatic dependent launch: nothing global is read before
 //    griddepcontrol.wait, so the launch and prologue overlap the previous kernel.
+#include "fp8_kv.cuh"
 #include "hsa_device.cuh"
 #include "hsa_internal.h"
 
@@ -49,14 +50,23 @@ constexpr int kMaxRows = 32;                    // G * T
 constexpr int kNewRows = 16;                    // new-token tile (T <= 4 used)
 constexpr int kCombFloats = 16 + 16 + 16 * kD;  // per warp: m, l, o[16][128]
 constexpr int kPartFloats = kMaxRows * (kD + 2);
+// FP8 full layers (fp8_kv.cuh): a stage holds the tile's E4M3 K (64 x 128 B,
+// 128-byte swizzle), transposed V (128 x 64 B, 64-byte swizzle) and the two rows
+// of 64 fp32 scales; half the bytes of a bf16 stage, so more stages fit in the
+// same shared memory and as many bytes stay in flight.
+constexpr int kFp8Stages = 7;
+constexpr int kFp8StageStride = 17408;  // 16.5 KB rounded up to 1 KB (swizzle alignment)
+constexpr int kFp8TileBytes = kTileKeys * kD;  // 8 KB
+constexpr int kMaxStages = 8;
+static_assert(kFp8Stages * kFp8StageStride <= kStages * kStageBytes, "FP8 stages fit");
 
 struct SharedStorage {
     alignas(1024) uint8_t stage[kStages][kStageBytes];  // [K lo|K hi|V lo|V hi] per stage
     alignas(16) uint8_t new_k[kNewRows * kD * 2];
     alignas(16) uint8_t new_v[kNewRows * kD * 2];
     alignas(16) float comb[kConsumerWarps][kCombFloats];
-    alignas(8) uint64_t full[kStages];
-    alignas(8) uint64_t empty[kStages];
+    alignas(8) uint64_t full[kMaxStages];
+    alignas(8) uint64_t empty[kMaxStages];
     int32_t scan[kThreads];
     int32_t first_b;
     int32_t first_items_before;  // items of all units of sequences < first_b (per KV head)
@@ -160,7 +170,25 @@ constexpr float kRescaleSlack = 8.0f;
 // memory (for the swizzle), vis(row, key) = key visible to that query row; when
 // all_vis is set every key of the tile is visible to every valid row and only rows
 // past G T (padding) are masked.
-template <int NT, typename Vis>
+template <bool F16>
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1)
+{
+    if (F16)
+        mma_f16_16816(d, a, b0, b1);
+    else
+        mma_bf16_16816(d, a, b0, b1);
+}
+
+template <bool F16>
+__device__ __forceinline__ uint32_t pack16(float lo, float hi)
+{
+    return F16 ? pack_f16(lo, hi) : pack_bf16(lo, hi);
+}
+
+// F16: the operands (Q fragments and the tile in shared memory) are fp16 instead
+// of bf16 (the FP8 kernel's new-token tile).
+template <int NT, bool F16 = false, typename Vis>
 __device__ __forceinline__ void run_tile(RowState &st, const uint32_t (&qa)[kD / 16][4],
                                          uint32_t sK, uint32_t sV, int tile_rows, int key0,
                                          float scale_log2, bool all_vis, bool row0_ok,
@@ -184,8 +212,8 @@ __device__ __forceinline__ void run_tile(RowState &st, const uint32_t (&qa)[kD /
                 const int dim = ks * 16 + (mi & 1) * 8;
                 uint32_t b0, b1, b2, b3;
                 ldmatrix_x4(sK + swz128_offset(key, dim, tile_rows), b0, b1, b2, b3);
-                mma_bf16_16816(s[2 * np], qa[ks], b0, b1);
-                mma_bf16_16816(s[2 * np + 1], qa[ks], b2, b3);
+                mma16816<F16>(s[2 * np], qa[ks], b0, b1);
+                mma16816<F16>(s[2 * np + 1], qa[ks], b2, b3);
             }
         }
     }
@@ -262,24 +290,192 @@ __device__ __forceinline__ void run_tile(RowState &st, const uint32_t (&qa)[kD /
 #pragma unroll
     for (int ks = 0; ks < NT / 2; ++ks) {
         uint32_t pa[4];
-        pa[0] = pack_bf16(s[2 * ks][0], s[2 * ks][1]);
-        pa[1] = pack_bf16(s[2 * ks][2], s[2 * ks][3]);
-        pa[2] = pack_bf16(s[2 * ks + 1][0], s[2 * ks + 1][1]);
-        pa[3] = pack_bf16(s[2 * ks + 1][2], s[2 * ks + 1][3]);
-        sum0 += bf16_lo(pa[0]) + bf16_hi(pa[0]) + bf16_lo(pa[2]) + bf16_hi(pa[2]);
-        sum1 += bf16_lo(pa[1]) + bf16_hi(pa[1]) + bf16_lo(pa[3]) + bf16_hi(pa[3]);
+        pa[0] = pack16<F16>(s[2 * ks][0], s[2 * ks][1]);
+        pa[1] = pack16<F16>(s[2 * ks][2], s[2 * ks][3]);
+        pa[2] = pack16<F16>(s[2 * ks + 1][0], s[2 * ks + 1][1]);
+        pa[3] = pack16<F16>(s[2 * ks + 1][2], s[2 * ks + 1][3]);
+        if constexpr (F16) {
+            sum0 += f16_lo(pa[0]) + f16_hi(pa[0]) + f16_lo(pa[2]) + f16_hi(pa[2]);
+            sum1 += f16_lo(pa[1]) + f16_hi(pa[1]) + f16_lo(pa[3]) + f16_hi(pa[3]);
+        } else {
+            sum0 += bf16_lo(pa[0]) + bf16_hi(pa[0]) + bf16_lo(pa[2]) + bf16_hi(pa[2]);
+            sum1 += bf16_lo(pa[1]) + bf16_hi(pa[1]) + bf16_lo(pa[3]) + bf16_hi(pa[3]);
+        }
         const int key = key0 + ks * 16 + (mi & 1) * 8 + r;
 #pragma unroll
         for (int np = 0; np < kD / 16; ++np) {
             const int dim = np * 16 + (mi >> 1) * 8;
             uint32_t b0, b1, b2, b3;
             ldmatrix_x4_trans(sV + swz128_offset(key, dim, tile_rows), b0, b1, b2, b3);
-            mma_bf16_16816(st.o[2 * np], pa, b0, b1);
-            mma_bf16_16816(st.o[2 * np + 1], pa, b2, b3);
+            mma16816<F16>(st.o[2 * np], pa, b0, b1);
+            mma16816<F16>(st.o[2 * np + 1], pa, b2, b3);
         }
     }
     st.l[0] += sum0;
     st.l[1] += sum1;
+}
+
+// One key tile of an FP8 full layer (fp8_kv.cuh layout) on tensor cores, fp16
+// MMAs.  K: one 32-bit shared load per (key, 16-dim step) holds a thread's four
+// E4M3 codes of the B fragment, converted exactly to fp16; the key's scale is then
+// applied to its S column.  V (stored transposed): one 32-bit load per (dimension,
+// 16-key step); each key's scale is folded into P, while the row sum takes P
+// itself.  qa holds fp16 Q fragments.
+template <int NT, typename Vis>
+__device__ __forceinline__ void run_tile_fp8(RowState &st, const uint32_t (&qa)[kD / 16][4],
+                                             const uint8_t *sK, const uint8_t *sV,
+                                             const float *k_scale, const float *v_scale, int key0,
+                                             float scale_log2, bool all_vis, bool row0_ok,
+                                             bool row1_ok, Vis vis)
+{
+    const int lane = threadIdx.x & 31;
+    const int g = lane >> 2, tq = lane & 3;
+    // plain shared-memory loads (ordered after the stage's barrier wait, free to be
+    // scheduled early within the tile); two accumulator chains per n-tile (even and
+    // odd k-steps) halve the dependent MMA chain
+    float s[NT][4], s2[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+        s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = s2[nt][0] = s2[nt][1] = s2[nt][2] = s2[nt][3] = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int key = key0 + nt * 8 + g;
+        const uint8_t *row = sK + key * 128 + 4 * tq;
+#pragma unroll
+        for (int ks = 0; ks < kD / 16; ++ks) {
+            const uint32_t w = *reinterpret_cast<const uint32_t *>(row + ((ks ^ (key & 7)) << 4));
+            mma_f16_16816((ks & 1) ? s2[nt] : s[nt], qa[ks], e4m3x2_to_f16x2(w & 0xffffu),
+                          e4m3x2_to_f16x2(w >> 16));
+        }
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            s[nt][e] += s2[nt][e];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const float ksc = k_scale[key0 + nt * 8 + 2 * tq + e];
+            s[nt][e] *= ksc;
+            s[nt][2 + e] *= ksc;
+        }
+    }
+    if (!all_vis) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int key = key0 + nt * 8 + 2 * tq + e;
+                if (!vis(g, key))
+                    s[nt][e] = -INFINITY;
+                if (!vis(g + 8, key))
+                    s[nt][2 + e] = -INFINITY;
+            }
+        }
+    } else {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            if (!row0_ok)
+                s[nt][0] = s[nt][1] = -INFINITY;
+            if (!row1_ok)
+                s[nt][2] = s[nt][3] = -INFINITY;
+        }
+    }
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
+        mx1 = fmaxf(mx1, fmaxf(s[nt][2], s[nt][3]));
+    }
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+    mx0 *= scale_log2;
+    mx1 *= scale_log2;
+    const bool up0 = mx0 != -INFINITY && (st.m[0] == -INFINITY || mx0 > st.m[0] + kRescaleSlack);
+    const bool up1 = mx1 != -INFINITY && (st.m[1] == -INFINITY || mx1 > st.m[1] + kRescaleSlack);
+    if (__any_sync(0xffffffffu, up0 || up1)) {
+        const float a0 = up0 ? fast_exp2(st.m[0] - mx0) : 1.f;
+        const float a1 = up1 ? fast_exp2(st.m[1] - mx1) : 1.f;
+        if (up0)
+            st.m[0] = mx0;
+        if (up1)
+            st.m[1] = mx1;
+        st.l[0] *= a0;
+        st.l[1] *= a1;
+#pragma unroll
+        for (int n = 0; n < kD / 8; ++n) {
+            st.o[n][0] *= a0;
+            st.o[n][1] *= a0;
+            st.o[n][2] *= a1;
+            st.o[n][3] *= a1;
+        }
+    }
+    const float base0 = st.m[0] == -INFINITY ? 0.f : st.m[0];
+    const float base1 = st.m[1] == -INFINITY ? 0.f : st.m[1];
+    float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        s[nt][0] = fast_exp2(fmaf(s[nt][0], scale_log2, -base0));
+        s[nt][1] = fast_exp2(fmaf(s[nt][1], scale_log2, -base0));
+        s[nt][2] = fast_exp2(fmaf(s[nt][2], scale_log2, -base1));
+        s[nt][3] = fast_exp2(fmaf(s[nt][3], scale_log2, -base1));
+        sum0 += s[nt][0] + s[nt][1];
+        sum1 += s[nt][2] + s[nt][3];
+    }
+#pragma unroll
+    for (int ks = 0; ks < NT / 2; ++ks) {
+        const int kb = key0 + ks * 16 + 2 * tq;
+        const float va0 = v_scale[kb], va1 = v_scale[kb + 1];
+        const float vb0 = v_scale[kb + 8], vb1 = v_scale[kb + 9];
+        uint32_t pa[4];
+        pa[0] = pack_f16(s[2 * ks][0] * va0, s[2 * ks][1] * va1);
+        pa[1] = pack_f16(s[2 * ks][2] * va0, s[2 * ks][3] * va1);
+        pa[2] = pack_f16(s[2 * ks + 1][0] * vb0, s[2 * ks + 1][1] * vb1);
+        pa[3] = pack_f16(s[2 * ks + 1][2] * vb0, s[2 * ks + 1][3] * vb1);
+        const int grp = (key0 >> 4) + ks;  // 16-key group: the 16-byte chunk of a V row
+#pragma unroll
+        for (int n = 0; n < kD / 8; ++n) {
+            const int dim = n * 8 + g;
+            const uint32_t w = *reinterpret_cast<const uint32_t *>(
+                sV + dim * 64 + ((grp ^ ((dim >> 1) & 3)) << 4) + 4 * tq);
+            mma_f16_16816(st.o[n], pa, e4m3x2_to_f16x2(w & 0xffffu), e4m3x2_to_f16x2(w >> 16));
+        }
+    }
+    st.l[0] += sum0;
+    st.l[1] += sum1;
+}
+
+// Append of unit (b, h) into an FP8 full layer: one warp per new K or V row.
+__device__ __forceinline__ void append_unit_fp8(const DecodeParams &p, int b, int h, int c, int warp,
+                                                int lane, int nwarps)
+{
+    uint8_t *const kc = reinterpret_cast<uint8_t *>(p.k_dst);
+    uint8_t *const vc = reinterpret_cast<uint8_t *>(p.v_dst);
+    const int64_t cb = fp8_codes_bytes(p.num_blocks, p.Hkv);
+    for (int e = warp; e < 2 * p.T; e += nwarps) {
+        const int kv = e & 1, t = e >> 1;
+        const int64_t pos = (int64_t)c + t;
+        const int64_t page = pos / kTileKeys;
+        if (page >= p.max_blocks) {
+            if (lane == 0)
+                set_err(p.dev_err, HSA_DEVERR_BAD_PAGE);
+            continue;
+        }
+        const int blk = __ldg(p.block_tables + (int64_t)b * p.max_blocks + page);
+        if (blk < 0 || blk >= p.num_blocks) {
+            if (lane == 0)
+                set_err(p.dev_err, HSA_DEVERR_BAD_BLOCK);
+            continue;
+        }
+        const __nv_bfloat16 *src = (kv ? p.v_new : p.k_new) + ((int64_t)(b * p.T + t) * p.Hkv + h) * kD;
+        uint8_t *codes = kv ? vc : kc;
+        fp8_store_row(src, codes, reinterpret_cast<float *>(codes + cb), blk, h, p.Hkv,
+                      (int)(pos % kTileKeys), kv, lane);
+    }
 }
 
 // Append the T new K/V rows of unit (b, h) to this layer's pool or ring.  Called by
@@ -327,11 +523,12 @@ __device__ __forceinline__ void append_unit(const DecodeParams &p, int b, int h,
     }
 }
 
-template <int MT>
+template <int MT, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const DecodeParams p)
 {
+    constexpr int NS = FP8 ? kFp8Stages : kStages;
     extern __shared__ uint8_t smem_raw[];
     SharedStorage &sh = *reinterpret_cast<SharedStorage *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -339,7 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = tid >> 5, lane = tid & 31;
 
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < NS; ++s) {
             mbar_init(&sh.full[s], 1);
             mbar_init(&sh.empty[s], kConsumerWarps);
         }
@@ -427,15 +624,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t pol = policy_evict_first();
             Walk w = w0;
             int64_t k = 0;
+            const int64_t fp8_cb = fp8_codes_bytes(p.num_blocks, p.Hkv);
             for (int64_t i = i0; i < i1; ++i, ++k) {
-                const int st = (int)(k % kStages);
-                const uint32_t ph = (uint32_t)((k / kStages) & 1);
+                const int st = (int)(k % NS);
+                const uint32_t ph = (uint32_t)((k / NS) & 1);
                 if (!mbar_wait(&sh.empty[st], ph ^ 1)) {
                     set_err(p.dev_err, HSA_DEVERR_TIMEOUT);
                     break;
                 }
                 const int64_t row = tile_row(p, w, true);
-                if (row >= 0) {
+                if (FP8 && row >= 0) {
+                    // E4M3 K page (64 rows x 128 B), transposed V page (128 rows x 64 B),
+                    // and the page's 64 K and 64 V scales
+                    mbar_arrive_expect_tx(&sh.full[st], 2 * kFp8TileBytes + 2 * 256);
+                    uint8_t *dst = sh.stage[0] + st * kFp8StageStride;
+                    tma_load_2d(dst, &tmK, &sh.full[st], 0, (int32_t)row, pol);
+                    tma_load_2d(dst + kFp8TileBytes, &tmV, &sh.full[st], 0, (int32_t)(2 * row), pol);
+                    const uint8_t *kb = reinterpret_cast<const uint8_t *>(p.k_dst) + fp8_cb;
+                    const uint8_t *vb = reinterpret_cast<const uint8_t *>(p.v_dst) + fp8_cb;
+                    bulk_load(dst + 2 * kFp8TileBytes, kb + row * 4, 256, &sh.full[st], pol);
+                    bulk_load(dst + 2 * kFp8TileBytes + 256, vb + row * 4, 256, &sh.full[st], pol);
+                } else if (row >= 0) {
                     mbar_arrive_expect_tx(&sh.full[st], kStageBytes);
                     uint8_t *dst = sh.stage[st];
                     tma_load_2d(dst, &tmK, &sh.full[st], 0, (int32_t)row, pol);
@@ -449,9 +658,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 walk_next(p, w);
             }
             // drain: no TMA write may still be in flight when the CTA exits
-            for (int64_t s = 0; s < kStages && s < k; ++s) {
-                const int64_t last = s + ((k - 1 - s) / kStages) * kStages;
-                mbar_wait(&sh.full[s], (uint32_t)((last / kStages) & 1));
+            for (int64_t s = 0; s < NS && s < k; ++s) {
+                const int64_t last = s + ((k - 1 - s) / NS) * NS;
+                mbar_wait(&sh.full[s], (uint32_t)((last / NS) & 1));
             }
         }
         return;
@@ -497,6 +706,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 qa[ks][1] = v1 ? __ldg(reinterpret_cast<const uint32_t *>(q1 + c0)) : 0u;
                 qa[ks][2] = v0 ? __ldg(reinterpret_cast<const uint32_t *>(q0 + c0 + 8)) : 0u;
                 qa[ks][3] = v1 ? __ldg(reinterpret_cast<const uint32_t *>(q1 + c0 + 8)) : 0u;
+                if (FP8) {  // the FP8 kernel multiplies in fp16
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        qa[ks][e] = bf16x2_to_f16x2(qa[ks][e]);
+                }
             }
             // stage this unit's new tokens now when this CTA owns the unit's last
             // tile; rows >= T are zero
@@ -509,14 +723,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                             ((int64_t)(w.b * p.T + rr) * p.Hkv + w.h) * kD + col;
                         kv = __ldg(reinterpret_cast<const uint4 *>(p.k_new + src));
                         vv = __ldg(reinterpret_cast<const uint4 *>(p.v_new + src));
+                        if (FP8) {
+                            kv = make_uint4(bf16x2_to_f16x2(kv.x), bf16x2_to_f16x2(kv.y),
+                                            bf16x2_to_f16x2(kv.z), bf16x2_to_f16x2(kv.w));
+                            vv = make_uint4(bf16x2_to_f16x2(vv.x), bf16x2_to_f16x2(vv.y),
+                                            bf16x2_to_f16x2(vv.z), bf16x2_to_f16x2(vv.w));
+                        }
                     }
                     *reinterpret_cast<uint4 *>(sh.new_k + swz128_offset(rr, col, kNewRows)) = kv;
                     *reinterpret_cast<uint4 *>(sh.new_v + swz128_offset(rr, col, kNewRows)) = vv;
                 }
             }
         }
-        const int stg = (int)(k % kStages);
-        const uint32_t ph = (uint32_t)((k / kStages) & 1);
+        const int stg = (int)(k % NS);
+        const uint32_t ph = (uint32_t)((k / NS) & 1);
         if (!timed_out && !mbar_wait(&sh.full[stg], ph)) {
             set_err(p.dev_err, HSA_DEVERR_TIMEOUT);
             timed_out = true;
@@ -543,8 +763,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             // full layers: every key of a complete page is visible to every query
             const bool all_vis = !ring && (j + 1) * kTileKeys <= c;
-            run_tile<2 * MT>(st, qa, sK, sV, kTileKeys, key0, p.scale_log2, all_vis, t0 < T,
-                             t1 < T, vis);
+            if constexpr (FP8) {
+                const uint8_t *base = sh.stage[0] + stg * kFp8StageStride;
+                const float *ksc = reinterpret_cast<const float *>(base + 2 * kFp8TileBytes);
+                run_tile_fp8<2 * MT>(st, qa, base, base + kFp8TileBytes, ksc, ksc + 64, key0,
+                                     p.scale_log2, all_vis, t0 < T, t1 < T, vis);
+            } else {
+                run_tile<2 * MT>(st, qa, sK, sV, kTileKeys, key0, p.scale_log2, all_vis, t0 < T,
+                                 t1 < T, vis);
+            }
         }
         __syncwarp();
         if (lane == 0)
@@ -567,8 +794,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int t = rr == g ? t0 : t1;
                     return t < T && key <= t;
                 };
-                run_tile<2>(st, qa, smem_u32(sh.new_k), smem_u32(sh.new_v), kNewRows, 0,
-                            p.scale_log2, false, t0 < T, t1 < T, vis_new);
+                run_tile<2, FP8>(st, qa, smem_u32(sh.new_k), smem_u32(sh.new_v), kNewRows, 0,
+                                 p.scale_log2, false, t0 < T, t1 < T, vis_new);
             }
         }
 
@@ -634,8 +861,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __stcg(part + 2 * kMaxRows + rr * kD + dim, O);
             }
         }
-        if (whole && (p.flags & kDecodeAppend))
-            append_unit(p, cur.b, cur.h, cur.c, tid, kConsumerWarps * 32);
+        if (whole && (p.flags & kDecodeAppend)) {
+            if constexpr (FP8)
+                append_unit_fp8(p, cur.b, cur.h, cur.c, warp, lane, kConsumerWarps);
+            else
+                append_unit(p, cur.b, cur.h, cur.c, tid, kConsumerWarps * 32);
+        }
         if (!whole) {
             // count this part in; the last CTA of the unit merges every part
             const int unit = cur.b * p.Hkv + cur.h;
@@ -672,8 +903,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     p.out[((int64_t)(cur.b * p.T + t) * Hq + cur.h * p.G + hh) * kD + dim] =
                         __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
                 }
-                if (p.flags & kDecodeAppend)
-                    append_unit(p, cur.b, cur.h, cur.c, tid, kConsumerWarps * 32);
+                if (p.flags & kDecodeAppend) {
+                    if constexpr (FP8)
+                        append_unit_fp8(p, cur.b, cur.h, cur.c, warp, lane, kConsumerWarps);
+                    else
+                        append_unit(p, cur.b, cur.h, cur.c, tid, kConsumerWarps * 32);
+                }
                 if (tid == 0)
                     ws_cnt[unit] = 0;
             }
@@ -698,18 +933,22 @@ cudaError_t launch_decode(const CUtensorMap &tmK, const CUtensorMap &tmV, const 
 {
     const size_t smem = sizeof(SharedStorage) + 1024;
     const int MT = (p.G * p.T + 15) / 16;
+    const bool fp8 = (p.flags & kDecodeFp8) != 0;
     // the opt-in shared-memory size is set once per process (the API is not a stream
     // operation, but setting it once keeps graph capture free of extra calls)
-    static bool attr_set[2] = {false, false};
-    auto k1 = decode_kernel<1>;
-    auto k2 = decode_kernel<2>;
-    auto kern = MT == 1 ? k1 : k2;
-    if (!attr_set[MT - 1]) {
+    static bool attr_set[4] = {false, false, false, false};
+    auto k1 = decode_kernel<1, false>;
+    auto k2 = decode_kernel<2, false>;
+    auto f1 = decode_kernel<1, true>;
+    auto f2 = decode_kernel<2, true>;
+    auto kern = fp8 ? (MT == 1 ? f1 : f2) : (MT == 1 ? k1 : k2);
+    const int which = (fp8 ? 2 : 0) + MT - 1;
+    if (!attr_set[which]) {
         cudaError_t e =
             cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess)
             return e;
-        attr_set[MT - 1] = true;
+        attr_set[which] = true;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)ctas);

@@ -36,6 +36,7 @@ struct DecodeParams {
 };
 constexpr int32_t kDecodeRing = 1;    // sliding layer: read the SWA ring
 constexpr int32_t kDecodeAppend = 2;  // append the T new rows (hsa_decode_attn_append)
+constexpr int32_t kDecodeFp8 = 4;     // full layer stored as E4M3 codes + scales (fp8_kv.cuh)
 static_assert(sizeof(DecodeParams) <= 128, "keep the decode parameter struct <= 128 bytes");
 
 // Bytes of the arrival-counter region at the start of a decode workspace.
@@ -62,6 +63,7 @@ struct AppendParams {
     int32_t R, ntok, Hkv, chunks_per_row;  // chunks_per_row = d * 2 / 16
     int32_t batch, max_blocks, num_blocks, page_size, n_ring_rows, W;
     int32_t ring_mode;
+    int32_t fp8;                 // full layer stored as E4M3 codes + scales (fp8_kv.cuh)
 };
 
 cudaError_t launch_append(const AppendParams &p, cudaStream_t stream);

@@ -13,15 +13,26 @@ import full_attention_kv_gb300 as hsa
 import workload
 
 
-def make_pool(inst, layers=None, device="cuda", stale="random", max_bytes=1 << 31):
+def make_pool(inst, layers=None, device="cuda", stale="random", max_bytes=1 << 31, fp8=False):
     """DualPool holding the cached prefix of every sequence for `layers`.
 
     Pool layer i is model layer layers[i].  `stale` = "random" fills unwritten pool
     rows with random bf16 (so that reading them would show), "zero" zero-fills.
+    fp8=True stores the full layers as FP8 layers (zero-filled, quantised on
+    append by the library); sliding rings stay bf16.
     """
     cfg = inst.cfg
     layers = list(range(cfg.n_layers)) if layers is None else list(layers)
     full = [inst.full[l] for l in layers]
+    if fp8:
+        bt = torch.from_numpy(inst.block_tables).to(device)
+        rr = torch.from_numpy(inst.ring_row).to(device)
+        pool = hsa.DualPool.allocate(full, inst.num_blocks, inst.n_ring_rows, bt, rr, cfg.Hq,
+                                     cfg.Hkv, d=cfg.d, W=cfg.W, page=cfg.page, device=device,
+                                     kv_fp8=True)
+        for i, l in enumerate(layers):
+            fill_layer(inst, pool, i, l, device, max_bytes=max_bytes)
+        return pool
     ks, vs = [], []
     for l in layers:
         if stale == "random":
@@ -118,3 +129,4 @@ def oracle_case(inst, layer, seqs, device="cuda"):
                 v_new=v.cpu(), hist_k=torch.cat(hk) if hk else empty,
                 hist_v=torch.cat(hv) if hv else empty, hist_off=np.array(off, np.int64),
                 hist_start=np.array(start, np.int32))
+

@@ -440,7 +440,8 @@ static void attend_row_fp8(const double *q, int d, double scale, int nkeys, int 
  * cached positions, history rows hist_off[r] .. hist_off[r+1]-1 holding positions
  * 0 .. prefix_len[r]-1 as codes [rows, Hkv, d] with scales [rows, Hkv]; its new
  * rows cu_rows[r] .. cu_rows[r+1]-1 (bf16) sit at positions prefix_len[r] + i.
- * Items as in orc_attention.  Returns 0, or -2 on bad arguments.
+ * Items as in orc_attention.  Returns 0, -1 if an asked row's request lacks its
+ * history, or -2 on bad arguments.
  */
 int orc_attention_fp8hist(int R, const int32_t *cu_rows, const int32_t *prefix_len, int Hq,
                           int Hkv, int d, double scale, const uint16_t *q,
@@ -460,8 +461,6 @@ int orc_attention_fp8hist(int R, const int32_t *cu_rows, const int32_t *prefix_l
         int64_t k = (int64_t)prefix_len[r] + (cu_rows[r + 1] - cu_rows[r]);
         if (k > max_keys)
             max_keys = k;
-        if (hist_off[r + 1] - hist_off[r] != prefix_len[r])
-            return -2;
     }
     if (nthreads <= 0)
         nthreads = 1;
@@ -491,6 +490,11 @@ int orc_attention_fp8hist(int R, const int32_t *cu_rows, const int32_t *prefix_l
             const int64_t P = prefix_len[r];
             const int64_t p = P + (row - cu_rows[r]);
             const int kv = h / group;
+            if (hist_off[r + 1] - hist_off[r] != P) {  /* history of 0 .. P-1 missing */
+#pragma omp atomic write
+                status = -1;
+                continue;
+            }
             int nk = 0;
             for (int64_t x = 0; x <= p; ++x, ++nk) {
                 if (x < P) {
