@@ -54,14 +54,21 @@ constexpr int kPartFloats = kMaxRows * (kD + 2);
 // 128-byte swizzle), transposed V (128 x 64 B, 64-byte swizzle) and the two rows
 // of 64 fp32 scales; half the bytes of a bf16 stage, so more stages fit in the
 // same shared memory and as many bytes stay in flight.
-constexpr int kFp8Stages = 7;
+constexpr int kFp8Stages = 8;
 constexpr int kFp8StageStride = 17408;  // 16.5 KB rounded up to 1 KB (swizzle alignment)
 constexpr int kFp8TileBytes = kTileKeys * kD;  // 8 KB
 constexpr int kMaxStages = 8;
-static_assert(kFp8Stages * kFp8StageStride <= kStages * kStageBytes, "FP8 stages fit");
+// One stage region serves both layouts.  Tile-parallel consumers (warp w runs items
+// k = w mod 4) need a stage count that is a multiple of the consumer warps, so that
+// stage k mod S always belongs to the same warp: a warp that skips ahead must never
+// wait on a stage whose earlier phase another warp has not consumed yet (the
+// mbarrier parity bit cannot tell two phases apart).
+constexpr int kStageRegion = kFp8Stages * kFp8StageStride > kStages * kStageBytes
+                                 ? kFp8Stages * kFp8StageStride
+                                 : kStages * kStageBytes;
 
 struct SharedStorage {
-    alignas(1024) uint8_t stage[kStages][kStageBytes];  // [K lo|K hi|V lo|V hi] per stage
+    alignas(1024) uint8_t stage[kStageRegion];  // bf16: [K lo|K hi|V lo|V hi] per stage
     alignas(16) uint8_t new_k[kNewRows * kD * 2];
     alignas(16) uint8_t new_v[kNewRows * kD * 2];
     alignas(16) float comb[kConsumerWarps][kCombFloats];
@@ -538,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) {
             mbar_init(&sh.full[s], 1);
-            mbar_init(&sh.empty[s], kConsumerWarps);
+            mbar_init(&sh.empty[s], MT == 1 ? 1 : kConsumerWarps);
         }
         fence_barrier_init();
     }
@@ -637,7 +644,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // E4M3 K page (64 rows x 128 B), transposed V page (128 rows x 64 B),
                     // and the page's 64 K and 64 V scales
                     mbar_arrive_expect_tx(&sh.full[st], 2 * kFp8TileBytes + 2 * 256);
-                    uint8_t *dst = sh.stage[0] + st * kFp8StageStride;
+                    uint8_t *dst = sh.stage + st * kFp8StageStride;
                     tma_load_2d(dst, &tmK, &sh.full[st], 0, (int32_t)row, pol);
                     tma_load_2d(dst + kFp8TileBytes, &tmV, &sh.full[st], 0, (int32_t)(2 * row), pol);
                     const uint8_t *kb = reinterpret_cast<const uint8_t *>(p.k_dst) + fp8_cb;
@@ -646,7 +653,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     bulk_load(dst + 2 * kFp8TileBytes + 256, vb + row * 4, 256, &sh.full[st], pol);
                 } else if (row >= 0) {
                     mbar_arrive_expect_tx(&sh.full[st], kStageBytes);
-                    uint8_t *dst = sh.stage[st];
+                    uint8_t *dst = sh.stage + st * kStageBytes;
                     tma_load_2d(dst, &tmK, &sh.full[st], 0, (int32_t)row, pol);
                     tma_load_2d(dst + kTileBytes / 2, &tmK, &sh.full[st], 64, (int32_t)row, pol);
                     tma_load_2d(dst + kTileBytes, &tmV, &sh.full[st], 0, (int32_t)row, pol);
@@ -669,8 +676,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // -------------------------------------------------------------------- consumers
     const int mt = warp % MT;
     const int slice = warp / MT;
-    constexpr int KW = 16 * MT;  // keys per warp per tile
-    const int key0 = slice * KW;
+    // 16 rows (MT = 1): tile-parallel -- warp w runs every fourth tile of the CTA's
+    // range with all 64 keys (eight independent MMA chains), four tiles in flight;
+    // 32 rows (MT = 2): each tile split into two key slices of 32 keys per m-tile
+    constexpr bool TP = MT == 1;
+    static_assert(!TP || NS % kConsumerWarps == 0, "tile-parallel stages have one owner each");
+    constexpr int NT = TP ? kTileKeys / 8 : 2 * MT;  // n-tiles of 8 keys per warp per tile
+    constexpr int KW = 16 * MT;
+    const int key0 = TP ? 0 : slice * KW;
     const int g = lane >> 2, tq = lane & 3;
     const int r0 = mt * 16 + g, r1 = r0 + 8;
     const int t0 = r0 / p.G, t1 = r1 / p.G;
@@ -737,18 +750,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int stg = (int)(k % NS);
         const uint32_t ph = (uint32_t)((k / NS) & 1);
-        if (!timed_out && !mbar_wait(&sh.full[stg], ph)) {
+        const bool mine = !TP || (int)(k % kConsumerWarps) == warp;
+        if (mine && !timed_out && !mbar_wait(&sh.full[stg], ph)) {
             set_err(p.dev_err, HSA_DEVERR_TIMEOUT);
             timed_out = true;
         }
-        const bool loaded = !timed_out && tile_row(p, w, false) >= 0;
+        const bool loaded = mine && !timed_out && tile_row(p, w, false) >= 0;
         const int c = w.c;
         const int j = w.j;
         bool any = loaded;
         if (loaded && !(p.flags & kDecodeRing))
             any = key0 < c - j * kTileKeys;  // this warp's keys hold a cached position
         if (any) {
-            const uint32_t sK = smem_u32(sh.stage[stg]);
+            const uint32_t sK = smem_u32(sh.stage + stg * kStageBytes);
             const uint32_t sV = sK + kTileBytes;
             const int W = p.W, T = p.T;
             const bool ring = (p.flags & kDecodeRing) != 0;
@@ -764,17 +778,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             // full layers: every key of a complete page is visible to every query
             const bool all_vis = !ring && (j + 1) * kTileKeys <= c;
             if constexpr (FP8) {
-                const uint8_t *base = sh.stage[0] + stg * kFp8StageStride;
+                const uint8_t *base = sh.stage + stg * kFp8StageStride;
                 const float *ksc = reinterpret_cast<const float *>(base + 2 * kFp8TileBytes);
-                run_tile_fp8<2 * MT>(st, qa, base, base + kFp8TileBytes, ksc, ksc + 64, key0,
-                                     p.scale_log2, all_vis, t0 < T, t1 < T, vis);
+                run_tile_fp8<NT>(st, qa, base, base + kFp8TileBytes, ksc, ksc + 64, key0,
+                                 p.scale_log2, all_vis, t0 < T, t1 < T, vis);
             } else {
-                run_tile<2 * MT>(st, qa, sK, sV, kTileKeys, key0, p.scale_log2, all_vis, t0 < T,
-                                 t1 < T, vis);
+                run_tile<NT>(st, qa, sK, sV, kTileKeys, key0, p.scale_log2, all_vis, t0 < T,
+                             t1 < T, vis);
             }
         }
         __syncwarp();
-        if (lane == 0)
+        if (mine && lane == 0)
             mbar_arrive(&sh.empty[stg]);
 
         const bool unit_last_tile = (j == w.n - 1);
