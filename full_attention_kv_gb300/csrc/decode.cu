@@ -58,11 +58,11 @@ constexpr int kFp8Stages = 8;
 constexpr int kFp8StageStride = 17408;  // 16.5 KB rounded up to 1 KB (swizzle alignment)
 constexpr int kFp8TileBytes = kTileKeys * kD;  // 8 KB
 constexpr int kMaxStages = 8;
-// One stage region serves both layouts.  Tile-parallel consumers (warp w runs items
-// k = w mod 4) need a stage count that is a multiple of the consumer warps, so that
-// stage k mod S always belongs to the same warp: a warp that skips ahead must never
-// wait on a stage whose earlier phase another warp has not consumed yet (the
-// mbarrier parity bit cannot tell two phases apart).
+// One stage region serves both layouts.  Tile-parallel consumer groups (group g
+// runs items k = g mod groups) need a stage count that is a multiple of the group
+// count, so that stage k mod S always belongs to the same group: a group that
+// skips ahead must never wait on a stage whose earlier phase another group has not
+// consumed yet (the mbarrier parity bit cannot tell two phases apart).
 constexpr int kStageRegion = kFp8Stages * kFp8StageStride > kStages * kStageBytes
                                  ? kFp8Stages * kFp8StageStride
                                  : kStages * kStageBytes;
@@ -545,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) {
             mbar_init(&sh.full[s], 1);
-            mbar_init(&sh.empty[s], MT == 1 ? 1 : kConsumerWarps);
+            mbar_init(&sh.empty[s], MT);  // the MT warps of the owning group
         }
         fence_barrier_init();
     }
@@ -676,14 +676,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // -------------------------------------------------------------------- consumers
     const int mt = warp % MT;
     const int slice = warp / MT;
-    // 16 rows (MT = 1): tile-parallel -- warp w runs every fourth tile of the CTA's
-    // range with all 64 keys (eight independent MMA chains), four tiles in flight;
-    // 32 rows (MT = 2): each tile split into two key slices of 32 keys per m-tile
-    constexpr bool TP = MT == 1;
-    static_assert(!TP || NS % kConsumerWarps == 0, "tile-parallel stages have one owner each");
-    constexpr int NT = TP ? kTileKeys / 8 : 2 * MT;  // n-tiles of 8 keys per warp per tile
-    constexpr int KW = 16 * MT;
-    const int key0 = TP ? 0 : slice * KW;
+    // Tile-parallel groups: the MT warps of group `slice` (one per 16-row m-tile) run
+    // every (4 / MT)-th tile of the CTA's range with all 64 keys (eight independent
+    // MMA chains per warp); 4 / MT tiles are in flight
+    constexpr int kGroups = kConsumerWarps / MT;
+    static_assert(NS % kGroups == 0, "each stage belongs to one group");
+    constexpr int NT = kTileKeys / 8;  // n-tiles of 8 keys per warp per tile
+    const int key0 = 0;
     const int g = lane >> 2, tq = lane & 3;
     const int r0 = mt * 16 + g, r1 = r0 + 8;
     const int t0 = r0 / p.G, t1 = r1 / p.G;
@@ -750,7 +749,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int stg = (int)(k % NS);
         const uint32_t ph = (uint32_t)((k / NS) & 1);
-        const bool mine = !TP || (int)(k % kConsumerWarps) == warp;
+        const bool mine = (int)(k % kGroups) == slice;
         if (mine && !timed_out && !mbar_wait(&sh.full[stg], ph)) {
             set_err(p.dev_err, HSA_DEVERR_TIMEOUT);
             timed_out = true;
