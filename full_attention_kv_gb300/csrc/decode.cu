@@ -545,7 +545,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) {
             mbar_init(&sh.full[s], 1);
-            mbar_init(&sh.empty[s], MT);  // the MT warps of the owning group
+            // full layers: the MT warps of the owning group; rings: every consumer warp
+            mbar_init(&sh.empty[s], (p.flags & kDecodeRing) ? kConsumerWarps : MT);
         }
         fence_barrier_init();
     }
@@ -676,13 +677,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // -------------------------------------------------------------------- consumers
     const int mt = warp % MT;
     const int slice = warp / MT;
-    // Tile-parallel groups: the MT warps of group `slice` (one per 16-row m-tile) run
-    // every (4 / MT)-th tile of the CTA's range with all 64 keys (eight independent
-    // MMA chains per warp); 4 / MT tiles are in flight
+    // Full layers (long units of pages): tile-parallel groups -- the MT warps of group
+    // `slice` (one per 16-row m-tile) run every (4 / MT)-th tile of the CTA's range
+    // with all 64 keys (eight independent MMA chains per warp), 4 / MT tiles in
+    // flight.  Rings (two tiles per unit): every warp runs its 16 MT-key slice of
+    // every tile, which keeps a unit's latency short.
     constexpr int kGroups = kConsumerWarps / MT;
     static_assert(NS % kGroups == 0, "each stage belongs to one group");
-    constexpr int NT = kTileKeys / 8;  // n-tiles of 8 keys per warp per tile
-    const int key0 = 0;
+    const bool tp = (p.flags & kDecodeRing) == 0;
+    const int key0 = tp ? 0 : slice * 16 * MT;
     const int g = lane >> 2, tq = lane & 3;
     const int r0 = mt * 16 + g, r1 = r0 + 8;
     const int t0 = r0 / p.G, t1 = r1 / p.G;
@@ -749,7 +752,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int stg = (int)(k % NS);
         const uint32_t ph = (uint32_t)((k / NS) & 1);
-        const bool mine = (int)(k % kGroups) == slice;
+        const bool mine = !tp || (int)(k % kGroups) == slice;
         if (mine && !timed_out && !mbar_wait(&sh.full[stg], ph)) {
             set_err(p.dev_err, HSA_DEVERR_TIMEOUT);
             timed_out = true;
@@ -776,14 +779,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             // full layers: every key of a complete page is visible to every query
             const bool all_vis = !ring && (j + 1) * kTileKeys <= c;
-            if constexpr (FP8) {
+            if constexpr (FP8) {  // full layers only: tile-parallel
                 const uint8_t *base = sh.stage + stg * kFp8StageStride;
                 const float *ksc = reinterpret_cast<const float *>(base + 2 * kFp8TileBytes);
-                run_tile_fp8<NT>(st, qa, base, base + kFp8TileBytes, ksc, ksc + 64, key0,
-                                 p.scale_log2, all_vis, t0 < T, t1 < T, vis);
+                run_tile_fp8<kTileKeys / 8>(st, qa, base, base + kFp8TileBytes, ksc, ksc + 64,
+                                            key0, p.scale_log2, all_vis, t0 < T, t1 < T, vis);
+            } else if (tp) {
+                run_tile<kTileKeys / 8>(st, qa, sK, sV, kTileKeys, key0, p.scale_log2, all_vis,
+                                        t0 < T, t1 < T, vis);
             } else {
-                run_tile<NT>(st, qa, sK, sV, kTileKeys, key0, p.scale_log2, all_vis, t0 < T,
-                             t1 < T, vis);
+                run_tile<2 * MT>(st, qa, sK, sV, kTileKeys, key0, p.scale_log2, all_vis,
+                                 t0 < T, t1 < T, vis);
             }
         }
         __syncwarp();
