@@ -633,10 +633,10 @@ def _ctx_desc(cfg):
 # workload and the source digest of the kernel it was taken on (None = not taken
 # on the current kernel).
 TRAFFIC = {
-    # profiles/decode_full_ncu_decode-b4.md: 389.5 MB on 4 sequences, scaled by units
-    "decode": ("5bb42670f6f357ac", 2831917823),
-    # profiles/prefill_full_ncu_prefill-r2.md: 5.846 GB on 2 requests, scaled by flops
-    "prefill": ("86e2430f370d57d3", 18418300622),
+    # profiles/decode_full_ncu_decode-b4.md: 389.4 MB on 4 sequences, scaled by units
+    "decode": ("f613d09609196f8a", 2831065198),
+    # profiles/prefill_full_ncu_prefill-r2.md: 4.552 GB on 2 requests, scaled by flops
+    "prefill": ("a02724ec0bfdb633", 14340211242),
 }
 
 
