@@ -507,3 +507,33 @@ def test_fp8_history_attention_equals_bf16_oracle_on_exact_values():
     a2 = oracle.attention_fp8hist(cu, pl, q, kn, vn, codes_k, two, codes_v, two, ho, 0.3)
     b2 = oracle.attention(cu, pl, q, kn, vn, bk2, bv2, ho, np.zeros(R, np.int32), 0, 0.3)
     assert np.max(np.abs(a2 - b2)) == 0.0
+
+
+# ---------------------------------------------------------------- prefix model
+# youleyou.com s2 "KVCache系统重构": a hit counts up to the window-safe length; the
+# Full index is authoritative; SWA is kept for a finished request's last window.
+
+def test_prefix_model_hand_cases():
+    from oracle.prefix_model import PrefixModel, ring_positions
+    m = PrefixModel(W=4)
+    assert m.match([1, 2]) == (0, [], -1, [-1] * 4)
+    dup, kept = m.insert([1, 2, 3, 4, 5, 6], [10, 11, 12, 13, 14, 15], 7, ring_positions(6, 4))
+    assert dup == [] and kept
+    assert ring_positions(6, 4) == [4, 5, 2, 3]           # slot s keeps the latest p = s mod 4
+    # a follow-up turn: full match, the path's own ring, every window position live
+    mm, slots, row, pos = m.match([1, 2, 3, 4, 5, 6, 9])
+    assert (mm, slots, row) == (6, [10, 11, 12, 13, 14, 15], 7)
+    assert int(oracle.window_safe_len_ring([mm], [pos], 4)[0]) == 6
+    # a branch before the path's end: the ring was written past the match
+    mm, _, row, pos = m.match([1, 2, 3, 8])
+    assert (mm, row) == (3, 7) and int(oracle.window_safe_len_ring([mm], [pos], 4)[0]) < 4
+    # a second path through the same point: the shorter path's ring is offered first
+    dup, kept = m.insert([1, 2, 3, 9], [10, 11, 12, 30], 8, ring_positions(4, 4))
+    assert dup == [] and kept
+    assert m.match([1, 2, 3, 5])[2] == 8
+    # duplicates: a request that recomputed a cached position returns its own slot
+    dup, kept = m.insert([1, 2, 7], [40, 41, 42], 8, ring_positions(3, 4))
+    assert dup == [40, 41] and not kept                   # row 8 is already held
+    # dropping the Full slots of a suffix shortens later matches
+    m.drop_slots([14, 15])
+    assert m.match([1, 2, 3, 4, 5, 6])[0] == 4
