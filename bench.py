@@ -462,6 +462,16 @@ def _prefetch_report(step, args, stream):
             "prefetch_alone_gbs": step.prefetch_bytes / (alone_ms / 1e3) / 1e9}
 
 
+def _swap_io(step, ins, outs):
+    """Point a step's input (q, k, v per layer) and output lists at other tensors;
+    returns the previous (inputs, outputs) for restoring."""
+    prev = (step.inputs(), step.outputs())
+    n = len(step.q)
+    step.q, step.k, step.v = list(ins[:n]), list(ins[n:2 * n]), list(ins[2 * n:3 * n])
+    step.out = list(outs)
+    return prev
+
+
 def run_ours(args, inst, ws, rank, local):
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
@@ -526,28 +536,60 @@ def run_ours(args, inst, ws, rank, local):
     step_ms = max_over_ranks(step_ms, ws)
 
     # ---- end to end through the C ABI with host buffers ----------------------
+    # A serving loop: every step copies its inputs from pinned host memory and reads
+    # its outputs back, all inside the timed region.  Two device input / output sets,
+    # each with its own captured step, let step i+1's host-to-device copies (one
+    # stream) and step i's device-to-host read (another) overlap step i's kernels.
     h_in = [t.cpu().pin_memory() for t in step.inputs()]
     h_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in step.outputs()]
-    d_in = step.inputs()
     h2d = sum(t.numel() * t.element_size() for t in h_in)
     d2h = sum(t.numel() * t.element_size() for t in h_out)
+    sets = [(step.inputs(), step.outputs(), graph)]
+    alt_in = [torch.empty_like(t) for t in step.inputs()]
+    alt_out = [torch.empty_like(t) for t in step.outputs()]
+    saved = _swap_io(step, alt_in, alt_out)
+    with torch.cuda.stream(stream):
+        step()  # warm the second set once before capture
+    torch.cuda.synchronize()
+    graph_b = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph_b, stream=stream):
+        step()
+    torch.cuda.synchronize()
+    _swap_io(step, *saved)
+    sets.append((alt_in, alt_out, graph_b))
     cur = torch.cuda.current_stream()
-    for _ in range(2):
-        for h, d in zip(h_in, d_in):
-            d.copy_(h, non_blocking=True)
-        graph.replay()
-        for h, d in zip(h_out, step.outputs()):
-            h.copy_(d, non_blocking=True)
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event(), torch.cuda.Event()]
+    ev_done = [torch.cuda.Event(), torch.cuda.Event()]
+    ev_out = [torch.cuda.Event(), torch.cuda.Event()]
+
+    def serve(n):
+        for i in range(n):
+            b = i & 1
+            d_in, d_out, g = sets[b]
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(ev_done[b])   # step i-2 has consumed this input set
+                for h, d in zip(h_in, d_in):
+                    d.copy_(h, non_blocking=True)
+                ev_in[b].record(s_in)
+            cur.wait_event(ev_in[b])
+            if i >= 2:
+                cur.wait_event(ev_out[b])         # step i-2's outputs are read back
+            g.replay()
+            ev_done[b].record(cur)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_done[b])
+                for h, d in zip(h_out, d_out):
+                    h.copy_(d, non_blocking=True)
+                ev_out[b].record(s_out)
+
+    serve(2)
     torch.cuda.synchronize()
     barrier(ws)
     t0 = time.perf_counter()
-    for _ in range(args.steps):
-        for h, d in zip(h_in, d_in):
-            d.copy_(h, non_blocking=True)
-        graph.replay()
-        for h, d in zip(h_out, step.outputs()):
-            h.copy_(d, non_blocking=True)
-    cur.synchronize()
+    serve(args.steps)
+    torch.cuda.synchronize()
     e2e_s = (time.perf_counter() - t0) / args.steps
     e2e_s = max_over_ranks(e2e_s, ws)
 
