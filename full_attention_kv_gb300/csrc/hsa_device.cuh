@@ -273,13 +273,6 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v)
     return pack_f16(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
 }
 
-__device__ __forceinline__ uint32_t lds32(uint32_t saddr)
-{
-    uint32_t v;
-    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(saddr));
-    return v;
-}
-
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
 {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);

@@ -160,3 +160,38 @@ def test_fp8_layers_are_decode_only():
     with pytest.raises(hsa.HsaError) as e:
         hsa.hsa_decode_attn(both, 0, q, k, v, cl, inst.cfg.scale)
     assert e.value.status == hsa.HSA_UNSUPPORTED_SHAPE
+
+
+@pytest.mark.parametrize("T", [1, 2, 4])
+def test_fp8_ragged_contexts(T):
+    """Empty, one-token, page-edge and partial-page contexts with 1, 2 and 4 new
+    tokens on an FP8 full layer, every row against the oracle; the fused append's
+    codes bit-exact."""
+    import dataclasses
+    hsa = _cuda()
+    contexts = (0, 1, 63, 64, 65, 127, 200)
+    cfg = dataclasses.replace(workload.CONFIGS["tiny"], T=T, contexts=contexts, B=len(contexts),
+                              index=70 + T)
+    inst = workload.draw(cfg)
+    l = 6
+    pool = harness.make_pool(inst, [l], fp8=True)
+    q, k, v, cl = harness.decode_inputs(inst, l)
+    ws = hsa.decode_workspace(pool, inst.R, T)
+    out = hsa.hsa_decode_attn_append(pool, 0, q, k, v, cl, cfg.scale, workspace=ws)
+    torch.cuda.synchronize()
+    ref = oracle.attention_fp8hist(scale=cfg.scale, **_fp8_case(inst, l, range(inst.R)))
+    got = out.view(-1, cfg.Hq, cfg.d).float().cpu().numpy()
+    err = float(np.max(np.abs(got - ref)))
+    assert err <= TOL, "T=%d: %g" % (T, err)
+    kc, ks, vc, vs = _logical(pool, 0)
+    pg = cfg.page
+    for s in range(inst.R):
+        ek, eks = oracle.quantize_e4m3(k[s].cpu())
+        ev, evs = oracle.quantize_e4m3(v[s].cpu())
+        for t in range(T):
+            pos = int(inst.prefix[s]) + t
+            blk = int(inst.block_tables[s, pos // pg])
+            assert np.array_equal(kc[blk, :, pos % pg], ek[t])
+            assert np.array_equal(vc[blk, :, pos % pg], ev[t])
+            assert np.array_equal(ks[blk, :, pos % pg], eks[t])
+            assert np.array_equal(vs[blk, :, pos % pg], evs[t])
