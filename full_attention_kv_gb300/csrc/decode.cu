@@ -74,6 +74,7 @@ struct SharedStorage {
     alignas(16) float comb[kConsumerWarps][kCombFloats];
     alignas(8) uint64_t full[kMaxStages];
     alignas(8) uint64_t empty[kMaxStages];
+    int32_t tile_ok[kMaxStages];  // the producer loaded the stage's tile (else: masked)
     int32_t scan[kThreads];
     int32_t first_b;
     int32_t first_items_before;  // items of all units of sequences < first_b (per KV head)
@@ -633,6 +634,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             Walk w = w0;
             int64_t k = 0;
             const int64_t fp8_cb = fp8_codes_bytes(p.num_blocks, p.Hkv);
+            // the block-table read of the next tile is issued before waiting for its
+            // stage, so its latency hides behind the wait
+            int64_t row = i0 < i1 ? tile_row(p, w, true) : -1;
             for (int64_t i = i0; i < i1; ++i, ++k) {
                 const int st = (int)(k % NS);
                 const uint32_t ph = (uint32_t)((k / NS) & 1);
@@ -640,7 +644,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     set_err(p.dev_err, HSA_DEVERR_TIMEOUT);
                     break;
                 }
-                const int64_t row = tile_row(p, w, true);
+                // read by the stage's consumers after the full barrier (whose arrive
+                // below releases this write)
+                sh.tile_ok[st] = row >= 0 ? 1 : 0;
                 if (FP8 && row >= 0) {
                     // E4M3 K page (64 rows x 128 B), transposed V page (128 rows x 64 B),
                     // and the page's 64 K and 64 V scales
@@ -664,6 +670,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive(&sh.full[st]);
                 }
                 walk_next(p, w);
+                row = i + 1 < i1 ? tile_row(p, w, true) : -1;
             }
             // drain: no TMA write may still be in flight when the CTA exits
             for (int64_t s = 0; s < NS && s < k; ++s) {
@@ -757,7 +764,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             set_err(p.dev_err, HSA_DEVERR_TIMEOUT);
             timed_out = true;
         }
-        const bool loaded = mine && !timed_out && tile_row(p, w, false) >= 0;
+        const bool loaded = mine && !timed_out && sh.tile_ok[stg] != 0;
         const int c = w.c;
         const int j = w.j;
         bool any = loaded;
