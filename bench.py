@@ -675,8 +675,8 @@ def _ctx_desc(cfg):
 # workload and the source digest of the kernel it was taken on (None = not taken
 # on the current kernel).
 TRAFFIC = {
-    # profiles/decode_full_ncu_decode-b4.md: 389.4 MB on 4 sequences, scaled by units
-    "decode": ("f613d09609196f8a", 2831065198),
+    # profiles/decode_full_ncu_decode-b4.md: 389.6 MB on 4 sequences, scaled by units
+    "decode": ("84b124d5e4ec1152", 2832576564),
     # profiles/prefill_full_ncu_prefill-r2.md: 4.552 GB on 2 requests, scaled by flops
     "prefill": ("a02724ec0bfdb633", 14340211242),
 }
