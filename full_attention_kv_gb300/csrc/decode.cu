@@ -547,7 +547,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < NS; ++s) {
             mbar_init(&sh.full[s], 1);
             // full layers: the MT warps of the owning group; rings: every consumer warp
-            mbar_init(&sh.empty[s], (p.flags & kDecodeRing) ? kConsumerWarps : MT);
+            // the warps of the stage's owning group: MT (full layers), 2 (rings)
+            mbar_init(&sh.empty[s], (p.flags & kDecodeRing) ? 2 : MT);
         }
         fence_barrier_init();
     }
@@ -687,12 +688,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Full layers (long units of pages): tile-parallel groups -- the MT warps of group
     // `slice` (one per 16-row m-tile) run every (4 / MT)-th tile of the CTA's range
     // with all 64 keys (eight independent MMA chains per warp), 4 / MT tiles in
-    // flight.  Rings (two tiles per unit): every warp runs its 16 MT-key slice of
-    // every tile, which keeps a unit's latency short.
+    // flight.  Rings (a unit is two tiles): two groups, one per tile of a unit, so the
+    // two run side by side -- MT = 1: two warps per tile, 32 keys each; MT = 2: one
+    // warp per m-tile with all 64 keys.
     constexpr int kGroups = kConsumerWarps / MT;
-    static_assert(NS % kGroups == 0, "each stage belongs to one group");
-    const bool tp = (p.flags & kDecodeRing) == 0;
-    const int key0 = tp ? 0 : slice * 16 * MT;
+    static_assert(NS % kGroups == 0 && NS % 2 == 0, "each stage belongs to one group");
+    const bool ring = (p.flags & kDecodeRing) != 0;
+    const int wt = (ring && MT == 1) ? 2 : 1;  // warps per m-tile sharing a tile
+    const int groups = ring ? 2 : kGroups;
+    const int key0 = (slice % wt) * (kTileKeys / wt);
     const int g = lane >> 2, tq = lane & 3;
     const int r0 = mt * 16 + g, r1 = r0 + 8;
     const int t0 = r0 / p.G, t1 = r1 / p.G;
@@ -759,7 +763,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int stg = (int)(k % NS);
         const uint32_t ph = (uint32_t)((k / NS) & 1);
-        const bool mine = !tp || (int)(k % kGroups) == slice;
+        const bool mine = (int)(k % groups) == slice / wt;
         if (mine && !timed_out && !mbar_wait(&sh.full[stg], ph)) {
             set_err(p.dev_err, HSA_DEVERR_TIMEOUT);
             timed_out = true;
@@ -791,12 +795,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float *ksc = reinterpret_cast<const float *>(base + 2 * kFp8TileBytes);
                 run_tile_fp8<kTileKeys / 8>(st, qa, base, base + kFp8TileBytes, ksc, ksc + 64,
                                             key0, p.scale_log2, all_vis, t0 < T, t1 < T, vis);
-            } else if (tp) {
+            } else if (wt == 1) {
                 run_tile<kTileKeys / 8>(st, qa, sK, sV, kTileKeys, key0, p.scale_log2, all_vis,
                                         t0 < T, t1 < T, vis);
             } else {
-                run_tile<2 * MT>(st, qa, sK, sV, kTileKeys, key0, p.scale_log2, all_vis,
-                                 t0 < T, t1 < T, vis);
+                run_tile<kTileKeys / 16>(st, qa, sK, sV, kTileKeys, key0, p.scale_log2, all_vis,
+                                         t0 < T, t1 < T, vis);
             }
         }
         __syncwarp();
