@@ -676,7 +676,7 @@ def _ctx_desc(cfg):
 # on the current kernel).
 TRAFFIC = {
     # profiles/decode_full_ncu_decode-b4.md: 389.6 MB on 4 sequences, scaled by units
-    "decode": ("84b124d5e4ec1152", 2832576564),
+    "decode": ("b7487d1774b2c444", 2832812948),
     # profiles/prefill_full_ncu_prefill-r2.md: 4.552 GB on 2 requests, scaled by flops
     "prefill": ("a02724ec0bfdb633", 14340211242),
 }
