@@ -672,22 +672,30 @@ def _ctx_desc(cfg):
 
 
 # DRAM bytes per launch of the dominant kernel from an ncu capture, keyed by the
-# workload and the source digest of the kernel it was taken on (None = not taken
-# on the current kernel).
+# workload and the code digest (code_digest) of the kernel it was taken on (None =
+# not taken on the current kernel).
 TRAFFIC = {
     # profiles/decode_full_ncu_decode-b4.md: 389.6 MB on 4 sequences, scaled by units
-    "decode": ("b7487d1774b2c444", 2832812948),
+    "decode": ("8968219e5757c4b2", 2832812948),
     # profiles/prefill_full_ncu_prefill-r2.md: 4.552 GB on 2 requests, scaled by flops
-    "prefill": ("a02724ec0bfdb633", 14340211242),
+    "prefill": ("0e97e900cd7e5029", 14340211242),
 }
 
 
-def _traffic(name):
+def code_digest(path):
+    """First 16 hex digits of the SHA-256 of a CUDA source with its comments and
+    blank lines removed, so that editing a comment keeps a capture valid."""
     import hashlib
+    import re
+    with open(path) as f:
+        s = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
+    lines = [re.sub(r"//.*$", "", l).rstrip() for l in s.splitlines()]
+    return hashlib.sha256("\n".join(l for l in lines if l).encode()).hexdigest()[:16]
+
+
+def _traffic(name):
     kern = "prefill.cu" if workload.CONFIGS[name].kind == "prefill" else "decode.cu"
-    src = os.path.join(ROOT, "full_attention_kv_gb300", "csrc", kern)
-    with open(src, "rb") as f:
-        digest = hashlib.sha256(f.read()).hexdigest()[:16]
+    digest = code_digest(os.path.join(ROOT, "full_attention_kv_gb300", "csrc", kern))
     t = TRAFFIC.get(name)
     if t and t[0] == digest:
         return t[1]

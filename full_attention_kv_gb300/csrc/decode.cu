@@ -15,14 +15,18 @@
 //    128-slot ring row.  Items of all (sequence, KV head) units are laid end to
 //    end and cut into equal contiguous ranges, one per CTA (flash-decoding with
 //    perfect balance whatever the length mix).
-//  * A producer warp streams each tile's K and V (2 x 16 KB) into a 4-stage
-//    shared-memory ring with TMA (128-byte swizzle), mbarrier-tracked.
-//  * Four consumer warps run the tile on tensor cores (mma.sync m16n8k16 bf16,
-//    fp32 accumulate).  GQA packing: the G query heads x T tokens that share a KV
-//    head form the M dimension (row = t * G + hh), so each KV byte is read once for
-//    all of them.  16 rows (T <= 2): each warp owns 16 keys of every tile; 32 rows
-//    (T = 3, 4): two warps per 16-row m-tile, 32 keys each.  Online softmax in
-//    registers (exp2, quad shuffles).
+//  * A producer warp streams each tile's K and V (2 x 16 KB bf16; FP8 codes plus
+//    their scales for an FP8 full layer) into a shared-memory stage ring with TMA
+//    (128-byte swizzle), mbarrier-tracked; 4 stages bf16, 8 FP8.  It flags per stage
+//    whether a tile was loaded and reads the next block-table entry before waiting
+//    for a free stage.
+//  * Four consumer warps run tiles on tensor cores (mma.sync m16n8k16, fp32
+//    accumulate).  GQA packing: the G query heads x T tokens that share a KV head
+//    form the M dimension (row = t * G + hh), so each KV byte is read once for all of
+//    them; MT = 1 (T <= 2) or 2 (T = 3, 4) 16-row m-tiles.  Full layers: 4 / MT
+//    groups of MT warps, a group taking every (4 / MT)-th tile with all 64 keys, so
+//    several tiles are in flight.  Rings: two groups, one per tile of a unit.  Online
+//    softmax in registers (exp2, quad shuffles).
 //  * At the end of a unit the warps merge their softmax states through shared
 //    memory.  A unit covered by one CTA is written straight to `out`; a unit split
 //    across CTAs leaves (m, l, o) partials in the workspace and the last CTA to

@@ -1,0 +1,64 @@
+"""Host-side arithmetic of bench.py: the algorithmic bytes and flops the roofline
+divides by, and the code digest that keys a traffic capture to a kernel.
+
+The byte and flop counts are checked against hand counts and brute-force key
+enumeration on small cases: each query row of a full layer sees every position up
+to its own, a sliding-layer row the newest W of them [hotdry.top "MiMo-V2.5
+ultra-speed inference architecture", "Hybrid SWA"]."""
+import dataclasses
+
+import numpy as np
+
+import bench
+import workload
+
+
+def test_decode_bytes_by_hand():
+    inst = workload.draw(workload.CONFIGS["tiny"])  # contexts 100, 128, 300, 512; T = 1
+    per_tok = 2 * 2 * 128 * 2        # K and V, Hkv = 2, d = 128, bf16
+    qo = 2 * 4 * 1 * 16 * 128 * 2    # q read + out written: R x T x Hq x d, bf16
+    assert bench.decode_bytes(inst, True) == (101 + 129 + 301 + 513) * per_tok + qo
+    assert bench.decode_bytes(inst, False) == (101 + 128 + 128 + 128) * per_tok + qo
+    # FP8 full layer: cached rows as codes + one fp32 scale per (token, head), new rows bf16
+    fp8_tok = 2 * 2 * (128 + 4)
+    assert bench.decode_bytes(inst, True, fp8=True) == 1040 * fp8_tok + 4 * per_tok + qo
+
+
+def test_decode_bytes_mtp_sliding_window():
+    """T = 4: the oldest of the four new rows still sees W keys, the newest W + 3
+    distinct keys are read in all."""
+    cfg = dataclasses.replace(workload.CONFIGS["tiny"], T=4, contexts=(0, 5, 200), B=3)
+    inst = workload.draw(cfg)
+    per_tok = 2 * cfg.Hkv * cfg.d * 2
+    qo = 2 * 3 * 4 * cfg.Hq * cfg.d * 2
+    assert bench.decode_bytes(inst, False) == (4 + 9 + 131) * per_tok + qo
+
+
+def _brute_keys(P, C, W, full):
+    n = 0
+    for i in range(C):
+        q = P + i
+        n += sum(1 for k in range(q + 1) if full or q - k < W)
+    return n
+
+
+def test_prefill_flops_against_enumeration():
+    cfg = dataclasses.replace(workload.CONFIGS["prefill"], prefixes=(0, 3, 130, 257),
+                              chunks=(5, 128, 1, 300), R=4)
+    inst = workload.draw(cfg)
+    for full in (True, False):
+        keys = sum(_brute_keys(int(P), int(C), cfg.W, full)
+                   for P, C in zip(inst.prefix, inst.new))
+        assert bench.prefill_flops(inst, full) == 4 * cfg.d * cfg.Hq * keys
+        assert int(bench.keys_per_row(inst, full).sum()) == keys
+
+
+def test_code_digest_ignores_comments_only(tmp_path):
+    a = tmp_path / "a.cu"
+    a.write_text("// header\n__global__ void k(int *p) {\n  p[0] = 1;  // one\n}\n")
+    b = tmp_path / "b.cu"
+    b.write_text("/* other\n   header */\n\n__global__ void k(int *p) {\n  p[0] = 1;\n}\n")
+    c = tmp_path / "c.cu"
+    c.write_text("__global__ void k(int *p) {\n  p[0] = 2;\n}\n")
+    assert bench.code_digest(a) == bench.code_digest(b)
+    assert bench.code_digest(a) != bench.code_digest(c)
