@@ -219,7 +219,7 @@ hsa_status decode_common(const hsa_pools *pools, int32_t layer, const void *q, c
     if (B < 0 || T < 1 || max_ctas < 0)
         return HSA_INVALID_ARG;
     const int G = pools->Hq / pools->Hkv;
-    if (G * T > 32 || T > 16)
+    if (T > 4 || G * T > 32)
         return HSA_UNSUPPORTED_SHAPE;
     if (B > pools->batch)
         return HSA_INVALID_ARG;

@@ -13,8 +13,6 @@
 
 #include "../../include/hsa.h"
 
-#define HSA_DEVERR_TIMEOUT 32  // a bounded wait gave up (internal, reported via dev_err)
-
 #ifndef HSA_WAIT_NS
 #define HSA_WAIT_NS 2000000000ull  // 2 s: far beyond any legitimate wait (microseconds)
 #endif

@@ -54,6 +54,8 @@ typedef int hsa_status;
 #define HSA_DEVERR_BAD_SEQ 4     /* sequence index outside [0, batch) */
 #define HSA_DEVERR_BAD_RING 8    /* ring row outside [0, n_ring_rows) */
 #define HSA_DEVERR_BAD_LEN 16    /* negative length or offsets out of order */
+#define HSA_DEVERR_TIMEOUT 32    /* a bounded wait inside a kernel (2 s) gave up: the kernel
+                                    stopped early and its outputs are incomplete */
 
 /*
  * The dual KV pool of one model (host struct of device pointers).
@@ -137,7 +139,7 @@ hsa_status hsa_kv_append(const hsa_pools *pools, int32_t layer, const void *k_ne
  * among themselves.
  *  q      [B, T, Hq, d] bf16      k_new, v_new [B, T, Hkv, d] bf16
  *  out    [B, T, Hq, d] bf16      cached_len   device int32 [B]
- *  T in 1..4.  Full layers attend positions 0 .. cached_len+t; sliding layers
+ *  T in 1..4 (else HSA_UNSUPPORTED_SHAPE).  Full layers attend positions 0 .. cached_len+t; sliding layers
  *  attend the last W positions, the cached part read from the ring.
  *  Full layers split each sequence's pages across all SMs (flash-decoding) and
  *  merge the partial softmax states in the same kernel; that needs `workspace`
@@ -199,7 +201,8 @@ hsa_status hsa_decode_attn_noalloc(const hsa_pools *pools, int32_t layer, const 
  * rows cu_rows[r] .. cu_rows[r+1]-1 at positions prefix_len[r] + i.
  *  q  [rows, Hq, d] bf16     k_new, v_new [rows, Hkv, d] bf16    out [rows, Hq, d] bf16
  *  cu_rows [R+1], prefix_len [R], seq_idx [R]: device int32.
- *  max_chunk: host upper bound on any request's row count (sizes the grid).
+ *  max_chunk: host upper bound on any request's row count (sizes the grid); rows of a
+ *  request past the bound it implies are left unwritten, so it must not understate.
  * A sliding layer needs the ring to hold the prefix's last W positions.
  */
 hsa_status hsa_prefill_attn(const hsa_pools *pools, int32_t layer, const void *q,
