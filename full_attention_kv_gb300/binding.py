@@ -153,6 +153,25 @@ def _need(t, name, dtype, device=None, ndim=None):
         raise ValueError("%s must have %d dims, got %d" % (name, ndim, t.dim()))
 
 
+def _shape(t, name, shape):
+    """The library takes plain pointers: sizes the pool implies are checked here."""
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must have shape %s, got %s" % (name, tuple(shape), tuple(t.shape)))
+
+
+def _same_device(ref, *ts):
+    for t in ts:
+        if t is not None and t.device != ref.device:
+            raise ValueError("all device tensors must be on %s" % ref.device)
+
+
+def _need_err(dev_err):
+    if dev_err is not None:
+        _need(dev_err, "dev_err", torch.int32)
+        if dev_err.numel() < 1:
+            raise ValueError("dev_err must hold one int32")
+
+
 def _check(fn, status):
     if status != HSA_OK:
         raise HsaError(fn, status)
@@ -274,8 +293,10 @@ def hsa_kv_append(pool, layer, k_new, v_new, cu_tokens, seq_idx, start_pos, dev_
     R = seq_idx.shape[0]
     if cu_tokens.shape[0] != R + 1 or start_pos.shape[0] != R:
         raise ValueError("cu_tokens must be [R+1] and start_pos [R]")
-    if dev_err is not None:
-        _need(dev_err, "dev_err", torch.int32)
+    _shape(k_new, "k_new", (k_new.shape[0], pool.Hkv, pool.d))
+    _shape(v_new, "v_new", k_new.shape)
+    _need_err(dev_err)
+    _same_device(k_new, v_new, cu_tokens, seq_idx, start_pos, dev_err)
     s = lib().hsa_kv_append(pool.ref(), int(layer), _ptr(k_new), _ptr(v_new), _ptr(cu_tokens),
                             _ptr(seq_idx), _ptr(start_pos), R, k_new.shape[0], _ptr(dev_err),
                             _stream(stream))
@@ -292,6 +313,15 @@ def decode_workspace(pool, B, T, device="cuda"):
     return torch.zeros(max(n, 16), dtype=torch.uint8, device=device)
 
 
+def _decode_shapes(pool, q, k_new, v_new, cached_len):
+    B, T = q.shape[0], q.shape[1]
+    _shape(q, "q", (B, T, pool.Hq, pool.d))
+    _shape(k_new, "k_new", (B, T, pool.Hkv, pool.d))
+    _shape(v_new, "v_new", (B, T, pool.Hkv, pool.d))
+    _shape(cached_len, "cached_len", (B,))
+    _same_device(q, k_new, v_new, cached_len)
+
+
 def hsa_decode_attn(pool, layer, q, k_new, v_new, cached_len, scale, out=None, workspace=None,
                     max_ctas=0, dev_err=None, stream=None, append=False):
     _need(q, "q", torch.bfloat16, ndim=4)
@@ -299,14 +329,16 @@ def hsa_decode_attn(pool, layer, q, k_new, v_new, cached_len, scale, out=None, w
     _need(v_new, "v_new", torch.bfloat16, ndim=4)
     _need(cached_len, "cached_len", torch.int32, ndim=1)
     B, T = q.shape[0], q.shape[1]
+    _decode_shapes(pool, q, k_new, v_new, cached_len)
     if out is None:
         out = torch.empty_like(q)
     _need(out, "out", torch.bfloat16, ndim=4)
+    _shape(out, "out", q.shape)
     if workspace is None:
         workspace = decode_workspace(pool, B, T, device=q.device)
     _need(workspace, "workspace", torch.uint8)
-    if dev_err is not None:
-        _need(dev_err, "dev_err", torch.int32)
+    _need_err(dev_err)
+    _same_device(q, out, workspace, dev_err)
     fn = lib().hsa_decode_attn_append if append else lib().hsa_decode_attn
     s = fn(pool.ref(), int(layer), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(cached_len), B, T,
            float(scale), _ptr(out), _ptr(workspace), workspace.numel(), int(max_ctas),
@@ -335,8 +367,10 @@ def hsa_decode_attn_noalloc(pool, layer, q, k_new, v_new, cached_len, scale, out
     _need(v_new, "v_new", torch.bfloat16, ndim=4)
     _need(cached_len, "cached_len", torch.int32, ndim=1)
     _need(out, "out", torch.bfloat16, ndim=4)
-    if dev_err is not None:
-        _need(dev_err, "dev_err", torch.int32)
+    _decode_shapes(pool, q, k_new, v_new, cached_len)
+    _shape(out, "out", q.shape)
+    _need_err(dev_err)
+    _same_device(q, out, dev_err)
     B, T = q.shape[0], q.shape[1]
     s = lib().hsa_decode_attn_noalloc(pool.ref(), int(layer), _ptr(q), _ptr(k_new), _ptr(v_new),
                                       _ptr(cached_len), B, T, float(scale), _ptr(out),
@@ -353,11 +387,18 @@ def hsa_prefill_attn(pool, layer, q, k_new, v_new, cu_rows, prefix_len, seq_idx,
     for n, t in (("cu_rows", cu_rows), ("prefix_len", prefix_len), ("seq_idx", seq_idx)):
         _need(t, n, torch.int32, ndim=1)
     R = seq_idx.shape[0]
+    rows = q.shape[0]
+    _shape(q, "q", (rows, pool.Hq, pool.d))
+    _shape(k_new, "k_new", (rows, pool.Hkv, pool.d))
+    _shape(v_new, "v_new", (rows, pool.Hkv, pool.d))
+    _shape(cu_rows, "cu_rows", (R + 1,))
+    _shape(prefix_len, "prefix_len", (R,))
     if out is None:
         out = torch.empty_like(q)
     _need(out, "out", torch.bfloat16, ndim=3)
-    if dev_err is not None:
-        _need(dev_err, "dev_err", torch.int32)
+    _shape(out, "out", q.shape)
+    _need_err(dev_err)
+    _same_device(q, k_new, v_new, cu_rows, prefix_len, seq_idx, out, dev_err)
     s = lib().hsa_prefill_attn(pool.ref(), int(layer), _ptr(q), _ptr(k_new), _ptr(v_new),
                                _ptr(cu_rows), _ptr(prefix_len), _ptr(seq_idx), R, q.shape[0],
                                int(max_chunk), float(scale), _ptr(out), _ptr(dev_err),
@@ -374,14 +415,15 @@ def hsa_swa_prefetch(pool, layer, host_k, host_v, host_row, seq_idx, dev_err=Non
             raise TypeError("%s must be a bf16 host tensor" % n)
         if not t.is_pinned() or not t.is_contiguous():
             raise ValueError("%s must be pinned and contiguous" % n)
-    if host_k.shape != host_v.shape or host_k.dim() != 4:
+    if host_k.shape != host_v.shape or host_k.dim() != 4 or \
+            tuple(host_k.shape[1:]) != (pool.Hkv, pool.W, pool.d):
         raise ValueError("host_k / host_v must be [n_host_rows, Hkv, W, d]")
     _need(host_row, "host_row", torch.int32, ndim=1)
     _need(seq_idx, "seq_idx", torch.int32, ndim=1)
     if host_row.shape != seq_idx.shape:
         raise ValueError("host_row and seq_idx must have the same length")
-    if dev_err is not None:
-        _need(dev_err, "dev_err", torch.int32)
+    _need_err(dev_err)
+    _same_device(host_row, seq_idx, dev_err)
     s = lib().hsa_swa_prefetch(pool.ref(), int(layer), ctypes.c_void_p(host_k.data_ptr()),
                                ctypes.c_void_p(host_v.data_ptr()), host_k.shape[0],
                                _ptr(host_row), _ptr(seq_idx), host_row.shape[0], _ptr(dev_err),
@@ -397,6 +439,9 @@ def hsa_window_safe_len(match_len, swa_slot_pos, W, out=None, stream=None):
         raise ValueError("swa_slot_pos must be [n, W]")
     if out is None:
         out = torch.empty_like(match_len)
+    _need(out, "out", torch.int32)
+    _shape(out, "out", match_len.shape)
+    _same_device(match_len, swa_slot_pos, out)
     s = lib().hsa_window_safe_len(_ptr(match_len), _ptr(swa_slot_pos), n, int(W), _ptr(out),
                                   _stream(stream))
     _check("hsa_window_safe_len", s)
@@ -412,6 +457,9 @@ def hsa_window_safe_len_bitmap(match_len, live_off, live, W, out=None, stream=No
         raise ValueError("live_off must be [n+1]")
     if out is None:
         out = torch.empty_like(match_len)
+    _need(out, "out", torch.int32)
+    _shape(out, "out", match_len.shape)
+    _same_device(match_len, live_off, live, out)
     s = lib().hsa_window_safe_len_bitmap(_ptr(match_len), _ptr(live_off), _ptr(live), n, int(W),
                                          _ptr(out), _stream(stream))
     _check("hsa_window_safe_len_bitmap", s)
