@@ -39,7 +39,7 @@ def _worker(rank, world, port, out):
 
 
 def test_two_ranks_draw_disjoint_shards_and_report_the_slowest():
-    mgr = mp.Manager()
+    mgr = mp.get_context("spawn").Manager()  # no fork of a multi-threaded process
     out = mgr.dict()
     mp.spawn(_worker, args=(2, _free_port(), out), nprocs=2, join=True)
     single = workload.draw(workload.CONFIGS["decode"]).prefix.tolist()
