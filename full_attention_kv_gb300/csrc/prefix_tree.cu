@@ -14,11 +14,17 @@
 // A radix tree over int32 tokens.  Node ids are stable (a split keeps the lower
 // part under the old id and gives the upper part a new one), so a lock handle -- the
 // id of the node where a match ended -- stays valid while the tree changes.
+// Every node caches the preferred ring holder of its subtree, so choosing the ring
+// row of a match costs O(1) however many paths share the match point; eviction
+// takes leaves from a heap ordered as the policies state, O(log n) per victim.
 #include <algorithm>
 #include <cstdint>
 #include <cstring>
+#include <functional>
 #include <new>
+#include <queue>
 #include <unordered_map>
+#include <utility>
 #include <vector>
 
 #include "../../include/hsa_tree.h"
@@ -36,6 +42,7 @@ struct Node {
     uint64_t ring_use = 0;                       // attach or last selection (SWA LRU)
     uint64_t last_use = 0;                       // last match or insert through it (Full LRU)
     int32_t lock = 0;
+    int32_t best = -1;                           // preferred ring holder in the subtree
     bool alive = false;
 };
 
@@ -99,36 +106,43 @@ struct hsa_ptree {
         return w;
     }
 
-    // Ring row for a match ending in node `end`: among the path ends in its subtree
-    // (the cached paths through the match point), the shortest path, then the
-    // latest attached row, then the smallest row id.  -1 if none.
-    int32_t choose_ring(const Walk &w) const
+    // Ring preference between two ring holders (b may be -1): the shorter path,
+    // then the later attached row, then the smaller row id.  A strict total order,
+    // since a row is attached at one node at most.
+    bool ring_better(int32_t a, int32_t b) const
     {
-        if (w.m == 0)
-            return -1;
-        int32_t best = -1;
-        std::vector<int32_t> stack(1, w.end);
-        while (!stack.empty()) {
-            const int32_t x = stack.back();
-            stack.pop_back();
-            const Node &nx = nodes[x];
-            if (nx.ring >= 0) {
-                if (best < 0) {
-                    best = x;
-                } else {
-                    const Node &nb = nodes[best];
-                    if (nx.depth < nb.depth ||
-                        (nx.depth == nb.depth &&
-                         (nx.ring_attach > nb.ring_attach ||
-                          (nx.ring_attach == nb.ring_attach && nx.ring < nb.ring))))
-                        best = x;
-                }
-            }
-            for (const auto &kv : nx.child)
-                stack.push_back(kv.second);
-        }
-        return best;
+        if (b < 0)
+            return true;
+        const Node &na = nodes[a], &nb = nodes[b];
+        if (na.depth != nb.depth)
+            return na.depth < nb.depth;
+        if (na.ring_attach != nb.ring_attach)
+            return na.ring_attach > nb.ring_attach;
+        return na.ring < nb.ring;
     }
+
+    // Recompute `best` of x and of its ancestors after a ring or a child of x
+    // changed.  An ancestor's value depends only on its own ring and its children's
+    // values, so the walk stops at the first node whose value is unchanged.
+    void refresh_best(int32_t x)
+    {
+        for (; x >= 0; x = nodes[x].parent) {
+            int32_t b = nodes[x].ring >= 0 ? x : -1;
+            for (const auto &kv : nodes[x].child) {
+                const int32_t cb = nodes[kv.second].best;
+                if (cb >= 0 && ring_better(cb, b))
+                    b = cb;
+            }
+            if (b == nodes[x].best)
+                return;
+            nodes[x].best = b;
+        }
+    }
+
+    // Ring row for a match ending in node `end`: the preferred ring holder among the
+    // path ends in its subtree (the cached paths through the match point).  -1 if
+    // none or if nothing matched.
+    int32_t choose_ring(const Walk &w) const { return w.m == 0 ? -1 : nodes[w.end].best; }
 
     void touch(int32_t x)
     {
@@ -153,9 +167,11 @@ struct hsa_ptree {
         nodes[nu.parent].child[nu.tok[0]] = u;
         nu.child[nc.tok[0]] = c;
         nc.parent = u;
+        refresh_best(u);  // u inherits c's value; the parent's is unchanged
         return u;
     }
 
+    // Detach x's ring row (the caller refreshes `best` from x or its parent).
     void detach_ring(int32_t x)
     {
         Node &nx = nodes[x];
@@ -200,8 +216,10 @@ hsa_status hsa_ptree_match(hsa_ptree *t, const int32_t *tokens, int32_t n, int32
         *ring_row = nx.ring;
         std::memcpy(swa_slot_pos, nx.ring_pos.data(), sizeof(int32_t) * (size_t)t->W);
         nx.ring_use = ++t->clock;
-        if (take_ring)
+        if (take_ring) {
             t->detach_ring(x);
+            t->refresh_best(x);
+        }
     } else {
         *ring_row = -1;
         for (int32_t s = 0; s < t->W; ++s)
@@ -227,7 +245,7 @@ hsa_status hsa_ptree_match_batch(hsa_ptree *t, const int32_t *tokens, const int6
         return HSA_INVALID_ARG;
     for (int32_t k = 0; k < n; ++k) {
         const int64_t len = tok_off[k + 1] - tok_off[k];
-        if (len < 0 || (len > 0 && !tokens))
+        if (tok_off[k] < 0 || len < 0 || (len > 0 && !tokens))
             return HSA_INVALID_ARG;
     }
     for (int32_t k = 0; k < n; ++k) {
@@ -302,6 +320,7 @@ hsa_status hsa_ptree_insert(hsa_ptree *t, const int32_t *tokens, const int32_t *
         t->row_held[ring_row] = 1;
         ++t->rows_held;
         *ring_kept = 1;
+        t->refresh_best(cur);
     }
     return HSA_OK;
 }
@@ -328,21 +347,24 @@ hsa_status hsa_ptree_evict_full(hsa_ptree *t, int32_t n_tokens, int32_t *freed_s
         return HSA_INVALID_ARG;
     *n_slots = 0;
     *n_rows = 0;
-    while (*n_slots < n_tokens) {
-        int32_t victim = -1;
+    // Evictable leaves, least recently used first (ties: smaller id).  Evicting a
+    // leaf changes no other node's stamp or lock, so the keys stay valid; a parent
+    // left without children joins the heap.
+    typedef std::pair<uint64_t, int32_t> Key;
+    std::priority_queue<Key, std::vector<Key>, std::greater<Key>> heap;
+    if (n_tokens > 0)
         for (int32_t x = 1; x < (int32_t)t->nodes.size(); ++x) {
             const Node &nx = t->nodes[x];
-            if (!nx.alive || nx.lock > 0 || !nx.child.empty())
-                continue;
-            if (victim < 0 || nx.last_use < t->nodes[victim].last_use)
-                victim = x;
+            if (nx.alive && nx.lock <= 0 && nx.child.empty())
+                heap.push(Key(nx.last_use, x));
         }
-        if (victim < 0)
-            break;
+    while (*n_slots < n_tokens && !heap.empty()) {
+        const int32_t victim = heap.top().second;
+        heap.pop();
         Node &nv = t->nodes[victim];
         const int32_t need_rows = nv.ring >= 0 ? 1 : 0;
         if (*n_slots + (int32_t)nv.slot.size() > slot_cap || *n_rows + need_rows > row_cap)
-            break;
+            return *n_slots == 0 && *n_rows == 0 ? HSA_OUT_OF_RANGE : HSA_OK;
         std::memcpy(freed_slots + *n_slots, nv.slot.data(), sizeof(int32_t) * nv.slot.size());
         *n_slots += (int32_t)nv.slot.size();
         if (need_rows) {
@@ -350,9 +372,14 @@ hsa_status hsa_ptree_evict_full(hsa_ptree *t, int32_t n_tokens, int32_t *freed_s
             t->detach_ring(victim);
         }
         t->cached -= (int64_t)nv.slot.size();
-        t->nodes[nv.parent].child.erase(nv.tok[0]);
+        const int32_t parent = nv.parent;
+        t->nodes[parent].child.erase(nv.tok[0]);
         nv = Node();
         t->free_ids.push_back(victim);
+        t->refresh_best(parent);
+        const Node &np = t->nodes[parent];
+        if (parent > 0 && np.lock <= 0 && np.child.empty())
+            heap.push(Key(np.last_use, parent));
     }
     return HSA_OK;
 }
@@ -363,21 +390,26 @@ hsa_status hsa_ptree_evict_swa(hsa_ptree *t, int32_t n_rows, int32_t *freed_rows
     if (!t || n_rows < 0 || !n_freed || (n_rows > 0 && !freed_rows))
         return HSA_INVALID_ARG;
     *n_freed = 0;
-    while (*n_freed < n_rows) {
-        int32_t victim = -1;
-        for (int32_t x = 1; x < (int32_t)t->nodes.size(); ++x) {
-            const Node &nx = t->nodes[x];
-            if (!nx.alive || nx.lock > 0 || nx.ring < 0)
-                continue;
-            const Node *nb = victim >= 0 ? &t->nodes[victim] : nullptr;
-            if (!nb || nx.ring_use < nb->ring_use ||
-                (nx.ring_use == nb->ring_use && nx.ring < nb->ring))
-                victim = x;
+    if (n_rows == 0)
+        return HSA_OK;
+    // Rows of unlocked nodes, least recently used first (ties: smaller row id);
+    // detaching one changes no other row's stamp.
+    std::vector<std::pair<uint64_t, int32_t>> cand;  // (ring_use, ring row) ...
+    std::vector<int32_t> holder(t->row_held.size(), -1);
+    for (int32_t x = 1; x < (int32_t)t->nodes.size(); ++x) {
+        const Node &nx = t->nodes[x];
+        if (nx.alive && nx.lock <= 0 && nx.ring >= 0) {
+            cand.push_back(std::make_pair(nx.ring_use, nx.ring));
+            holder[nx.ring] = x;
         }
-        if (victim < 0)
-            break;
-        freed_rows[(*n_freed)++] = t->nodes[victim].ring;
-        t->detach_ring(victim);
+    }
+    const size_t take = std::min(cand.size(), (size_t)n_rows);
+    std::partial_sort(cand.begin(), cand.begin() + take, cand.end());
+    for (size_t i = 0; i < take; ++i) {
+        const int32_t x = holder[cand[i].second];
+        freed_rows[(*n_freed)++] = cand[i].second;
+        t->detach_ring(x);
+        t->refresh_best(x);
     }
     return HSA_OK;
 }

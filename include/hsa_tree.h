@@ -32,9 +32,13 @@
  * Ownership: the tree is host memory owned by the library between create and
  * destroy; every buffer passed in is caller-owned host memory, read or written
  * only during the call.  The tree is not thread-safe: one caller at a time.
- * Errors: HSA_INVALID_ARG for a null handle or pointer, a negative length, or a
- * ring row outside [0, n_ring_rows); HSA_OUT_OF_RANGE when a caller buffer is too
- * small (the call then changes nothing).
+ * Errors: HSA_INVALID_ARG for a null handle or pointer, a negative length or
+ * offset, or a ring row outside [0, n_ring_rows); HSA_OUT_OF_RANGE from
+ * hsa_ptree_evict_full when the first leaf to evict does not fit the caller's
+ * buffers (the call then changes nothing).  Output arrays sized by the stated
+ * rule ("room for n") are the caller's contract and are not checked.
+ * Cost: match O(matched tokens) plus O(1) for the ring choice; insert O(len);
+ * the evictions O(nodes + victims * log nodes).
  */
 #ifndef HSA_TREE_H
 #define HSA_TREE_H
@@ -95,13 +99,15 @@ hsa_status hsa_ptree_unlock(hsa_ptree *t, int64_t lock_handle);
  * Evict least-recently-used unlocked leaves until at least n_tokens Full slots
  * are freed or none is evictable.  Freed slots go to freed_slots (room for
  * slot_cap), freed ring rows to freed_rows (room for row_cap); the call stops
- * before a leaf whose slots or row would not fit.
+ * before a leaf whose slots or row would not fit (HSA_OUT_OF_RANGE if that is the
+ * first leaf).  Ties in last use go to the smaller node id.
  */
 hsa_status hsa_ptree_evict_full(hsa_ptree *t, int32_t n_tokens, int32_t *freed_slots,
                                 int32_t slot_cap, int32_t *n_slots, int32_t *freed_rows,
                                 int32_t row_cap, int32_t *n_rows);
 
-/* Detach up to n_rows least-recently-used ring rows of unlocked nodes. */
+/* Detach up to n_rows least-recently-used ring rows of unlocked nodes (last use:
+ * attach or last selection by a match; ties go to the smaller row id). */
 hsa_status hsa_ptree_evict_swa(hsa_ptree *t, int32_t n_rows, int32_t *freed_rows,
                                int32_t *n_freed);
 

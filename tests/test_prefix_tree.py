@@ -207,3 +207,87 @@ def test_invalid_arguments():
         tree.unlock(h)  # already released
     L = hsa.lib()
     assert L.hsa_ptree_create(0, 4, None) == hsa.HSA_INVALID_ARG
+
+
+@pytest.mark.parametrize("seed", [21, 22, 23, 24])
+def test_interleaved_operations_match_model(seed):
+    """Inserts, locked matches, unlocks, ring hand-overs and both evictions in a
+    random interleaving; after every few operations each probe's match (length,
+    ring row, slot positions, Full slots) equals the model's, and every locked path
+    is still cached with the slots it had when it was locked."""
+    tree, model, wl = _tree(), PrefixModel(W), Workload(seed)
+    rng = wl.rng
+    held = []  # (handle, tokens, m, slots) of live locks
+    for step in range(300):
+        u = rng.random()
+        if u < 0.45 or not wl.paths:
+            _finish(tree, model, wl, wl.request(), reuse=rng.random() < 0.7)
+        elif u < 0.6:
+            toks = list(rng.choice(wl.paths))[:rng.randint(1, 3 * W)]
+            m, slots, _, _, h = tree.match(toks, lock=True)
+            if h > 0:
+                held.append((h, toks, m, [int(x) for x in slots]))
+        elif u < 0.7 and held:
+            h, _, _, _ = held.pop(rng.randrange(len(held)))
+            tree.unlock(h)
+        elif u < 0.8:
+            toks = rng.choice(wl.paths)
+            _, _, row, _, _ = tree.match(toks, take_ring=True)
+            if row >= 0:
+                model.take_ring(row)
+                wl.free_rows.append(row)
+        elif u < 0.92:
+            freed, rows = tree.evict_full(rng.randint(1, 4 * W))
+            model.drop_slots(freed)
+            model.drop_rows(rows)
+            wl.free_rows.extend(int(r) for r in rows)
+        else:
+            rows = tree.evict_swa(rng.randint(1, 4))
+            model.drop_rows(rows)
+            wl.free_rows.extend(int(r) for r in rows)
+        if step % 5 == 4:
+            probes = [wl.request() for _ in range(12)] + wl.paths[-4:] + [[]]
+            _same_match(tree, model, probes)
+            c, rows_held, _ = tree.stats()
+            assert c == model.cached_tokens()
+            assert rows_held == len(model.rows_held())
+            for _, toks, m0, slots0 in held:
+                m, slots, _, _, _ = tree.match(toks)
+                assert m >= m0 and [int(x) for x in slots[:m0]] == slots0
+    for h, _, _, _ in held:
+        tree.unlock(h)
+    freed, rows = tree.evict_full(1 << 30)
+    assert tree.stats()[:2] == (0, 0)
+
+
+def test_evict_full_reports_a_buffer_too_small():
+    import full_attention_kv_gb300 as hsa
+    tree = _tree()
+    tree.insert([7], [20])                   # least recently used
+    tree.insert([1, 2, 3, 4], [10, 11, 12, 13])
+    freed, _ = tree.evict_full(10, slot_cap=3)  # [7] fits, then the four-slot leaf does not
+    assert [int(x) for x in freed] == [20] and tree.stats()[0] == 4
+    with pytest.raises(hsa.HsaError) as e:
+        tree.evict_full(1, slot_cap=3)       # the first leaf already does not fit
+    assert e.value.status == hsa.HSA_OUT_OF_RANGE
+    assert tree.stats()[0] == 4              # nothing changed
+
+
+def test_ring_choice_scales_with_shared_prefixes():
+    """Thousands of cached paths below one shared system prompt: a batch of
+    requests matching up to the shared end each gets the preferred row (shortest
+    path, then latest attached) without walking the subtree."""
+    W_ = 128
+    tree = _tree(W=W_, rows=4096)
+    system = list(range(1000, 1000 + 2 * W_))
+    for i in range(3000):
+        toks = system + [i % 50, i] + [7] * (i % 5)
+        tree.insert(toks, list(range(len(toks))), i, ring_positions(len(toks), W_))
+    reqs = [system + [99999, k] for k in range(2000)]
+    m, rows, pos = tree.match_batch(reqs)
+    # shortest cached paths through the prompt end have 2 extra tokens (i % 5 == 0);
+    # among them the latest attached row wins
+    want = max(i for i in range(3000) if i % 5 == 0)
+    assert all(int(x) == len(system) for x in m)
+    assert all(int(r) == want for r in rows)
+    assert list(pos[0]) == ring_positions(len(system) + 2, W_)
