@@ -159,6 +159,18 @@ def decode_bytes(inst, layer_full, fp8=False):
     return int(keys.sum()) * per_tok + qo
 
 
+def pool_ratio(inst):
+    """Bytes the dual pool allocates for this workload (bf16 layout: pages of the
+    full layers, one W-slot ring row per sequence for each sliding layer) over the
+    bytes an all-full stack would allocate for the same pages."""
+    cfg = inst.cfg
+    row = cfg.Hkv * cfg.d * 2 * 2          # K and V of one position, bf16
+    full = inst.num_blocks * cfg.page * row
+    ring = inst.n_ring_rows * cfg.W * row
+    n_full = sum(1 for f in inst.full if f)
+    return (n_full * full + (len(inst.full) - n_full) * ring) / (len(inst.full) * full)
+
+
 def keys_per_row(inst, layer_full):
     """Keys each new row attends (int64 [rows])."""
     cfg = inst.cfg
@@ -631,6 +643,7 @@ def run_ours(args, inst, ws, rank, local):
                    "context_total_tokens": int(inst.prefix.sum()),
                    "parallelism": "replicas x%d" % ws,
                    "l2": "inputs larger than L2 (KV pools %.1f GB)" % (_pool_bytes(step.pool) / 1e9),
+                   "kv_pool_vs_all_full": pool_ratio(inst),
                    "graph": "one CUDA graph per step (%d launches)" % step.launches_per_step},
         "roofline": roof,
         "clocks": clocks,

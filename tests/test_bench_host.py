@@ -62,3 +62,21 @@ def test_code_digest_ignores_comments_only(tmp_path):
     c.write_text("__global__ void k(int *p) {\n  p[0] = 2;\n}\n")
     assert bench.code_digest(a) == bench.code_digest(b)
     assert bench.code_digest(a) != bench.code_digest(c)
+
+
+def test_pool_allocation_realises_the_kv_byte_ratio():
+    """The dual pool's allocation for a drawn workload over an all-full stack's
+    equals the pages' KV-byte ratio (oracle.kv_bytes, pinned to "about 1/7") summed
+    over the sequences, up to the rounding of each sequence to whole 64-token pages."""
+    import oracle
+    for name in ("decode", "long", "mtp"):
+        inst = workload.draw(workload.CONFIGS[name])
+        cfg = inst.cfg
+        per_tok = 2 * cfg.Hkv * cfg.d * 2
+        lens = [int(L) for L in inst.prefix + inst.new]
+        hyb = sum(oracle.kv_bytes(inst.full, cfg.W, L, per_tok) for L in lens)
+        full = sum(oracle.kv_bytes([1] * cfg.n_layers, cfg.W, L, per_tok) for L in lens)
+        got = bench.pool_ratio(inst)
+        assert abs(got - hyb / full) / (hyb / full) < 0.02, (name, got, hyb / full)
+    inst = workload.draw(workload.CONFIGS["decode"])
+    assert 1 / 7 < bench.pool_ratio(inst) < 0.16
