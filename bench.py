@@ -64,15 +64,17 @@ class ClockSampler:
         self.dev = device_index
         self.proc = None
         self.path = None
+        self.out = None
 
     def __enter__(self):
         fd, self.path = tempfile.mkstemp(suffix=".csv")
         os.close(fd)
+        self.out = open(self.path, "w")
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.dev), "--query-gpu=" + self.FIELDS,
                  "--format=csv,noheader,nounits", "-lms", "200"],
-                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+                stdout=self.out, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
         time.sleep(0.3)
@@ -85,9 +87,13 @@ class ClockSampler:
                 self.proc.wait(timeout=5)
             except Exception:
                 self.proc.kill()
+        if self.out is not None:
+            self.out.close()
 
     def summary(self):
         if self.proc is None or not self.path:
+            if self.path and os.path.exists(self.path):
+                os.unlink(self.path)
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         rows = []
         with open(self.path) as f:
