@@ -537,3 +537,13 @@ def test_prefix_model_hand_cases():
     # dropping the Full slots of a suffix shortens later matches
     m.drop_slots([14, 15])
     assert m.match([1, 2, 3, 4, 5, 6])[0] == 4
+    # equal path lengths through the match point: the latest attached row wins,
+    # whatever its id (the most recent request's window is the freshest)
+    m2 = PrefixModel(W=4)
+    m2.insert([1, 2, 3, 4], [10, 11, 12, 13], 5, ring_positions(4, 4))
+    m2.insert([1, 2, 3, 6], [10, 11, 12, 16], 9, ring_positions(4, 4))
+    assert m2.match([1, 2, 3, 7])[2] == 9
+    m2.insert([1, 2, 3, 8], [10, 11, 12, 18], 2, ring_positions(4, 4))
+    assert m2.match([1, 2, 3, 7])[2] == 2
+    m2.take_ring(2)
+    assert m2.match([1, 2, 3, 7])[2] == 9
