@@ -4,6 +4,8 @@ import ctypes
 import os
 import re
 
+import pytest
+
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
@@ -92,3 +94,107 @@ def test_decode_rejects_more_than_four_new_tokens():
                                  None, 0, 0, None, None) == hsa.HSA_UNSUPPORTED_SHAPE
     assert L.hsa_decode_attn(ctypes.byref(pools), 0, None, None, None, None, 1, 0, 1.0, None,
                              None, 0, 0, None, None) == hsa.HSA_INVALID_ARG
+
+
+def _pools(hsa, **kw):
+    """A host struct that passes every host check unless `kw` breaks one.  Pointer
+    values are never dereferenced by the checks (no CUDA call is reached)."""
+    n = kw.pop("n_layers", 2)
+    full = (ctypes.c_uint8 * n)(*kw.pop("full", [0, 1]))
+    fp8 = kw.pop("fp8", None)
+    fp8a = (ctypes.c_uint8 * n)(*fp8) if fp8 is not None else None
+    ptr = kw.pop("ptr", 256)
+    kv = (ctypes.c_void_p * n)(*([ptr] * n))
+    args = dict(n_layers=n, layer_is_full=ctypes.cast(full, ctypes.POINTER(ctypes.c_uint8)),
+                k=ctypes.cast(kv, ctypes.POINTER(ctypes.c_void_p)),
+                v=ctypes.cast(kv, ctypes.POINTER(ctypes.c_void_p)), num_blocks=8, page_size=64,
+                block_tables=256, max_blocks=4, ring_row=256, n_ring_rows=2, batch=2, W=128,
+                Hq=32, Hkv=4, d=128,
+                layer_kv_fp8=ctypes.cast(fp8a, ctypes.POINTER(ctypes.c_uint8)) if fp8a else None)
+    args.update(kw)
+    p = hsa.HsaPools(**args)
+    p._keep = (full, kv, fp8a)
+    return p
+
+
+_BAD_POOLS = [
+    # (change, layer, expected status name)
+    (dict(d=64), 1, "HSA_UNSUPPORTED_SHAPE"),
+    (dict(page_size=32), 1, "HSA_UNSUPPORTED_SHAPE"),
+    (dict(W=96), 0, "HSA_UNSUPPORTED_SHAPE"),
+    (dict(W=320), 0, "HSA_UNSUPPORTED_SHAPE"),
+    (dict(Hq=24), 1, "HSA_UNSUPPORTED_SHAPE"),      # group of 6
+    (dict(Hq=30), 1, "HSA_UNSUPPORTED_SHAPE"),      # Hq not a multiple of Hkv
+    (dict(Hq=64), 1, "HSA_UNSUPPORTED_SHAPE"),      # group of 16
+    (dict(Hkv=0), 1, "HSA_UNSUPPORTED_SHAPE"),
+    (dict(batch=-1), 1, "HSA_INVALID_ARG"),
+    (dict(ptr=264), 1, "HSA_INVALID_ARG"),          # pool not 16-byte aligned
+    (dict(ptr=0), 1, "HSA_INVALID_ARG"),
+    (dict(block_tables=None), 1, "HSA_INVALID_ARG"),  # full layer without block tables
+    (dict(num_blocks=0), 1, "HSA_INVALID_ARG"),
+    (dict(ring_row=None), 0, "HSA_INVALID_ARG"),    # sliding layer without ring rows
+    (dict(n_ring_rows=0), 0, "HSA_INVALID_ARG"),
+    (dict(fp8=[1, 0]), 0, "HSA_UNSUPPORTED_SHAPE"),  # a sliding layer flagged FP8
+    (dict(), 2, "HSA_INVALID_ARG"),                 # layer index past n_layers
+    (dict(), -1, "HSA_INVALID_ARG"),
+]
+
+
+@pytest.mark.parametrize("change,layer,status", _BAD_POOLS)
+def test_pool_checks_refuse_on_the_host(change, layer, status):
+    """Every entry point taking the pools refuses a malformed struct with the
+    documented status and launches nothing (this runs without a GPU)."""
+    import full_attention_kv_gb300 as hsa
+    L = hsa.lib()
+    want = getattr(hsa, status)
+    p = ctypes.byref(_pools(hsa, **change))
+    assert L.hsa_kv_append(p, layer, 256, 256, 256, 256, 256, 1, 1, None, None) == want
+    assert L.hsa_decode_attn(p, layer, 256, 256, 256, 256, 1, 1, 0.1, 256, 256, 1 << 20, 0,
+                             None, None) == want
+    assert L.hsa_decode_attn_append(p, layer, 256, 256, 256, 256, 1, 1, 0.1, 256, 256, 1 << 20,
+                                    0, None, None) == want
+    if change.get("fp8") is None:
+        assert L.hsa_prefill_attn(p, layer, 256, 256, 256, 256, 256, 256, 1, 1, 1, 0.1, 256,
+                                  None, None) == want
+
+
+def test_call_argument_checks_refuse_on_the_host():
+    import full_attention_kv_gb300 as hsa
+    L = hsa.lib()
+    p = ctypes.byref(_pools(hsa))
+    INV, UNS, OK = hsa.HSA_INVALID_ARG, hsa.HSA_UNSUPPORTED_SHAPE, hsa.HSA_OK
+    # append: negative sizes, null or unaligned rows; nothing to do is OK
+    assert L.hsa_kv_append(p, 1, 256, 256, 256, 256, 256, -1, 1, None, None) == INV
+    assert L.hsa_kv_append(p, 1, 256, 256, 256, 256, 256, 1, -1, None, None) == INV
+    assert L.hsa_kv_append(p, 1, None, 256, 256, 256, 256, 1, 1, None, None) == INV
+    assert L.hsa_kv_append(p, 1, 264, 256, 256, 256, 256, 1, 1, None, None) == INV
+    assert L.hsa_kv_append(p, 1, None, None, None, None, None, 0, 0, None, None) == OK
+    # decode: T out of range, B past the pool's batch, null / unaligned buffers, B = 0 is OK
+    dec = L.hsa_decode_attn
+    assert dec(p, 1, 256, 256, 256, 256, 1, 0, 0.1, 256, 256, 1 << 20, 0, None, None) == INV
+    assert dec(p, 1, 256, 256, 256, 256, 1, 5, 0.1, 256, 256, 1 << 20, 0, None, None) == UNS
+    assert dec(p, 1, 256, 256, 256, 256, 3, 1, 0.1, 256, 256, 1 << 20, 0, None, None) == INV
+    assert dec(p, 1, 256, 256, 256, 256, 1, 1, 0.1, 256, 256, 1 << 20, -1, None, None) == INV
+    assert dec(p, 1, 264, 256, 256, 256, 1, 1, 0.1, 256, 256, 1 << 20, 0, None, None) == INV
+    assert dec(p, 1, 256, 256, 256, None, 1, 1, 0.1, 256, 256, 1 << 20, 0, None, None) == INV
+    assert dec(p, 1, None, None, None, None, 0, 1, 0.1, None, None, 0, 0, None, None) == OK
+    # prefill: negative sizes, null buffers; an empty call is OK; FP8 layers refused
+    pre = L.hsa_prefill_attn
+    assert pre(p, 1, 256, 256, 256, 256, 256, 256, -1, 1, 1, 0.1, 256, None, None) == INV
+    assert pre(p, 1, 256, 256, 256, 256, 256, 256, 1, 1, -1, 0.1, 256, None, None) == INV
+    assert pre(p, 1, 256, 256, 256, None, 256, 256, 1, 1, 1, 0.1, 256, None, None) == INV
+    assert pre(p, 1, None, None, None, None, None, None, 0, 0, 0, 0.1, None, None, None) == OK
+    p8 = ctypes.byref(_pools(hsa, fp8=[0, 1]))
+    assert pre(p8, 1, 256, 256, 256, 256, 256, 256, 1, 1, 1, 0.1, 256, None, None) == UNS
+    # prefetch: full layers have no ring; negative counts; n = 0 is OK
+    pf = L.hsa_swa_prefetch
+    assert pf(p, 1, 256, 256, 1, 256, 256, 1, None, None) == INV
+    assert pf(p, 0, 256, 256, 1, 256, 256, -1, None, None) == INV
+    assert pf(p, 0, None, None, 0, None, None, 0, None, None) == OK
+    # window-safe: bad W or n, null buffers
+    assert L.hsa_window_safe_len(256, 256, 1, 0, 256, None) == INV
+    assert L.hsa_window_safe_len(None, 256, 1, 128, 256, None) == INV
+    assert L.hsa_window_safe_len_bitmap(256, 256, 256, -1, 128, 256, None) == INV
+    assert L.hsa_window_safe_len_bitmap(256, None, 256, 1, 128, 256, None) == INV
+    assert L.hsa_decode_workspace_bytes(None, 1, 1) == 0
+    assert L.hsa_decode_workspace_bytes(p, -1, 1) == 0
