@@ -206,13 +206,13 @@ size_t hsa_decode_workspace_bytes(const hsa_pools *pools, int32_t B, int32_t T)
 
 }  // extern "C"
 
-namespace {
+namespace hsa {
 
-hsa_status decode_common(const hsa_pools *pools, int32_t layer, const void *q, const void *k_new,
-                         const void *v_new, const int32_t *cached_len, int32_t B, int32_t T,
-                         float scale, void *out, void *workspace, size_t ws_bytes,
-                         int32_t max_ctas, int32_t *dev_err, void *stream, int append)
+hsa_status decode_host_check(const hsa_pools *pools, int32_t layer, const void *q,
+                             const void *k_new, const void *v_new, const int32_t *cached_len,
+                             int32_t B, int32_t T, const void *out, int32_t max_ctas, bool *done)
 {
+    *done = false;
     hsa_status st = check_pools(pools, layer);
     if (st != HSA_OK)
         return st;
@@ -223,11 +223,31 @@ hsa_status decode_common(const hsa_pools *pools, int32_t layer, const void *q, c
         return HSA_UNSUPPORTED_SHAPE;
     if (B > pools->batch)
         return HSA_INVALID_ARG;
-    if (B == 0)
+    if (B == 0) {
+        *done = true;
         return HSA_OK;
+    }
     if (!q || !k_new || !v_new || !cached_len || !out || !aligned16(q) || !aligned16(k_new) ||
         !aligned16(v_new) || !aligned16(out))
         return HSA_INVALID_ARG;
+    return HSA_OK;
+}
+
+}  // namespace hsa
+
+namespace {
+
+hsa_status decode_common(const hsa_pools *pools, int32_t layer, const void *q, const void *k_new,
+                         const void *v_new, const int32_t *cached_len, int32_t B, int32_t T,
+                         float scale, void *out, void *workspace, size_t ws_bytes,
+                         int32_t max_ctas, int32_t *dev_err, void *stream, int append)
+{
+    bool done = false;
+    const hsa_status st = hsa::decode_host_check(pools, layer, q, k_new, v_new, cached_len, B, T,
+                                                 out, max_ctas, &done);
+    if (st != HSA_OK || done)
+        return st;
+    const int G = pools->Hq / pools->Hkv;
     const bool full = pools->layer_is_full[layer] != 0;
     const int sms = device_sms();
     if (sms <= 0)

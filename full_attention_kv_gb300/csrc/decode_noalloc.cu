@@ -58,11 +58,12 @@ extern "C" hsa_status hsa_decode_attn_noalloc(const hsa_pools *pools, int32_t la
                                               int32_t B, int32_t T, float scale, void *out,
                                               int32_t max_ctas, int32_t *dev_err, void *stream)
 {
-    if (!pools || pools->Hkv <= 0 || B < 0 || max_ctas < 0)
-        return HSA_INVALID_ARG;
-    if (B == 0)
-        return hsa_decode_attn(pools, layer, q, k_new, v_new, cached_len, B, T, scale, out,
-                               nullptr, 0, max_ctas, dev_err, stream);
+    // every host check first: a refused call must launch nothing (not even the memset)
+    bool done = false;
+    const hsa_status st = hsa::decode_host_check(pools, layer, q, k_new, v_new, cached_len, B, T,
+                                                 out, max_ctas, &done);
+    if (st != HSA_OK || done)
+        return st;
     // CTA cap so that the counters and every CTA's partial slots fit the array
     if ((int64_t)B * pools->Hkv > 4096)
         return HSA_UNSUPPORTED_SHAPE;  // more units than the fixed scratch is sized for

@@ -46,6 +46,11 @@ __host__ __device__ inline size_t decode_counter_bytes(int B, int Hkv)
 }
 
 size_t decode_workspace_bytes(int num_sms, int B, int Hkv);
+// Every host-side check of a decode call except the workspace's (api.cu); HSA_OK
+// with *done = true means there is nothing to do (B = 0).
+hsa_status decode_host_check(const hsa_pools *pools, int32_t layer, const void *q,
+                             const void *k_new, const void *v_new, const int32_t *cached_len,
+                             int32_t B, int32_t T, const void *out, int32_t max_ctas, bool *done);
 cudaError_t launch_decode(const CUtensorMap &tmK, const CUtensorMap &tmV, const DecodeParams &p,
                           int ctas, cudaStream_t stream);
 

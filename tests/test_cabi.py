@@ -198,3 +198,22 @@ def test_call_argument_checks_refuse_on_the_host():
     assert L.hsa_window_safe_len_bitmap(256, None, 256, 1, 128, 256, None) == INV
     assert L.hsa_decode_workspace_bytes(None, 1, 1) == 0
     assert L.hsa_decode_workspace_bytes(p, -1, 1) == 0
+
+
+def test_noalloc_refuses_before_touching_its_scratch():
+    """The no-workspace decode applies every host check before it queues anything
+    (its scratch reset included): without a GPU a malformed call still gets the
+    argument error, not a CUDA error from the scratch lookup."""
+    import full_attention_kv_gb300 as hsa
+    L = hsa.lib()
+    p = ctypes.byref(_pools(hsa))
+    na = L.hsa_decode_attn_noalloc
+    assert na(p, 5, 256, 256, 256, 256, 1, 1, 0.1, 256, 0, None, None) == hsa.HSA_INVALID_ARG
+    assert na(p, 1, 256, 256, 256, 256, 1, 5, 0.1, 256, 0, None, None) == \
+        hsa.HSA_UNSUPPORTED_SHAPE
+    assert na(p, 1, 256, 256, 256, None, 1, 1, 0.1, 256, 0, None, None) == hsa.HSA_INVALID_ARG
+    assert na(p, 1, 256, 256, 256, 256, 3, 1, 0.1, 256, 0, None, None) == hsa.HSA_INVALID_ARG
+    assert na(p, 1, None, None, None, None, 0, 1, 0.1, None, 0, None, None) == hsa.HSA_OK
+    bad = ctypes.byref(_pools(hsa, W=96))
+    assert na(bad, 0, 256, 256, 256, 256, 1, 1, 0.1, 256, 0, None, None) == \
+        hsa.HSA_UNSUPPORTED_SHAPE
