@@ -177,11 +177,7 @@ struct RowState {
 // 64-register rescale of O.
 constexpr float kRescaleSlack = 8.0f;
 
-// One key tile on tensor cores.  NT = n-tiles of 8 keys this warp owns inside the
-// tile (keys key0 .. key0 + 8 NT - 1), rows = the tile's row count in shared
-// memory (for the swizzle), vis(row, key) = key visible to that query row; when
-// all_vis is set every key of the tile is visible to every valid row and only rows
-// past G T (padding) are masked.
+// m16n8k16 MMA and operand packing in bf16, or fp16 when F16 is set.
 template <bool F16>
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                          uint32_t b1)
@@ -198,6 +194,11 @@ __device__ __forceinline__ uint32_t pack16(float lo, float hi)
     return F16 ? pack_f16(lo, hi) : pack_bf16(lo, hi);
 }
 
+// One key tile on tensor cores.  NT = n-tiles of 8 keys this warp owns inside the
+// tile (keys key0 .. key0 + 8 NT - 1), rows = the tile's row count in shared
+// memory (for the swizzle), vis(row, key) = key visible to that query row; when
+// all_vis is set every key of the tile is visible to every valid row and only rows
+// past G T (padding) are masked.
 // F16: the operands (Q fragments and the tile in shared memory) are fp16 instead
 // of bf16 (the FP8 kernel's new-token tile).
 template <int NT, bool F16 = false, typename Vis>
@@ -550,8 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) {
             mbar_init(&sh.full[s], 1);
-            // full layers: the MT warps of the owning group; rings: every consumer warp
-            // the warps of the stage's owning group: MT (full layers), 2 (rings)
+            // released by the warps of the stage's owning group: MT (full layers), 2 (rings)
             mbar_init(&sh.empty[s], (p.flags & kDecodeRing) ? 2 : MT);
         }
         fence_barrier_init();
