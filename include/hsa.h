@@ -30,9 +30,10 @@
  *    appending first would overwrite ring slots the earlier queries still need.
  *  - Query head h uses KV head h / (Hq / Hkv).  A sliding-window query at
  *    position p attends positions max(0, p-W+1) .. p (W keys including itself).
- *  - One device per process: the kernels' shared-memory opt-in is set on the
- *    device current at a kernel's first call.  A process that drives several GPUs
- *    gets HSA_CUDA_ERROR from the first call on another device (nothing runs).
+ *  - One device per process: the kernels' shared-memory opt-in is set once, on the
+ *    device current at a kernel's first call.  In a process that drives several
+ *    GPUs a call on another device may be refused with HSA_CUDA_ERROR (the launch
+ *    fails; nothing runs).
  */
 #ifndef HSA_H
 #define HSA_H
