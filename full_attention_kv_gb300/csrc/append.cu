@@ -10,6 +10,9 @@
 // For the ring only a request's last W tokens are written, so every slot is
 // written once per call (deterministic, race-free) and the result equals
 // appending the tokens one by one in position order.
+// An FP8 full layer (fp8_kv.cuh) is written by append_fp8_kernel instead: one warp
+// per (token, KV head, K or V) row quantises the row to E4M3 codes plus one fp32
+// scale (amax / 448, found by a warp reduction) and stores them in the page layout.
 #include "fp8_kv.cuh"
 #include "hsa_device.cuh"
 #include "hsa_internal.h"
