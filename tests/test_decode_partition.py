@@ -48,3 +48,39 @@ def test_partition_extremes():
     _check([16384] * 16, 152)   # 4 sequences x 4 KV heads at 1M tokens, one CTA per SM
     _check([1] * 2000, 152)     # more units than CTAs, one tile each
     _check([3], 152)            # fewer items than CTAs: the grid shrinks to N
+
+
+def _prefill_grid_pairs(rows, R, max_chunk):
+    """Tile-pair count the prefill launch sizes its grid for (api.cu, prefill.cu)."""
+    b1 = rows // 128 + R
+    b2 = R * ((max_chunk + 127) // 128)
+    tiles = min(b1, b2)
+    return (tiles + R + 1) // 2
+
+
+def test_prefill_grid_covers_every_tile_pair_once():
+    """prefill.cu maps CTA x (per query head) to the x-th (request, 256-row pair)
+    in request order; the grid bound computed on the host from rows, R and
+    max_chunk must cover every pair, and CTAs past the last pair map to none."""
+    rng = random.Random(11)
+    for _ in range(3000):
+        R = rng.randint(1, 12)
+        C = [rng.choice([0, 1, 127, 128, 129, 255, 256, 257, rng.randint(0, 9000)])
+             for _ in range(R)]
+        rows = sum(C)
+        if rows == 0:
+            continue
+        grid = _prefill_grid_pairs(rows, R, max(C))
+        seen = []
+        for tl in range(grid):
+            acc, found = 0, None
+            for r, c in enumerate(C):
+                n_pairs = (c + 255) // 256
+                if tl < acc + n_pairs:
+                    found = (r, tl - acc)
+                    break
+                acc += n_pairs
+            if found is not None:
+                seen.append(found)
+        want = [(r, q) for r, c in enumerate(C) for q in range((c + 255) // 256)]
+        assert seen == want
