@@ -1,6 +1,7 @@
-"""Index arithmetic of the decode kernel's stream-K split and in-kernel merge
-(full_attention_kv_gb300/csrc/decode.cu), restated on the host and checked over
-random unit layouts, CTA counts and the 1M-token extreme.
+"""Grid index arithmetic of the kernels, restated on the host and checked over
+random layouts: the decode kernel's stream-K split and in-kernel merge
+(full_attention_kv_gb300/csrc/decode.cu, including the 1M-token extreme) and the
+prefill kernel's CTA-to-tile-pair map and grid bound (csrc/prefill.cu, csrc/api.cu).
 
 Items (64-key tiles) of all units are laid end to end; CTA c takes items
 [c N / C, (c + 1) N / C).  A unit split across CTAs leaves one partial state per
