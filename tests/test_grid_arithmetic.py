@@ -85,3 +85,37 @@ def test_prefill_grid_covers_every_tile_pair_once():
                 seen.append(found)
         want = [(r, q) for r, c in enumerate(C) for q in range((c + 255) // 256)]
         assert seen == want
+
+
+def _ring_after(P, W):
+    """Position each ring slot holds after positions 0 .. P-1 were appended (-1: none)."""
+    held = [-1] * W
+    for p in range(P):
+        held[p % W] = p
+    return held
+
+
+def test_ring_visibility_formulas():
+    """The kernels never build the ring's slot -> position table: decode derives a
+    slot's position as c - 1 - ((c - 1 - s) mod W), prefill as P - 1 - back with
+    back = r0 - s (+ W when s > r0), r0 = (P - 1) mod W, and a row sees the slot
+    iff back <= P - 1 - max(0, P + i - W + 1).  Both must equal the definition:
+    the slot's held position p (if any) lies in the row's window
+    [max(0, q - W + 1), q] of its query position q."""
+    for W in (64, 128, 256):
+        for P in list(range(0, 3 * W + 2, 7)) + [1, W - 1, W, W + 1, 2 * W]:
+            held = _ring_after(P, W)
+            r0 = (P - 1) % W if P > 0 else 0
+            for i in (0, 1, 5, W - 2, W - 1, W, W + 3):
+                q = P + i
+                lim = P - 1 - max(0, q - W + 1)
+                for s in range(W):
+                    want = held[s] >= 0 and held[s] >= max(0, q - W + 1)
+                    # prefill (the ring is read only when P > 0)
+                    if P > 0:
+                        back = r0 - s + (W if s > r0 else 0)
+                        assert (back <= lim) == want, (W, P, i, s)
+                    # decode: query t = i of a T-token step on c = P cached tokens
+                    pos = P - 1 - ((P - 1 - s) % W)
+                    got = pos >= 0 and pos >= q - W + 1
+                    assert got == want, (W, P, i, s)
