@@ -1,7 +1,8 @@
 """Grid index arithmetic of the kernels, restated on the host and checked over
 random layouts: the decode kernel's stream-K split and in-kernel merge
 (full_attention_kv_gb300/csrc/decode.cu, including the 1M-token extreme) and the
-prefill kernel's CTA-to-tile-pair map and grid bound (csrc/prefill.cu, csrc/api.cu).
+prefill kernel's CTA-to-tile-pair map, grid bound and key-tile schedule (csrc/prefill.cu,
+csrc/api.cu), and both kernels' ring-visibility formulas.
 
 Items (64-key tiles) of all units are laid end to end; CTA c takes items
 [c N / C, (c + 1) N / C).  A unit split across CTAs leaves one partial state per
@@ -119,3 +120,41 @@ def test_ring_visibility_formulas():
                     pos = P - 1 - ((P - 1 - s) % W)
                     got = pos >= 0 and pos >= q - W + 1
                     assert got == want, (W, P, i, s)
+
+
+def _sched(P, i0, has_b, W, ring):
+    """prefill.cu make_sched: (prefix or ring tiles, first chunk tile, tile count)."""
+    i_last = i0 + (256 if has_b else 128) - 1
+    if not ring:
+        n_fixed, m_lo = (P + 127) // 128, 0
+    else:
+        n_fixed = (W + 127) // 128 if (P > 0 and i0 < W - 1) else 0
+        lo = i0 - W + 1
+        m_lo = lo // 128 if lo > 0 else 0
+    return n_fixed, m_lo, n_fixed + (i_last // 128 - m_lo + 1)
+
+
+def test_prefill_schedule_covers_every_visible_key():
+    """Each CTA of a request runs its prefix (or ring) tiles and the chunk tiles
+    m_lo .. last row / 128; every key a row of the pair can see must lie in one."""
+    for W in (64, 128, 256):
+        for ring in (False, True):
+            for P in (0, 1, 63, 64, 200, 5000):
+                for C in (1, 100, 128, 129, 256, 257, 700):
+                    for qp in range((C + 255) // 256):
+                        i0 = qp * 256
+                        has_b = i0 + 128 < C
+                        n_fixed, m_lo, nt = _sched(P, i0, has_b, W, ring)
+                        chunk_lo, chunk_hi = m_lo * 128, (m_lo + nt - n_fixed) * 128
+                        for i in range(i0, min(i0 + 256, C)):
+                            q = P + i
+                            first = max(0, q - W + 1) if ring else 0
+                            # prefix keys [first, P) need the prefix / ring tiles
+                            if first < P:
+                                if ring:
+                                    assert n_fixed == (W + 127) // 128
+                                else:
+                                    assert n_fixed * 128 >= P
+                            # chunk rows [max(first - P, 0), i]
+                            lo_row = max(first - P, 0)
+                            assert chunk_lo <= lo_row and i < chunk_hi, (W, ring, P, C, i)
