@@ -35,6 +35,7 @@ import torch
 import workload
 
 METRIC = ("decode attn tokens/s & KV-read GB/s (% HBM peak); prefill attn TFLOP/s (% peak)")
+DATA = "synthetic (seeded bf16 N(0,1), drawn lengths, random page permutation)"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
@@ -640,17 +641,11 @@ def run_ours(args, inst, ws, rank, local):
         "metric": METRIC, "value": value, "unit": unit, "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic (seeded bf16 N(0,1), drawn lengths, random page permutation)",
-        "config": {"workload": "%s: %d-layer 6:1 Hybrid-SWA stack (W=%d), Hq=%d Hkv=%d d=%d, "
-                               "batch %d, T=%d, contexts %s" % (
-                                   cfg.name, cfg.n_layers, cfg.W, cfg.Hq, cfg.Hkv, cfg.d, inst.R,
-                                   cfg.T, _ctx_desc(cfg)),
-                   "global_batch": inst.R * ws, "T": cfg.T,
-                   "context_total_tokens": int(inst.prefix.sum()),
-                   "parallelism": "replicas x%d" % ws,
-                   "l2": "inputs larger than L2 (KV pools %.1f GB)" % (_pool_bytes(step.pool) / 1e9),
-                   "kv_pool_vs_all_full": pool_ratio(inst),
-                   "graph": "one CUDA graph per step (%d launches)" % step.launches_per_step},
+        "data": DATA,
+        "config": dict(
+            workload_config(inst, ws),
+            l2="inputs larger than L2 (KV pools %.1f GB)" % (_pool_bytes(step.pool) / 1e9),
+            graph="one CUDA graph per step (%d launches)" % step.launches_per_step),
         "roofline": roof,
         "clocks": clocks,
         "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": h2d,
@@ -673,6 +668,19 @@ def run_ours(args, inst, ws, rank, local):
         line["cpu_baseline"] = {"value": v, "unit": unit, "cores": cores, "kind": "oracle",
                                 "sample": sample}
     return line
+
+
+def workload_config(inst, ws):
+    """The `config` object both arms report: the workload by what it is, its sizes."""
+    cfg = inst.cfg
+    return {"workload": "%s: %d-layer 6:1 Hybrid-SWA stack (W=%d), Hq=%d Hkv=%d d=%d, "
+                        "batch %d, T=%d, contexts %s" % (
+                            cfg.name, cfg.n_layers, cfg.W, cfg.Hq, cfg.Hkv, cfg.d, inst.R,
+                            cfg.T, _ctx_desc(cfg)),
+            "global_batch": inst.R * ws, "T": cfg.T,
+            "context_total_tokens": int(inst.prefix.sum()),
+            "parallelism": "replicas x%d" % ws,
+            "kv_pool_vs_all_full": pool_ratio(inst)}
 
 
 def _pool_bytes(pool):
@@ -756,8 +764,9 @@ def main():
                 "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "f64",
-                "data": "synthetic (seeded bf16 N(0,1))",
-                "config": {"workload": cfg.name, "global_batch": inst.R},
+                "data": DATA,
+                "config": dict(workload_config(inst, 1),
+                               parallelism="oracle on the host cores (rank 0's workload)"),
                 "cpu_baseline": {"value": v, "unit": unit, "cores": cores, "kind": "oracle",
                                  "sample": sample},
                 "e2e": {"value": v, "unit": unit, "h2d_bytes_per_step": 0,

@@ -80,3 +80,17 @@ def test_pool_allocation_realises_the_kv_byte_ratio():
         assert abs(got - hyb / full) / (hyb / full) < 0.02, (name, got, hyb / full)
     inst = workload.draw(workload.CONFIGS["decode"])
     assert 1 / 7 < bench.pool_ratio(inst) < 0.16
+
+
+def test_workload_config_names_the_workload():
+    """Both arms report this object: JSON-serialisable, the workload named by what
+    it is with its sizes, the whole-job batch over the ranks."""
+    import json
+    for name, cfg in workload.CONFIGS.items():
+        inst = workload.draw(cfg)
+        c = bench.workload_config(inst, 2)
+        json.dumps(c)
+        assert c["workload"].startswith(name + ": 70-layer" if cfg.n_layers == 70 else name)
+        assert c["global_batch"] == 2 * inst.R and c["T"] == cfg.T
+        assert c["parallelism"] == "replicas x2"
+        assert 0 < c["kv_pool_vs_all_full"] <= 1
