@@ -651,6 +651,9 @@ def run_ours(args, inst, ws, rank, local):
         "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": step.launches_per_step * args.steps,
+        "env": {"gpu": torch.cuda.get_device_name(local),
+                "sms": torch.cuda.get_device_properties(local).multi_processor_count,
+                "torch": torch.__version__, "cuda": torch.version.cuda},
     }
     line.update(extra)
     if getattr(args, "kv_fp8", False):
