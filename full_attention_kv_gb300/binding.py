@@ -561,8 +561,13 @@ class PrefixTree:
     def unlock(self, handle):
         _check("hsa_ptree_unlock", lib().hsa_ptree_unlock(self._h, int(handle)))
 
-    def evict_full(self, n_tokens, slot_cap=1 << 20, row_cap=1 << 16):
-        """-> (freed Full slots, freed ring rows)."""
+    def evict_full(self, n_tokens, slot_cap=None, row_cap=None):
+        """-> (freed Full slots, freed ring rows).  The default capacities are what the
+        tree holds, so every evictable leaf fits."""
+        if slot_cap is None or row_cap is None:
+            cached, rows, _ = self.stats()
+            slot_cap = min(max(cached, 1), (1 << 31) - 1) if slot_cap is None else slot_cap
+            row_cap = max(rows, 1) if row_cap is None else row_cap
         fs = torch.empty(max(slot_cap, 1), dtype=torch.int32)
         fr = torch.empty(max(row_cap, 1), dtype=torch.int32)
         ns, nr = ctypes.c_int32(), ctypes.c_int32()

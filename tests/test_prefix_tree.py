@@ -291,3 +291,13 @@ def test_ring_choice_scales_with_shared_prefixes():
     assert all(int(x) == len(system) for x in m)
     assert all(int(r) == want for r in rows)
     assert list(pos[0]) == ring_positions(len(system) + 2, W_)
+
+
+def test_evict_full_default_buffers_fit_any_leaf():
+    """A leaf longer than any fixed buffer (a 1M-token context is one leaf) is
+    evicted by the default call: the binding sizes its buffers from the tree."""
+    tree = _tree()
+    n = (1 << 20) + 5
+    tree.insert(list(range(n)), list(range(n)))
+    freed, rows = tree.evict_full(1)
+    assert len(freed) == n and tree.stats()[0] == 0
