@@ -149,7 +149,8 @@ hsa_status hsa_kv_append(const hsa_pools *pools, int32_t layer, const void *k_ne
  *  merge the partial softmax states in the same kernel; that needs `workspace`
  *  of at least hsa_decode_workspace_bytes() bytes, ZERO-FILLED ONCE after
  *  allocation (every call leaves it zeroed again).  Calls sharing one workspace
- *  must not run concurrently.
+ *  must not run concurrently.  After a call that set any bit in *dev_err, zero
+ *  the workspace again before reusing it.
  *  max_ctas: 0 = one persistent CTA per SM (the default); > 0 caps the CTA count
  *  (results do not depend on it beyond rounding).
  */
