@@ -151,3 +151,34 @@ def test_pool_struct_mirrors_the_tensors(fake):
     assert [c.layer_kv_fp8[i] for i in range(2)] == [0, 0]
     assert c.k[1] == pool.k[1].data_ptr() and c.v[0] == pool.v[0].data_ptr()
     assert ctypes.sizeof(binding.HsaPools) >= 16 * 4
+
+
+def test_readme_example_passes_the_binding(fake, monkeypatch):
+    """The README's Python example, run on CPU tensors against the recorder: every
+    call it makes is well formed and reaches the library."""
+    import os
+    import re
+    import types
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    text = open(os.path.join(root, "README.md"), encoding="utf-8").read()
+    code = re.search(r"```python\n(.*?)```", text, re.S).group(1)
+    code = code.replace('device="cuda"', 'device="cpu"')
+    code = code.replace("import full_attention_kv_gb300 as hsa\n", "")
+
+    class CpuPool(binding.DualPool):
+        @classmethod
+        def allocate(cls, *a, **kw):
+            kw["device"] = "cpu"
+            return binding.DualPool.allocate.__func__(cls, *a, **kw)
+
+    shim = types.SimpleNamespace(**{k: getattr(binding, k) for k in dir(binding)
+                                    if not k.startswith("__")})
+    shim.DualPool = CpuPool
+    shim.decode_workspace = lambda pool, B, T: binding.decode_workspace(pool, B, T, "cpu")
+    monkeypatch.setattr(binding.torch.cuda, "current_stream",
+                        lambda: types.SimpleNamespace(cuda_stream=0))
+    ns = {"hsa": shim, "torch": torch}
+    exec(compile(code, "README.md", "exec"), ns)
+    names = [c[0] for c in fake.calls]
+    assert names.count("hsa_kv_append") == 2 and names[-1] == "hsa_decode_attn_append"
+    assert tuple(ns["out"].shape) == (2, 1, 32, 128)
