@@ -245,11 +245,10 @@ def window_cases(n: int, W: int, seed: int, m_hi: int = 4096):
         m = rng.randint(0, m_hi)
         q = m if rng.random() < 0.5 else m + rng.randint(1, 256)
         match[k] = m
-        # slot j holds the latest position p < q with p congruent to j modulo W
-        for j in range(W):
-            if q > 0:
-                p = q - 1 - ((q - 1 - j) % W)
-                slots[k, j] = p if p >= 0 else -1
+        # the ring was written in position order: positions 0 .. q-1, each into slot
+        # p mod W over whatever it held (only the last W writes survive)
+        for p in range(max(0, q - W), q):
+            slots[k, p % W] = p
         e = rng.uniform(0.0, 0.2)
         for j in range(W):
             if rng.random() < e:
