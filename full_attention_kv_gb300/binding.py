@@ -515,11 +515,11 @@ class PrefixTree:
 
     def match_batch(self, seqs):
         """-> (match_len [n], ring_row [n], swa_slot_pos [n, W]) host int32, read-only."""
-        lens = [len(x) for x in seqs]
+        parts = [_i32_host(x, "tokens") for x in seqs]
         off = torch.zeros(len(seqs) + 1, dtype=torch.int64)
         if seqs:
-            off[1:] = torch.cumsum(torch.tensor(lens, dtype=torch.int64), 0)
-        flat = _i32_host([int(v) for x in seqs for v in x], "tokens")
+            off[1:] = torch.cumsum(torch.tensor([t.numel() for t in parts], dtype=torch.int64), 0)
+        flat = torch.cat(parts) if parts else torch.zeros(0, dtype=torch.int32)
         n = len(seqs)
         m = torch.empty(max(n, 1), dtype=torch.int32)
         r = torch.empty(max(n, 1), dtype=torch.int32)
