@@ -1,22 +1,28 @@
 #!/usr/bin/env python3
 """Benchmark of the Hybrid-SWA dual-KV-pool attention path on GB300.
 
-Default workload: decode, 70-layer stack (60 sliding W=128 + 10 full, 6:1),
+Headline workload: decode, 70-layer stack (60 sliding W=128 + 10 full, 6:1),
 32 q / 4 KV heads, d = 128, batch 32, contexts U[8K, 64K], one new token per
 sequence.  A step is the whole hot path for one batch: for every layer the
 decode attention and the append of the new token (hsa_decode_attn_append, one
 fused launch per layer), captured once in a CUDA graph and replayed.
 
-Other workloads (--workload): tiny, long (batch 4, 256K-1M), mtp (batch 48,
-mixed buckets, 4 query tokens + 1000 window-safe cases), prefill (8 requests,
-prefix 16K-128K, chunk 2K-8K).  Inputs are seeded synthetic bf16 N(0,1); the KV
-pools (tens of GB) are far larger than L2, so no extra flush is needed.
+The default run then measures, in the same JSON line, the other workloads of the
+metric, each as an object of its own with the same keys (value, ms_per_step,
+roofline, e2e, clocks, cpu_baseline): "prefill" (8 requests, prefix 16K-128K,
+chunk 2K-8K: chunked prefill attention + append on all 70 layers; TFLOP/s),
+"long" (batch 4, contexts 256K-1M) and "mtp" (batch 48, mixed buckets, 4 query
+tokens + 1000 window-safe cases).  --workload NAME measures one workload alone
+(its line then carries it at the top level).  Inputs are seeded synthetic bf16
+N(0,1); the KV pools (tens of GB) are far larger than L2, so no extra flush is
+needed.
 
 Prints ONE JSON line (rank 0).  Under torchrun every rank runs an independent
 replica of the workload (sequences are independent: weak scaling, no
 collective on the data path).
 """
 import argparse
+import gc
 import json
 import os
 import statistics
@@ -203,9 +209,27 @@ def prefill_flops(inst, layer_full):
     return 4 * cfg.d * cfg.Hq * total
 
 
+def prefill_swa_bytes(inst):
+    """Algorithmic bytes of one sliding-layer prefill launch: q read and out
+    written (rows x Hq x d bf16 each), the chunk's k_new / v_new read, and the
+    ring positions some row still sees (min(P, W - 1) per request, 2048 B each)."""
+    cfg = inst.cfg
+    rows = inst.rows
+    qo = 2 * rows * cfg.Hq * cfg.d * 2
+    kv_new = 2 * rows * cfg.Hkv * cfg.d * 2
+    per_tok = 2 * cfg.Hkv * cfg.d * 2
+    ring = int(np.minimum(inst.prefix.astype(np.int64), cfg.W - 1).sum()) * per_tok
+    return qo + kv_new + ring
+
+
 # --------------------------------------------------------------------------- reference arm
 def run_reference(args, inst):
-    """The CPU oracle as it stands on this host's cores, bounded samples."""
+    """The CPU oracle as it stands on this host's cores, bounded samples.
+
+    One timed call = the oracle on one full and one sliding layer of the sampled
+    sequences (rows).  Returns (value, unit, extrapolated 70-layer step seconds,
+    threads, sample description, median measured seconds per call); the value is
+    the workload's throughput at the extrapolated step time."""
     import oracle
     import harness  # noqa: F401  (host-only use below)
     cfg = inst.cfg
@@ -229,19 +253,24 @@ def run_reference(args, inst):
             rows = rows[:: max(1, len(rows) // 64)]  # a row subsample
         items = np.array([(r, h) for r in rows for h in range(cfg.Hq)], np.int32)
         cases[l] = (_host_case(inst, l, seqs), rows, items)
+    calls = []
     for step in range(args.warmup + args.steps):
         t_layer = {}
+        call = 0.0
         for l in (full_layer, swa_layer):
             c, rows, items = cases[l]
             t0 = time.perf_counter()
             oracle.attention(window=0 if inst.full[l] else cfg.W, scale=cfg.scale, items=items,
                              nthreads=nthreads, **c)
             dt = time.perf_counter() - t0
+            call += dt
             kpr = keys_per_row(inst, inst.full[l])
             t_layer[l] = dt * (kpr.sum() / kpr[rows].sum())  # extrapolate by keys attended
         if step >= args.warmup:
             times.append(t_layer[full_layer] * n_full + t_layer[swa_layer] * n_swa)
+            calls.append(call)
     step_s = statistics.median(times)
+    call_s = statistics.median(calls)
     if cfg.kind == "decode":
         value = inst.R * cfg.T / step_s
         unit = "tokens/s"
@@ -253,7 +282,7 @@ def run_reference(args, inst):
               "to %d layers and to all rows" % (cfg.name, len(seqs), inst.R,
                                                  ", row subsample" if cfg.kind == "prefill" else "",
                                                  n_full, n_swa, cfg.n_layers))
-    return value, unit, step_s, nthreads, sample
+    return value, unit, step_s, nthreads, sample, call_s
 
 
 def _host_case(inst, layer, seqs):
@@ -362,11 +391,20 @@ class DecodeStep:
     def outputs(self):
         return self.out
 
-    def dominant(self):
-        """(name, [layers], algorithmic bytes per launch list)."""
+    def kernels(self):
+        """The step's kernels, dominant first: (key, name, pool layers, algorithmic
+        bytes per launch, bound)."""
         full = [i for i, l in enumerate(self.model_layers) if self.inst.full[l]]
-        name = "decode_kernel (full layers%s)" % (", FP8 KV" if self.kv_fp8 else "")
-        return name, full, [decode_bytes(self.inst, True, self.kv_fp8)] * len(full)
+        swa = [i for i, l in enumerate(self.model_layers) if not self.inst.full[l]]
+        out = []
+        if full:
+            out.append(("full_fp8" if self.kv_fp8 else "full",
+                        "decode_kernel (full layers%s)" % (", FP8 KV" if self.kv_fp8 else ""),
+                        full, decode_bytes(self.inst, True, self.kv_fp8), "hbm", self.attn))
+        if swa:
+            out.append(("sliding", "decode_kernel (sliding layers, ring)", swa,
+                        decode_bytes(self.inst, False), "hbm", self.attn))
+        return out
 
     def units_per_step(self):
         return self.inst.R * self.inst.cfg.T
@@ -406,11 +444,14 @@ class PrefillStep:
                                   self.pl, self.seq, self.max_chunk, self.inst.cfg.scale,
                                   out=self.out[l], dev_err=self.err, stream=stream)
 
+    def append(self, l, stream=None):
+        self.hsa.hsa_kv_append(self.pool, l, self.k[l], self.v[l], self.cu, self.seq,
+                               self.pl, dev_err=self.err, stream=stream)
+
     def __call__(self):
         for l in self.layers:
             self.attn(l)
-            self.hsa.hsa_kv_append(self.pool, l, self.k[l], self.v[l], self.cu, self.seq,
-                                   self.pl, dev_err=self.err)
+            self.append(l)
 
     def inputs(self):
         return self.q + self.k + self.v
@@ -418,18 +459,35 @@ class PrefillStep:
     def outputs(self):
         return self.out
 
-    def dominant(self):
+    def kernels(self):
         full = [i for i, l in enumerate(self.model_layers) if self.inst.full[l]]
-        return ("prefill_kernel (full layers)", full,
-                [prefill_flops(self.inst, True)] * len(full))
+        swa = [i for i, l in enumerate(self.model_layers) if not self.inst.full[l]]
+        out = []
+        # appends move each written row once in and once out: 2 x 2048 B per token
+        # (a sliding layer writes only the last W rows of each request)
+        row = 2 * self.inst.cfg.Hkv * self.inst.cfg.d * 2
+        if full:
+            out.append(("full", "prefill_kernel (full layers)", full,
+                        prefill_flops(self.inst, True), "tensor", self.attn))
+        if swa:
+            out.append(("sliding", "prefill_swa_kernel (sliding layers)", swa,
+                        prefill_swa_bytes(self.inst), "hbm", self.attn))
+        if full:
+            out.append(("append_full", "append_kernel (full layers)", full,
+                        2 * self.inst.rows * row, "hbm", self.append))
+        if swa:
+            kept = int(np.minimum(self.inst.new, self.inst.cfg.W).sum())
+            out.append(("append_sliding", "append_kernel (sliding layers, last W rows)", swa,
+                        2 * kept * row, "hbm", self.append))
+        return out
 
     def units_per_step(self):
         return sum(prefill_flops(self.inst, self.inst.full[l]) for l in self.model_layers)
 
 
-def time_dominant(step, iters):
-    """Average duration of the dominant kernel's launches, CUDA events on its stream."""
-    name, layers, nbytes = step.dominant()
+def time_kernel(launch, layers, iters):
+    """Average duration of one kernel's launches (launch(layer, stream=...)) on
+    `layers`, CUDA events recorded on the stream the launches go to."""
     stream = torch.cuda.current_stream()
     starts = [torch.cuda.Event(enable_timing=True) for _ in layers]
     ends = [torch.cuda.Event(enable_timing=True) for _ in layers]
@@ -438,7 +496,7 @@ def time_dominant(step, iters):
     for it in range(iters + 1):
         for i, l in enumerate(layers):
             starts[i].record(stream)
-            step.attn(l, stream=stream)
+            launch(l, stream=stream)
             ends[i].record(stream)
         torch.cuda.synchronize()
         if it == 0:
@@ -446,8 +504,7 @@ def time_dominant(step, iters):
         for i in range(len(layers)):
             total_ms += starts[i].elapsed_time(ends[i])
             n += 1
-    avg_s = total_ms / n / 1e3
-    return name, avg_s, float(np.mean(nbytes))
+    return total_ms / n / 1e3
 
 
 def _prefetch_report(step, args, stream):
@@ -491,34 +548,8 @@ def _swap_io(step, ins, outs):
     return prev
 
 
-def run_ours(args, inst, ws, rank, local):
-    torch.cuda.set_device(local)
-    device = torch.device("cuda", local)
-    import full_attention_kv_gb300 as hsa
-    hsa.lib()
-    cfg = inst.cfg
-    layers = None if args.layers is None else [int(x) for x in args.layers.split(",")]
-    if cfg.kind == "decode":
-        step = DecodeStep(inst, device, layers, swa_prefetch=args.swa_prefetch,
-                          kv_fp8=args.kv_fp8)
-    else:
-        step = PrefillStep(inst, device, layers)
-    # the attention stream runs at high priority (a side stream, if any, at the default)
-    stream = torch.cuda.Stream(device, priority=-1)
-    if args.profile_step:
-        # one eager step between cudaProfilerStart / Stop (for ncu --profile-from-start off)
-        with torch.cuda.stream(stream):
-            for _ in range(args.warmup):
-                step()
-        torch.cuda.synchronize()
-        torch.cuda.cudart().cudaProfilerStart()
-        with torch.cuda.stream(stream):
-            step()
-        torch.cuda.synchronize()
-        torch.cuda.cudart().cudaProfilerStop()
-        return {"profile_step": cfg.name, "launches": step.launches_per_step,
-                "dev_err": int(step.err.item())}
-    # warm-up outside and inside the graph
+def _graph_step(step, stream, warmup):
+    """Warm the step eagerly, capture it in one CUDA graph, replay `warmup` times."""
     with torch.cuda.stream(stream):
         for _ in range(2):
             step()
@@ -527,38 +558,22 @@ def run_ours(args, inst, ws, rank, local):
     with torch.cuda.graph(graph, stream=stream):
         step()
     torch.cuda.synchronize()
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         graph.replay()
     torch.cuda.synchronize()
     if int(step.err.item()) != 0:
         raise SystemExit("device error flag set: %d" % int(step.err.item()))
+    return graph
 
-    # ---- timed region: K graph replays ------------------------------------
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
-        barrier(ws)
-        torch.cuda.synchronize()
-        e0.record()
-        for _ in range(args.steps):
-            graph.replay()
-        e1.record()
-        torch.cuda.synchronize()
-        barrier(ws)
-        step_ms = e0.elapsed_time(e1) / args.steps
-        # dominant kernel, same stream, per-launch events
-        dom_name, dom_s, dom_bytes = time_dominant(step, max(3, min(args.steps, 10)))
-        prefetch_info = None
-        if getattr(step, "prefetch", False):
-            prefetch_info = _prefetch_report(step, args, stream)
-    clocks = clk.summary()
-    step_ms = max_over_ranks(step_ms, ws)
 
-    # ---- end to end through the C ABI with host buffers ----------------------
-    # A serving loop: every step copies its inputs from pinned host memory and reads
-    # its outputs back, all inside the timed region.  Two device input / output sets,
-    # each with its own captured step, let step i+1's host-to-device copies (one
-    # stream) and step i's device-to-host read (another) overlap step i's kernels.
+def _e2e(step, graph, stream, steps, ws):
+    """End to end through the C ABI with host buffers: seconds per step, H2D and
+    D2H bytes per step.
+
+    A serving loop: every step copies its inputs from pinned host memory and reads
+    its outputs back, all inside the timed region.  Two device input / output sets,
+    each with its own captured step, let step i+1's host-to-device copies (one
+    stream) and step i's device-to-host read (another) overlap step i's kernels."""
     h_in = [t.cpu().pin_memory() for t in step.inputs()]
     h_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in step.outputs()]
     h2d = sum(t.numel() * t.element_size() for t in h_in)
@@ -607,69 +622,139 @@ def run_ours(args, inst, ws, rank, local):
     torch.cuda.synchronize()
     barrier(ws)
     t0 = time.perf_counter()
-    serve(args.steps)
+    serve(steps)
     torch.cuda.synchronize()
-    e2e_s = (time.perf_counter() - t0) / args.steps
-    e2e_s = max_over_ranks(e2e_s, ws)
+    e2e_s = (time.perf_counter() - t0) / steps
+    del sets, alt_in, alt_out, graph_b, h_in, h_out
+    return max_over_ranks(e2e_s, ws), h2d, d2h
+
+
+def _roofline(cfg_name, key, name, per_launch, bound, launch_s, pk):
+    """Roofline entry of one kernel: algorithmic work per launch / launch time."""
+    if bound == "hbm":
+        achieved = per_launch / launch_s / 1e9
+        r = {"kernel": name, "bound": "hbm", "achieved": achieved, "peak": pk["hbm"],
+             "unit": "GB/s", "frac": achieved / pk["hbm"], "traffic": _traffic(cfg_name, key),
+             "peak_source": pk["source"], "launch_us": launch_s * 1e6,
+             "bytes_per_launch": per_launch}
+    else:
+        achieved = per_launch / launch_s / 1e12
+        r = {"kernel": name, "bound": "tensor", "achieved": achieved, "peak": pk["bf16"],
+             "unit": "TFLOP/s", "frac": achieved / pk["bf16"],
+             "frac_sustained": achieved / pk["bf16_sustained"],
+             "traffic": _traffic(cfg_name, key),
+             "peak_source": pk["source"] + " (burst: each launch timed alone)",
+             "launch_us": launch_s * 1e6, "flops_per_launch": per_launch}
+    return r
+
+
+def measure(args, inst, ws, rank, local, cpu_repeats=None):
+    """One workload on this rank's GPU: the graph-timed step (max over ranks), every
+    kernel of the step against its roofline, the end-to-end serving loop, clocks
+    during the timed region, and (rank 0) the CPU oracle on a bounded sample."""
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    import full_attention_kv_gb300 as hsa
+    hsa.lib()
+    cfg = inst.cfg
+    layers = None if args.layers is None else [int(x) for x in args.layers.split(",")]
+    if cfg.kind == "decode":
+        step = DecodeStep(inst, device, layers, swa_prefetch=args.swa_prefetch,
+                          kv_fp8=args.kv_fp8)
+    else:
+        step = PrefillStep(inst, device, layers)
+    # the attention stream runs at high priority (a side stream, if any, at the default)
+    stream = torch.cuda.Stream(device, priority=-1)
+    if args.profile_step:
+        # one eager step between cudaProfilerStart / Stop (for ncu --profile-from-start off)
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                step()
+        torch.cuda.synchronize()
+        torch.cuda.cudart().cudaProfilerStart()
+        with torch.cuda.stream(stream):
+            step()
+        torch.cuda.synchronize()
+        torch.cuda.cudart().cudaProfilerStop()
+        return {"profile_step": cfg.name, "launches": step.launches_per_step,
+                "dev_err": int(step.err.item())}
+    graph = _graph_step(step, stream, args.warmup)
+
+    # ---- timed region: K graph replays ------------------------------------
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    kernels = step.kernels()
+    with ClockSampler(local) as clk:
+        barrier(ws)
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(args.steps):
+            graph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        barrier(ws)
+        step_ms = e0.elapsed_time(e1) / args.steps
+        # each kernel of the step, same stream, per-launch events
+        iters = max(3, min(args.steps, 10))
+        launch_s = [time_kernel(k[5], k[2], iters) for k in kernels]
+        prefetch_info = None
+        if getattr(step, "prefetch", False):
+            prefetch_info = _prefetch_report(step, args, stream)
+    clocks = clk.summary()
+    step_ms = max_over_ranks(step_ms, ws)
+    e2e_s, h2d, d2h = _e2e(step, graph, stream, args.steps, ws)
 
     units = step.units_per_step()
     pk = peaks()
+    roofs = [_roofline(cfg.name, k[0], k[1], k[3], k[4], s, pk) for k, s in zip(kernels, launch_s)]
     if cfg.kind == "decode":
         value = units * ws / (step_ms / 1e3)
         unit = "tokens/s"
         e2e_value = units * ws / e2e_s
-        achieved = dom_bytes / dom_s / 1e9
-        roof = {"kernel": dom_name, "bound": "hbm", "achieved": achieved, "peak": pk["hbm"],
-                "unit": "GB/s", "frac": achieved / pk["hbm"], "traffic": _traffic(cfg.name),
-                "peak_source": pk["source"], "launch_us": dom_s * 1e6,
-                "bytes_per_launch": dom_bytes}
-        kv_step = sum(decode_bytes(inst, inst.full[l]) for l in step.model_layers)
+        kv_step = sum(decode_bytes(inst, inst.full[l], args.kv_fp8 and inst.full[l])
+                      for l in step.model_layers)
         extra = {"kv_read_gbs": kv_step / (step_ms / 1e3) / 1e9,
                  "hbm_frac_step": kv_step / (step_ms / 1e3) / 1e9 / pk["hbm"]}
     else:
         value = units * ws / (step_ms / 1e3) / 1e12
         unit = "TFLOP/s"
         e2e_value = units * ws / e2e_s / 1e12
-        achieved = dom_bytes / dom_s / 1e12
-        roof = {"kernel": dom_name, "bound": "tensor", "achieved": achieved, "peak": pk["bf16"],
-                "unit": "TFLOP/s", "frac": achieved / pk["bf16"], "traffic": _traffic(cfg.name),
-                "peak_source": pk["source"] + " (burst: each launch timed alone)",
-                "launch_us": dom_s * 1e6, "flops_per_launch": dom_bytes}
-        extra = {"step_tflops_frac_sustained": value / ws / pk["bf16_sustained"],
+        extra = {"step_tflops_frac": value / ws / pk["bf16"],
+                 "step_tflops_frac_sustained": value / ws / pk["bf16_sustained"],
                  "prefill_rows": inst.rows}
     line = {
-        "metric": METRIC, "value": value, "unit": unit, "n_gpus": ws,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": DATA,
+        "value": value, "unit": unit, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": step_ms,
         "config": dict(
             workload_config(inst, ws),
             l2="inputs larger than L2 (KV pools %.1f GB)" % (_pool_bytes(step.pool) / 1e9),
             graph="one CUDA graph per step (%d launches)" % step.launches_per_step),
-        "roofline": roof,
+        "roofline": roofs[0],
+        "kernels": roofs,
         "clocks": clocks,
         "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": step.launches_per_step * args.steps,
-        "env": {"gpu": torch.cuda.get_device_name(local),
-                "sms": torch.cuda.get_device_properties(local).multi_processor_count,
-                "torch": torch.__version__, "cuda": torch.version.cuda},
     }
     line.update(extra)
-    if getattr(args, "kv_fp8", False):
+    if args.kv_fp8:
         line["dtype"] = "e4m3 Full KV Pool (fp16 MMA, fp32 accumulate), bf16 rings / q / out"
         line["config"]["kv_fp8"] = ("full layers stored as E4M3 codes + one fp32 scale per "
                                     "(token, KV head) row; sliding rings bf16")
-        line["roofline"]["traffic"] = None  # the ncu traffic figure is for the bf16 layers
     if prefetch_info is not None:
         line["swa_prefetch"] = prefetch_info
         line["config"]["swa_prefetch"] = ("every step reloads all sliding layers' rings from a "
                                           "pinned host tier on a side stream, layer by layer")
-    if rank == 0 and not args.no_cpu_baseline and not getattr(args, "kv_fp8", False):
-        v, unit, _, cores, sample = run_reference(
-            argparse.Namespace(steps=1, warmup=0), inst)
-        line["cpu_baseline"] = {"value": v, "unit": unit, "cores": cores, "kind": "oracle",
-                                "sample": sample}
+    del graph, step
+    gc.collect()
+    torch.cuda.empty_cache()
+    if rank == 0 and not args.no_cpu_baseline and not args.kv_fp8:
+        reps = args.steps if cpu_repeats is None else cpu_repeats
+        v, unit_c, _, cores, sample, call_s = run_reference(
+            argparse.Namespace(steps=reps, warmup=1), inst)
+        line["cpu_baseline"] = {"value": v, "unit": unit_c, "cores": cores, "kind": "oracle",
+                                "sample": sample + "; median of %d timed calls after 1 "
+                                "untimed (%.3f s per call)" % (reps, call_s)}
     return line
 
 
@@ -701,14 +786,27 @@ def _ctx_desc(cfg):
     return "U[%d,%d]" % (cfg.ctx_lo, cfg.ctx_hi)
 
 
-# DRAM bytes per launch of the dominant kernel from an ncu capture, keyed by the
-# workload and the code digest (code_digest) of the kernel it was taken on (None =
-# not taken on the current kernel).
+# DRAM bytes per launch of a kernel from an ncu capture, keyed by (workload, kernel)
+# and by the code digest (code_digest) of the source the capture was taken on; a
+# kernel whose source has changed since reports None.  Captures of fewer
+# sequences / requests are scaled to the full launch by the units processed.
 TRAFFIC = {
-    # profiles/decode_full_ncu_decode-b4.md: 389.6 MB on 4 sequences, scaled by units
-    "decode": ("8968219e5757c4b2", 2832812948),
-    # profiles/prefill_full_ncu_prefill-r2.md: 4.552 GB on 2 requests, scaled by flops
-    "prefill": ("0e97e900cd7e5029", 14340211242),
+    # decode_kernel, full layer: 389.6 MB on 4 sequences, scaled by units
+    ("decode", "full"): ("decode.cu", "8968219e5757c4b2", 2832812948),
+    # decode_kernel, sliding layer: full-size launch (32 sequences)
+    ("decode", "sliding"): ("decode.cu", "8968219e5757c4b2", 8785408),
+    # decode_kernel, FP8 full layer: 202.6 MB on 4 sequences, scaled by units
+    ("decode", "full_fp8"): ("decode.cu", "8968219e5757c4b2", 1472737897),
+    # decode_kernel, full layer: 1.608 GB on 1 sequence, scaled by units
+    ("long", "full"): ("decode.cu", "8968219e5757c4b2", 5675719535),
+    # decode_kernel, full layer, T = 4: 1.658 GB on 8 sequences, scaled by units
+    ("mtp", "full"): ("decode.cu", "8968219e5757c4b2", 11701335556),
+    # prefill_kernel, full layer: 4.552 GB on 2 requests, scaled by flops
+    ("prefill", "full"): ("prefill.cu", "0e97e900cd7e5029", 14340211242),
+    # append_kernel, full-size launches (writes still held in L2 at the kernel's end
+    # reach DRAM after it)
+    ("prefill", "append_full"): ("append.cu", "5b0ffb5eddb0d066", 146275328),
+    ("prefill", "append_sliding"): ("append.cu", "5b0ffb5eddb0d066", 2109184),
 }
 
 
@@ -723,13 +821,18 @@ def code_digest(path):
     return hashlib.sha256("\n".join(l for l in lines if l).encode()).hexdigest()[:16]
 
 
-def _traffic(name):
-    kern = "prefill.cu" if workload.CONFIGS[name].kind == "prefill" else "decode.cu"
-    digest = code_digest(os.path.join(ROOT, "full_attention_kv_gb300", "csrc", kern))
-    t = TRAFFIC.get(name)
-    if t and t[0] == digest:
-        return t[1]
-    return None
+def _traffic(name, key):
+    t = TRAFFIC.get((name, key))
+    if not t:
+        return None
+    digest = code_digest(os.path.join(ROOT, "full_attention_kv_gb300", "csrc", t[0]))
+    return t[2] if t[1] == digest else None
+
+
+EXTRA_WORKLOADS = ("prefill", "long", "mtp")
+# CPU oracle repeats for the extra workloads (each call already covers a bounded
+# sample of the workload; the headline workload repeats as many times as --steps)
+EXTRA_CPU_REPEATS = 2
 
 
 def main():
@@ -738,7 +841,9 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="decode", choices=sorted(workload.CONFIGS))
+    ap.add_argument("--workload", default=None, choices=sorted(workload.CONFIGS),
+                    help="measure one workload alone (default: decode as the headline, then "
+                         "%s in the same line)" % ", ".join(EXTRA_WORKLOADS))
     ap.add_argument("--batch", type=int, default=None, help="truncate the draw (profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--swa-prefetch", action="store_true",
@@ -751,27 +856,36 @@ def main():
     ap.add_argument("--profile-step", action="store_true",
                     help="run one eager step inside cudaProfilerStart/Stop and exit")
     args = ap.parse_args()
-    if args.kv_fp8 and workload.CONFIGS[args.workload].kind != "decode":
+    head_name = args.workload or "decode"
+    single = (args.workload is not None or args.swa_prefetch or args.kv_fp8 or
+              args.layers is not None or args.batch is not None or args.profile_step)
+    if args.kv_fp8 and workload.CONFIGS[head_name].kind != "decode":
         ap.error("--kv-fp8 is a decode variant (prefill reads bf16 pools)")
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     ws, rank, local = dist_env()
-    cfg = workload.shard(workload.CONFIGS[args.workload], rank)
+    cfg = workload.shard(workload.CONFIGS[head_name], rank)
     inst = workload.draw(cfg, R=args.batch)
 
     if args.impl == "reference":
         if rank != 0:
             return
-        v, unit, step_s, cores, sample = run_reference(args, inst)
+        v, unit, step_s, cores, sample, call_s = run_reference(args, inst)
         line = {"impl": "reference", "metric": METRIC, "value": v, "unit": unit,
                 "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-                "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
+                "ms_per_step": call_s * 1e3,
+                "extrapolated_ms_per_step": step_s * 1e3,
+                "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "f64",
                 "data": DATA,
                 "config": dict(workload_config(inst, 1),
                                parallelism="oracle on the host cores (rank 0's workload)"),
                 "cpu_baseline": {"value": v, "unit": unit, "cores": cores, "kind": "oracle",
-                                 "sample": sample},
+                                 "sample": sample + "; ms_per_step is the measured time of "
+                                 "one call on the sample (median of %d after %d untimed), "
+                                 "extrapolated_ms_per_step the %d-layer step time the value "
+                                 "is computed from" % (args.steps, args.warmup,
+                                                       cfg.n_layers)},
                 "e2e": {"value": v, "unit": unit, "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
@@ -779,7 +893,32 @@ def main():
 
     if ws > 1:
         torch.distributed.init_process_group("nccl")
-    line = run_ours(args, inst, ws, rank, local)
+    res = measure(args, inst, ws, rank, local)
+    if "profile_step" in res:
+        if rank == 0:
+            print(json.dumps(res))
+        if ws > 1:
+            torch.distributed.destroy_process_group()
+        return
+    line = {"metric": METRIC, "value": res.pop("value"), "unit": res.pop("unit"),
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": res.pop("ms_per_step"), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": res.pop("dtype", "bf16"),
+            "data": DATA}
+    res.pop("steps")
+    res.pop("warmup")
+    line.update(res)
+    line["env"] = {"gpu": torch.cuda.get_device_name(local),
+                   "sms": torch.cuda.get_device_properties(local).multi_processor_count,
+                   "torch": torch.__version__, "cuda": torch.version.cuda}
+    if not single:
+        # the metric's other workloads, each with the same keys, in the same line
+        for name in EXTRA_WORKLOADS:
+            sub = workload.draw(workload.shard(workload.CONFIGS[name], rank))
+            r = measure(args, sub, ws, rank, local, cpu_repeats=EXTRA_CPU_REPEATS)
+            r["dtype"] = "bf16"
+            line[name] = r
+            line["gpu_launches"] += r["gpu_launches"]
     if rank == 0:
         print(json.dumps(line))
     if ws > 1:

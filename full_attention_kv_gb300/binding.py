@@ -467,11 +467,22 @@ def hsa_window_safe_len_bitmap(match_len, live_off, live, W, out=None, stream=No
 
 
 def _i32_host(a, name):
-    """A contiguous host int32 tensor view of a sequence of ints (or a tensor)."""
-    t = torch.as_tensor(a, dtype=torch.int32)
+    """A contiguous host int32 tensor of a one-dimensional sequence of ints (or a
+    tensor).  Values outside the int32 range are refused, not wrapped."""
+    t = a if isinstance(a, torch.Tensor) else torch.as_tensor(a)
     if t.is_cuda:
         raise ValueError("%s must be host memory" % name)
-    return t.contiguous().view(-1)
+    if t.dim() > 1:
+        raise ValueError("%s must be one-dimensional, got shape %s" % (name, tuple(t.shape)))
+    if t.numel() == 0:
+        return torch.zeros(0, dtype=torch.int32)
+    if t.is_floating_point() or t.is_complex():
+        raise ValueError("%s must hold integers, got %s" % (name, t.dtype))
+    if t.dtype != torch.int32:
+        lo, hi = int(t.min()), int(t.max())
+        if lo < -2 ** 31 or hi > 2 ** 31 - 1:
+            raise ValueError("%s holds values outside the int32 range" % name)
+    return t.to(torch.int32).contiguous().view(-1)
 
 
 class PrefixTree:

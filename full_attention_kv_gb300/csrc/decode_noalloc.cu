@@ -29,7 +29,10 @@ std::mutex g_mu;
 void *g_scratch_addr[kMaxDevices] = {};
 
 // Device address of g_decode_scratch on the current device, looked up once per
-// device (the first call on a device may load this module's device code).
+// device (the first call on a device may load this module's device code).  The
+// address is kept for the life of the process: it stays valid while the device's
+// context lives, so the entry point must not be called again after cudaDeviceReset
+// (or any teardown of the primary context) in the same process.
 cudaError_t scratch_address(void **out)
 {
     int dev = 0;
@@ -58,7 +61,10 @@ extern "C" hsa_status hsa_decode_attn_noalloc(const hsa_pools *pools, int32_t la
                                               int32_t B, int32_t T, float scale, void *out,
                                               int32_t max_ctas, int32_t *dev_err, void *stream)
 {
-    // every host check first: a refused call must launch nothing (not even the memset)
+    // every host argument check first: a call refused for its arguments queues
+    // nothing, not even the memset (a CUDA failure further on -- the symbol lookup,
+    // tensor-map encoding or the launch -- may leave the counter reset queued, which
+    // only zeroes counters)
     bool done = false;
     const hsa_status st = hsa::decode_host_check(pools, layer, q, k_new, v_new, cached_len, B, T,
                                                  out, max_ctas, &done);

@@ -190,6 +190,8 @@ hsa_status hsa_decode_attn_append(const hsa_pools *pools, int32_t layer, const v
  * at what fits (about 250).  This call allocates and frees nothing.
  *  - The first call on a device looks up the array's device address (and may load
  *    the library's device code): make that first call before any stream capture.
+ *    The address is kept until the process exits: do not call this again after
+ *    cudaDeviceReset (or another teardown of the device's primary context).
  *  - Each call zeroes the counter part of the array on `stream`, then launches.
  *  - All calls share the one array, so calls whose kernels could overlap on the
  *    GPU (different streams, or different host threads) race; serialise them.

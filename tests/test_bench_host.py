@@ -94,3 +94,39 @@ def test_workload_config_names_the_workload():
         assert c["global_batch"] == 2 * inst.R and c["T"] == cfg.T
         assert c["parallelism"] == "replicas x2"
         assert 0 < c["kv_pool_vs_all_full"] <= 1
+
+
+def test_prefill_sliding_bytes_against_enumeration():
+    """Sliding-layer prefill moves q in, out back, the chunk's new K/V in, and each
+    prefix position that some chunk row still sees (brute force over the rows)."""
+    cfg = dataclasses.replace(workload.CONFIGS["prefill"], prefixes=(0, 3, 130, 257, 127),
+                              chunks=(5, 128, 1, 300, 2), R=5)
+    inst = workload.draw(cfg)
+    per_tok = 2 * cfg.Hkv * cfg.d * 2
+    ring = 0
+    for P, C in zip(inst.prefix, inst.new):
+        seen = set()
+        for i in range(int(C)):
+            q = int(P) + i
+            seen.update(k for k in range(int(P)) if q - k < cfg.W)
+        ring += len(seen) * per_tok
+    rows = inst.rows
+    want = 2 * rows * cfg.Hq * cfg.d * 2 + 2 * rows * cfg.Hkv * cfg.d * 2 + ring
+    assert bench.prefill_swa_bytes(inst) == want
+
+
+def test_traffic_is_dropped_once_the_kernel_source_changes(tmp_path, monkeypatch):
+    """A capture's DRAM figure is reported only while the kernel's source (comments
+    aside) still matches the digest it was taken on."""
+    src = tmp_path / "full_attention_kv_gb300" / "csrc"
+    src.mkdir(parents=True)
+    f = src / "k.cu"
+    f.write_text("__global__ void k(int *p) { p[0] = 1; }\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "TRAFFIC", {("w", "full"): ("k.cu", bench.code_digest(f), 123)})
+    assert bench._traffic("w", "full") == 123
+    assert bench._traffic("w", "sliding") is None
+    f.write_text("// a comment\n__global__ void k(int *p) { p[0] = 1; }\n")
+    assert bench._traffic("w", "full") == 123
+    f.write_text("__global__ void k(int *p) { p[0] = 2; }\n")
+    assert bench._traffic("w", "full") is None

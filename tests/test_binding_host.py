@@ -6,6 +6,7 @@ Every entry point must refuse a tensor whose size disagrees with the pool (the C
 ABI cannot see sizes) and pass a well-formed call through with the sizes it was
 given."""
 import ctypes
+import types
 
 import pytest
 import torch
@@ -153,32 +154,31 @@ def test_pool_struct_mirrors_the_tensors(fake):
     assert ctypes.sizeof(binding.HsaPools) >= 16 * 4
 
 
-def test_readme_example_passes_the_binding(fake, monkeypatch):
-    """The README's Python example, run on CPU tensors against the recorder: every
-    call it makes is well formed and reaches the library."""
-    import os
-    import re
-    import types
-    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    text = open(os.path.join(root, "README.md"), encoding="utf-8").read()
-    code = re.search(r"```python\n(.*?)```", text, re.S).group(1)
-    code = code.replace('device="cuda"', 'device="cpu"')
-    code = code.replace("import full_attention_kv_gb300 as hsa\n", "")
-
-    class CpuPool(binding.DualPool):
-        @classmethod
-        def allocate(cls, *a, **kw):
-            kw["device"] = "cpu"
-            return binding.DualPool.allocate.__func__(cls, *a, **kw)
-
-    shim = types.SimpleNamespace(**{k: getattr(binding, k) for k in dir(binding)
-                                    if not k.startswith("__")})
-    shim.DualPool = CpuPool
-    shim.decode_workspace = lambda pool, B, T: binding.decode_workspace(pool, B, T, "cpu")
+def test_usage_flow_passes_the_binding(fake, monkeypatch):
+    """The documented flow of a decode step -- allocate the dual pool, fill it with
+    hsa_kv_append, then one fused decode step -- on CPU tensors against the recorder:
+    every call is well formed and reaches the library."""
     monkeypatch.setattr(binding.torch.cuda, "current_stream",
                         lambda: types.SimpleNamespace(cuda_stream=0))
-    ns = {"hsa": shim, "torch": torch}
-    exec(compile(code, "README.md", "exec"), ns)
+    dev = "cpu"
+    full = [False, True]                                   # one sliding, one full layer
+    bt = torch.tensor([[0, 1], [2, 3]], dtype=torch.int32)  # 2 sequences x 2 pages
+    rr = torch.tensor([1, 0], dtype=torch.int32)
+    pool = binding.DualPool.allocate(full, num_blocks=4, n_ring_rows=2, block_tables=bt,
+                                     ring_row=rr, Hq=32, Hkv=4, device=dev)
+    for layer in range(2):
+        k = torch.zeros((70, 4, 128), dtype=torch.bfloat16)
+        v = torch.zeros_like(k)
+        cu = torch.tensor([0, 30, 70], dtype=torch.int32)
+        seq = torch.tensor([0, 1], dtype=torch.int32)
+        start = torch.tensor([0, 0], dtype=torch.int32)
+        binding.hsa_kv_append(pool, layer, k, v, cu, seq, start)
+    q = torch.zeros((2, 1, 32, 128), dtype=torch.bfloat16)
+    kn = torch.zeros((2, 1, 4, 128), dtype=torch.bfloat16)
+    cl = torch.tensor([30, 40], dtype=torch.int32)
+    ws = binding.decode_workspace(pool, 2, 1, dev)
+    out = binding.hsa_decode_attn_append(pool, 1, q, kn, kn.clone(), cl, 128 ** -0.5,
+                                         workspace=ws)
     names = [c[0] for c in fake.calls]
     assert names.count("hsa_kv_append") == 2 and names[-1] == "hsa_decode_attn_append"
-    assert tuple(ns["out"].shape) == (2, 1, 32, 128)
+    assert tuple(out.shape) == (2, 1, 32, 128)

@@ -217,3 +217,19 @@ def test_noalloc_refuses_before_touching_its_scratch():
     bad = ctypes.byref(_pools(hsa, W=96))
     assert na(bad, 0, 256, 256, 256, 256, 1, 1, 0.1, 256, 0, None, None) == \
         hsa.HSA_UNSUPPORTED_SHAPE
+
+
+def test_noalloc_unit_cap_is_refused_on_the_host():
+    """The no-workspace decode holds arrival counters for at most 4096 (sequence, KV
+    head) units in its fixed scratch: a batch of 1025 sequences x 4 KV heads (4100
+    units) inside a pool that has room for it is refused with HSA_UNSUPPORTED_SHAPE
+    on either kind of layer.  (No call here passes the host checks: the pointers are
+    placeholders that no kernel may ever receive.)"""
+    import full_attention_kv_gb300 as hsa
+    L = hsa.lib()
+    na = L.hsa_decode_attn_noalloc
+    p = ctypes.byref(_pools(hsa, batch=2048, Hkv=4, Hq=32))
+    assert na(p, 1, 256, 256, 256, 256, 1025, 1, 0.1, 256, 0, None, None) == \
+        hsa.HSA_UNSUPPORTED_SHAPE
+    assert na(p, 0, 256, 256, 256, 256, 1025, 1, 0.1, 256, 0, None, None) == \
+        hsa.HSA_UNSUPPORTED_SHAPE

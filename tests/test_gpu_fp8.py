@@ -45,11 +45,13 @@ def _logical(pool, i):
 
 
 def _gather(inst, arr, s, n):
-    """Rows of positions 0 .. n-1 of sequence s from a [nb, Hkv, page, ...] array."""
-    pg = inst.cfg.page
-    pos = np.arange(n)
-    blk = inst.block_tables[s, pos // pg]
-    return arr[blk, :, pos % pg]
+    """Rows of positions 0 .. n-1 of sequence s from a [nb, Hkv, page, ...] array,
+    each located by the oracle's placement."""
+    at = [oracle.full_place(inst.block_tables, inst.num_blocks, inst.cfg.page, s, p)
+          for p in range(n)]
+    blk = np.array([b for b, _ in at], np.int64)
+    off = np.array([o for _, o in at], np.int64)
+    return arr[blk, :, off]
 
 
 def _fp8_case(inst, layer, seqs):

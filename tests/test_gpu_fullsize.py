@@ -68,8 +68,10 @@ def test_decode_full_size_sampled(name):
             for t in range(T):
                 pos = int(inst.prefix[s]) + t
                 if inst.full[l]:
-                    blk = int(inst.block_tables[s, pos // cfg.page])
-                    row_k = pool.k[i][blk, :, pos % cfg.page]
+                    blk, off = oracle.full_place(inst.block_tables, inst.num_blocks, cfg.page,
+                                                 s, pos)
+                    row_k = pool.k[i][blk, :, off]
                 else:
-                    row_k = pool.k[i][int(inst.ring_row[s]), :, pos % cfg.W]
+                    row, slot = oracle.ring_place(inst.ring_row, inst.n_ring_rows, cfg.W, s, pos)
+                    row_k = pool.k[i][row, :, slot]
                 assert torch.equal(row_k, k[s, t])

@@ -9,6 +9,7 @@ model) and invariants (locked paths survive, only least-recently-used leaves go)
 import random
 
 import pytest
+import torch
 
 import oracle
 from oracle.prefix_model import PrefixModel, ring_positions
@@ -301,3 +302,20 @@ def test_evict_full_default_buffers_fit_any_leaf():
     tree.insert(list(range(n)), list(range(n)))
     freed, rows = tree.evict_full(1)
     assert len(freed) == n and tree.stats()[0] == 0
+
+
+def test_token_arrays_are_checked_not_wrapped():
+    """Token ids past the int32 range and two-dimensional token arrays are refused
+    by the binding before they reach the C ABI (a silent wrap would match the wrong
+    prefix)."""
+    tree = _tree()
+    with pytest.raises(ValueError):
+        tree.match(torch.tensor([1, 2 ** 31], dtype=torch.int64))
+    with pytest.raises(ValueError):
+        tree.match_batch([torch.tensor([5, -(2 ** 31) - 1], dtype=torch.int64)])
+    with pytest.raises(ValueError):
+        tree.match(torch.ones((2, 3), dtype=torch.int32))
+    with pytest.raises(ValueError):
+        tree.match([1.5, 2.0])
+    m, _, _ = tree.match_batch([torch.tensor([7, 2 ** 31 - 1], dtype=torch.int64), []])
+    assert m.tolist() == [0, 0]
