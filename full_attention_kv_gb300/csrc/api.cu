@@ -50,16 +50,16 @@ bool encode_2d(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows,
 }
 
 // 3-D bf16 tensor map over a packed [d2][d1][d0] tensor (d0 = 128 elements);
-// box = box0 x 1 x box2; 128-byte swizzle.
+// box = box0 x box1 x box2; 128-byte swizzle.
 bool encode_3d(CUtensorMap *map, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
-               uint32_t box0, uint32_t box2)
+               uint32_t box0, uint32_t box2, uint32_t box1 = 1)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn)
         return false;
     cuuint64_t dims[3] = {d0, d1, d2};
     cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
-    cuuint32_t box[3] = {box0, 1, box2};
+    cuuint32_t box[3] = {box0, box1, box2};
     cuuint32_t estr[3] = {1, 1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -240,8 +240,11 @@ namespace {
 hsa_status decode_common(const hsa_pools *pools, int32_t layer, const void *q, const void *k_new,
                          const void *v_new, const int32_t *cached_len, int32_t B, int32_t T,
                          float scale, void *out, void *workspace, size_t ws_bytes,
-                         int32_t max_ctas, int32_t *dev_err, void *stream, int append)
+                         int32_t max_ctas, int32_t *dev_err, void *stream, int32_t options)
 {
+    if (options & ~(HSA_DECODE_APPEND | HSA_DECODE_EARLY_POOL_READ))
+        return HSA_INVALID_ARG;
+    const bool append = (options & HSA_DECODE_APPEND) != 0;
     bool done = false;
     const hsa_status st = hsa::decode_host_check(pools, layer, q, k_new, v_new, cached_len, B, T,
                                                  out, max_ctas, &done);
@@ -302,7 +305,8 @@ hsa_status decode_common(const hsa_pools *pools, int32_t layer, const void *q, c
     p.T = (int16_t)T;
     p.G = (int16_t)G;
     p.flags = (full ? 0 : hsa::kDecodeRing) | (append ? hsa::kDecodeAppend : 0) |
-              (fp8 ? hsa::kDecodeFp8 : 0);
+              (fp8 ? hsa::kDecodeFp8 : 0) |
+              ((!full && (options & HSA_DECODE_EARLY_POOL_READ)) ? hsa::kDecodeEarly : 0);
     p.scale_log2 = scale * 1.4426950408889634f;
     return hsa::launch_decode(tmK, tmV, p, ctas, static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? HSA_OK
@@ -329,7 +333,17 @@ hsa_status hsa_decode_attn_append(const hsa_pools *pools, int32_t layer, const v
                                   int32_t *dev_err, void *stream)
 {
     return decode_common(pools, layer, q, k_new, v_new, cached_len, B, T, scale, out, workspace,
-                         ws_bytes, max_ctas, dev_err, stream, 1);
+                         ws_bytes, max_ctas, dev_err, stream, HSA_DECODE_APPEND);
+}
+
+hsa_status hsa_decode_attn_ex(const hsa_pools *pools, int32_t layer, const void *q,
+                              const void *k_new, const void *v_new, const int32_t *cached_len,
+                              int32_t B, int32_t T, float scale, void *out, void *workspace,
+                              size_t ws_bytes, int32_t max_ctas, int32_t options,
+                              int32_t *dev_err, void *stream)
+{
+    return decode_common(pools, layer, q, k_new, v_new, cached_len, B, T, scale, out, workspace,
+                         ws_bytes, max_ctas, dev_err, stream, options);
 }
 
 hsa_status hsa_prefill_attn(const hsa_pools *pools, int32_t layer, const void *q,
@@ -355,7 +369,17 @@ hsa_status hsa_prefill_attn(const hsa_pools *pools, int32_t layer, const void *q
     CUtensorMap tmPK, tmPV, tmNK, tmNV, tmQ;
     const uint64_t prow = full ? (uint64_t)pools->num_blocks * pools->Hkv * pools->page_size
                                : (uint64_t)pools->n_ring_rows * pools->Hkv * pools->W;
-    if (!encode_2d(&tmPK, pools->k[layer], 128, prow, 128, 64, 64) ||
+    const bool swa_kernel = !full && hsa::prefill_swa_supported(pools->W, G);
+    if (swa_kernel) {
+        // q boxes of 128 / G positions x the G heads of one KV head; K / V boxes of
+        // 16 rows (chunk rows, or 16 slots of a ring)
+        if (!encode_2d(&tmPK, pools->k[layer], 128, prow, 128, 64, 16) ||
+            !encode_2d(&tmPV, pools->v[layer], 128, prow, 128, 64, 16) ||
+            !encode_3d(&tmNK, k_new, 128, pools->Hkv, rows, 64, 16) ||
+            !encode_3d(&tmNV, v_new, 128, pools->Hkv, rows, 64, 16) ||
+            !encode_3d(&tmQ, q, 128, pools->Hq, rows, 64, 128 / G, G))
+            return HSA_CUDA_ERROR;
+    } else if (!encode_2d(&tmPK, pools->k[layer], 128, prow, 128, 64, 64) ||
         !encode_2d(&tmPV, pools->v[layer], 128, prow, 128, 64, 64) ||
         !encode_3d(&tmNK, k_new, 128, pools->Hkv, rows, 64, 128) ||
         !encode_3d(&tmNV, v_new, 128, pools->Hkv, rows, 64, 128) ||
@@ -388,10 +412,17 @@ hsa_status hsa_prefill_attn(const hsa_pools *pools, int32_t layer, const void *q
     const int64_t b2 = (int64_t)R * ((max_chunk + 127) / 128);
     p.tiles_per_req_bound = (int32_t)std::min(b1, b2);
     p.scale_log2 = scale * 1.4426950408889634f;
-    return hsa::launch_prefill(tmPK, tmPV, tmNK, tmNV, tmQ, p, static_cast<cudaStream_t>(stream)) ==
-                   cudaSuccess
-               ? HSA_OK
-               : HSA_CUDA_ERROR;
+    cudaError_t e;
+    if (swa_kernel) {
+        const int sms = device_sms();
+        if (sms <= 0)
+            return HSA_CUDA_ERROR;
+        e = hsa::launch_prefill_swa(tmQ, tmNK, tmNV, tmPK, tmPV, p, sms,
+                                    static_cast<cudaStream_t>(stream));
+    } else {
+        e = hsa::launch_prefill(tmPK, tmPV, tmNK, tmNV, tmQ, p, static_cast<cudaStream_t>(stream));
+    }
+    return e == cudaSuccess ? HSA_OK : HSA_CUDA_ERROR;
 }
 
 hsa_status hsa_swa_prefetch(const hsa_pools *pools, int32_t layer, const void *host_k,

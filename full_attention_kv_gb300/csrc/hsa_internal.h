@@ -37,6 +37,8 @@ struct DecodeParams {
 constexpr int32_t kDecodeRing = 1;    // sliding layer: read the SWA ring
 constexpr int32_t kDecodeAppend = 2;  // append the T new rows (hsa_decode_attn_append)
 constexpr int32_t kDecodeFp8 = 4;     // full layer stored as E4M3 codes + scales (fp8_kv.cuh)
+constexpr int32_t kDecodeEarly = 8;   // sliding layer: walk and load the ring before the
+                                      // grid-dependency wait (HSA_DECODE_EARLY_POOL_READ)
 static_assert(sizeof(DecodeParams) <= 128, "keep the decode parameter struct <= 128 bytes");
 
 // Bytes of the arrival-counter region at the start of a decode workspace.
@@ -97,6 +99,16 @@ size_t prefill_smem_bytes();
 cudaError_t launch_prefill(const CUtensorMap &tmPoolK, const CUtensorMap &tmPoolV,
                            const CUtensorMap &tmNewK, const CUtensorMap &tmNewV,
                            const CUtensorMap &tmQ, const PrefillParams &p, cudaStream_t stream);
+
+// Sliding layers whose window and GQA group fit one key tile (W + 128 / G + 16 <=
+// 160 keys: W = 64 or 128 at G = 8, W = 64 at G = 2 or 4) run the persistent
+// sliding-window prefill kernel
+// (prefill_swa.cu); other sliding shapes run prefill_kernel in ring mode.
+bool prefill_swa_supported(int W, int G);
+cudaError_t launch_prefill_swa(const CUtensorMap &tmQ, const CUtensorMap &tmNewK,
+                               const CUtensorMap &tmNewV, const CUtensorMap &tmRingK,
+                               const CUtensorMap &tmRingV, const PrefillParams &p, int sms,
+                               cudaStream_t stream);
 
 struct SwaPrefetchParams {
     const uint4 *host_k;         // pinned host ring rows [n_host_rows, Hkv, W, d] (device-visible)

@@ -340,6 +340,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
         const uint32_t col_s = t * 128, col_o = kColO + t * 128;
         float m_used = -INFINITY, l = 0.f;
+        // Full layers let the running max lag by up to 2^8 (few O rescales over long
+        // rows).  Ring mode raises it exactly: its rows see at most W keys, some only
+        // a handful, and then the dominant weight must stay exactly 1 (a lagging max
+        // rounds it to bf16 like the rest, which at |o| ~ 2 costs a bf16 output ulp).
+        const float slack = p.ring_mode ? 0.f : kRescaleSlack;
         int ring_row_ok = 1;
         if (p.ring_mode) {
             const int rr = __ldg(p.ring_row + seq);
@@ -418,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * p.scale_log2;
             // ---- running max, lazily raised (O is rescaled below when it moves) ----
             float m_new = m_used;
-            if (mx != -INFINITY && (m_used == -INFINITY || mx > m_used + kRescaleSlack))
+            if (mx != -INFINITY && (m_used == -INFINITY || mx > m_used + slack))
                 m_new = mx;
             const bool resc = m_used != -INFINITY && m_new != m_used;
             const float alpha = resc ? fast_exp2(m_used - m_new) : 1.0f;

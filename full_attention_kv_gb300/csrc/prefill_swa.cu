@@ -1,0 +1,585 @@
+// prefill_swa.cu -- chunked prefill attention of a sliding-window layer (sm_103a,
+// tcgen05).
+//
+// What it computes [youleyou.com "小米MiMo首次公开模型推理系统全链路优化降价99%", s1
+// "为什么选择 Hybrid SWA 架构": an SWA layer attends only the last 128 tokens, so its
+// prefill work is set by the window, not the context; s2 "KVCache系统重构": the SWA KV
+// Pool is a ring of W slots per sequence]: request r has P cached tokens and C new
+// rows at positions P + i; row i attends positions max(0, P + i - W + 1) .. P + i,
+// those below P read from the sequence's ring (slot = position mod W), the others
+// from the chunk's own k_new / v_new.
+//
+// Why a kernel of its own: a row of a sliding layer attends at most W keys, so per
+// chunk row the launch does 4 d W Hq flops (2.1 MFLOP at W = 128, Hq = 32) while it
+// reads the row's q and writes its output (16 KB) plus the row's new K / V (2 KB):
+// about 115 flops per byte, below the ~270 per byte at which GB300's tensor cores
+// and HBM balance.  HBM bounds it.  So q and out stream through once, every K / V
+// byte loaded serves all G query heads that share it, and a row's tensor work is one
+// S tile and one PV tile.
+//
+// Design (persistent, one CTA per SM, tiles dealt round-robin):
+//  * A tile is one KV head h and 128 / G consecutive chunk rows i0 .. of one request.
+//    Its M = 128 query rows are those positions times the G query heads sharing h
+//    (row = position * G + head): one TMA box of q gives them.
+//  * Its keys are two regions in shared memory, loaded by TMA in 16-row boxes:
+//      ring region   prefix positions a0 .. ceil16(P) - 1 (a0 = the first position a
+//                    row of the tile sees, rounded down to 16) read from ring slots
+//                    position mod W -- 16-aligned blocks never wrap the ring;
+//      chunk region  chunk rows max(0, i0 - W) .. i0 + 128/G - 1.
+//    At most W + 128/G + 16 keys (160 for W = 128, G = 8), so S = Q K^T is one MMA
+//    chain of N <= 160 columns and each row's softmax is exact: the row maximum is
+//    known before any exponential, no running max, no rescale of O.
+//  * Two shared-memory stages (q, K, V of one tile) and two TMEM slots (S, P, O of
+//    one tile); tile n uses stage and slot n mod 2.  Warp 0 = TMA producer; warp 1 =
+//    TMEM owner and single-thread MMA issuer; warps 2-5 / 6-9 = softmax and epilogue
+//    of the even / odd tiles, one query row per thread (TMEM lane = row).  The MMA
+//    thread issues S(n) and then PV(n-1), so the tensor cores run one tile while the
+//    other tile's warps compute softmax or write their output.
+//  * TMEM slot (256 columns): S at [0, N); P as bf16 pairs over S's first N/2
+//    columns; O at [128, 256), written by the PV MMA once the softmax has read all of
+//    S.  The epilogue divides O by the row sum (of the bf16 P the MMA used) and
+//    writes bf16.
+#include "hsa_device.cuh"
+#include "hsa_internal.h"
+
+namespace hsa {
+namespace {
+
+constexpr int kBM = 128;                   // query rows per tile (positions x heads)
+constexpr int kD = 128;
+constexpr int kKvRows = 160;               // key capacity of a stage
+constexpr int kBox = 16;                   // rows per K / V TMA box
+constexpr int kQHalf = kBM * 128;          // 128 rows x 64 bf16 (one swizzle column block)
+constexpr int kKvHalf = kKvRows * 128;
+constexpr int kThreads = 320;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kSlotCols = 256;
+constexpr uint32_t kColO = 128;
+
+struct TileInfo {
+    int32_t valid;     // 0: a bad request -- nothing loaded, nothing written
+    int32_t i0;        // first chunk row of the tile
+    int32_t C, P;      // chunk rows and prefix length of the request
+    int32_t row_base;  // the request's first row in q / k_new / out
+    int32_t h;         // KV head
+    int32_t nr, nc;    // keys in the ring and chunk regions (multiples of 16)
+    int32_t a0, z0;    // first position of the ring region, first chunk row
+};
+
+struct SwaSmem {
+    alignas(1024) uint8_t q[2][2 * kQHalf];
+    alignas(1024) uint8_t k[2][2 * kKvHalf];
+    alignas(1024) uint8_t v[2][2 * kKvHalf];
+    // stage s: q + K loaded / free (free once S has read them), V loaded / free
+    alignas(8) uint64_t full_qk[2], empty_qk[2], full_v[2], empty_v[2];
+    uint64_t s_full[2], p_full[2], o_full[2], t_free[2];  // per TMEM slot
+    // description of tile k in info[k mod 4]: the producer writes tile k + 4's once
+    // stage k mod 2 frees for it, i.e. after S(k + 2), which waits for tile k's
+    // epilogue -- so no slot is overwritten while its tile's warps may still read it
+    TileInfo info[4];
+    uint32_t tmem_base;
+    int32_t total;
+    int32_t red[kThreads / 32];
+};
+
+__device__ __forceinline__ int chunk_rows(const PrefillParams &p, int r)
+{
+    return __ldg(p.cu_rows + r + 1) - __ldg(p.cu_rows + r);
+}
+
+__device__ __forceinline__ int tiles_of(const PrefillParams &p, int r, int ppt)
+{
+    const int C = chunk_rows(p, r);
+    return C > 0 ? ((C + ppt - 1) / ppt) * p.Hkv : 0;
+}
+
+// Bit c set iff column c0 + c lies in [lo, hi).
+__device__ __forceinline__ uint32_t range_mask(int c0, int lo, int hi)
+{
+    const int a = min(max(lo - c0, 0), 32), b = min(max(hi - c0, 0), 32);
+    if (b <= a)
+        return 0u;
+    const uint32_t below_b = b == 32 ? 0xffffffffu : (1u << b) - 1u;
+    return below_b & ~((1u << a) - 1u);  // a < b <= 32, so a < 32
+}
+
+// Scores of the columns whose bit in vm is clear become -inf; skipped when every
+// lane of the warp sees the whole chunk (the common case inside a tile).
+__device__ __forceinline__ void mask_chunk(uint32_t (&r32)[32], uint32_t vm)
+{
+    if (__all_sync(0xffffffffu, vm == 0xffffffffu))
+        return;
+#pragma unroll
+    for (int c = 0; c < 32; ++c)
+        if (!(vm & (1u << c)))
+            r32[c] = __float_as_uint(-INFINITY);
+}
+
+// Request cursor of the producer's tile walk (tiles are dealt in request order).
+struct Cursor {
+    int r, acc, tr;  // request, tiles of requests < r, tiles of request r
+};
+
+// Describe tile t (the cursor only moves forward): its request, rows and the two key
+// regions; reports a bad request once (on its first tile) and marks it invalid.
+__device__ __forceinline__ void describe(const PrefillParams &p, int ppt, int t, Cursor &cur,
+                                         TileInfo &inf, int &rr)
+{
+    while (t >= cur.acc + cur.tr) {
+        cur.acc += cur.tr;
+        ++cur.r;
+        cur.tr = tiles_of(p, cur.r, ppt);
+    }
+    const int r = cur.r;
+    const int loc = t - cur.acc;
+    const int blk = loc / p.Hkv;
+    inf.h = loc % p.Hkv;
+    inf.i0 = blk * ppt;
+    inf.row_base = __ldg(p.cu_rows + r);
+    inf.C = __ldg(p.cu_rows + r + 1) - inf.row_base;
+    inf.P = __ldg(p.prefix_len + r);
+    const int seq = __ldg(p.seq_idx + r);
+    const bool report = inf.h == 0 && blk == 0;  // one report per request
+    inf.valid = 1;
+    if (inf.row_base < 0 || inf.row_base + inf.C > p.rows) {
+        if (report)
+            set_err(p.dev_err, HSA_DEVERR_BAD_LEN);  // rows outside q / out
+        inf.valid = 0;
+    } else if (seq < 0 || seq >= p.batch) {
+        if (report)
+            set_err(p.dev_err, HSA_DEVERR_BAD_SEQ);
+        inf.valid = 0;
+    } else if (inf.P < 0) {
+        if (report)
+            set_err(p.dev_err, HSA_DEVERR_BAD_LEN);
+        inf.valid = 0;
+    }
+    rr = 0;
+    inf.nr = 0;
+    inf.a0 = 0;
+    if (inf.valid && inf.P > 0 && inf.i0 < p.W - 1) {
+        // some row of the tile still sees the prefix
+        rr = __ldg(p.ring_row + seq);
+        if (rr < 0 || rr >= p.n_ring_rows) {
+            if (report)
+                set_err(p.dev_err, HSA_DEVERR_BAD_RING);  // prefix keys absent
+        } else {
+            inf.a0 = max(0, inf.P + inf.i0 - p.W + 1) & ~(kBox - 1);
+            inf.nr = ((inf.P + kBox - 1) & ~(kBox - 1)) - inf.a0;
+        }
+    }
+    inf.z0 = max(0, inf.i0 - p.W);
+    inf.nc = inf.i0 + ppt - inf.z0;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_swa_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmNK,
+                       const __grid_constant__ CUtensorMap tmNV, const __grid_constant__ CUtensorMap tmRK,
+                       const __grid_constant__ CUtensorMap tmRV, const PrefillParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    SwaSmem &sh = *reinterpret_cast<SwaSmem *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int ppt = kBM / p.G;  // positions per tile
+
+    // ---- tiles of the launch: Hkv x sum_r ceil(C_r / ppt) ------------------------
+    {
+        int local = 0;
+        for (int r = tid; r < p.R; r += kThreads)
+            local += tiles_of(p, r, ppt);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            local += __shfl_xor_sync(0xffffffffu, local, o);
+        if (lane == 0)
+            sh.red[warp] = local;
+        __syncthreads();
+        if (tid == 0) {
+            int t = 0;
+            for (int w = 0; w < kThreads / 32; ++w)
+                t += sh.red[w];
+            sh.total = t;
+        }
+        __syncthreads();
+    }
+    const int total = sh.total;
+    const int n_my = (int)blockIdx.x < total ? (total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    if (n_my == 0)
+        return;  // the whole CTA, before any barrier or TMEM is set up
+
+    if (tid == 0) {
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&sh.full_qk[s], 1);
+            mbar_init(&sh.empty_qk[s], 1);
+            mbar_init(&sh.full_v[s], 1);
+            mbar_init(&sh.empty_v[s], 1);
+            mbar_init(&sh.s_full[s], 1);
+            mbar_init(&sh.p_full[s], 4 * 32);
+            mbar_init(&sh.o_full[s], 1);
+            mbar_init(&sh.t_free[s], 4 * 32);
+        }
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&sh.tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sh.tmem_base;
+
+    if (warp == 0) {
+        // ================================================================ producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tmQ);
+            tma_prefetch_desc(&tmNK);
+            tma_prefetch_desc(&tmNV);
+            tma_prefetch_desc(&tmRK);
+            tma_prefetch_desc(&tmRV);
+            const uint64_t pol_q = policy_evict_first();  // q is read once
+            const uint64_t pol_kv = policy_evict_last();  // a key serves ~W / ppt tiles
+            // Loads go out in the order their stages free up: q + K of tile k (stage
+            // k mod 2 is free once S(k-2) has read it), then V of tile k-1 (free once
+            // PV(k-3) has); a tile's description is read one tile ahead, so its
+            // global loads overlap the waits.
+            Cursor cur{0, 0, tiles_of(p, 0, ppt)};
+            TileInfo inf_next, inf_prev{};
+            int rr_next = 0, rr_prev = 0;
+            describe(p, ppt, (int)blockIdx.x, cur, inf_next, rr_next);
+            bool ok = true;
+            int k = 0;
+            auto load_v = [&](int j, const TileInfo &inf, int rr) -> bool {
+                const int s = j & 1;
+                if (!mbar_wait_sleep(&sh.empty_v[s], ((j >> 1) & 1) ^ 1))
+                    return false;
+                uint64_t *bar = &sh.full_v[s];
+                if (!inf.valid) {
+                    mbar_arrive(bar);
+                    return true;
+                }
+                mbar_arrive_expect_tx(bar, (inf.nr + inf.nc) * 256);
+                for (int b = 0; b < inf.nr; b += kBox) {
+                    const int y = (rr * p.Hkv + inf.h) * p.W + (inf.a0 + b) % p.W;
+                    tma_load_2d(sh.v[s] + b * 128, &tmRV, bar, 0, y, pol_kv);
+                    tma_load_2d(sh.v[s] + kKvHalf + b * 128, &tmRV, bar, 64, y, pol_kv);
+                }
+                for (int b = 0; b < inf.nc; b += kBox) {
+                    const int z = inf.row_base + inf.z0 + b;
+                    const int off = (inf.nr + b) * 128;
+                    tma_load_3d(sh.v[s] + off, &tmNV, bar, 0, inf.h, z, pol_kv);
+                    tma_load_3d(sh.v[s] + kKvHalf + off, &tmNV, bar, 64, inf.h, z, pol_kv);
+                }
+                return true;
+            };
+            for (; k < n_my; ++k) {
+                const TileInfo inf = inf_next;
+                const int rr = rr_next;
+                if (k + 1 < n_my)
+                    describe(p, ppt, (int)blockIdx.x + (k + 1) * (int)gridDim.x, cur, inf_next,
+                             rr_next);
+                const int s = k & 1;
+                if (!mbar_wait_sleep(&sh.empty_qk[s], ((k >> 1) & 1) ^ 1)) {
+                    ok = false;
+                    break;
+                }
+                sh.info[k & 3] = inf;  // released to the consumers by the q + K barrier
+                uint64_t *bar = &sh.full_qk[s];
+                if (!inf.valid) {
+                    mbar_arrive(bar);
+                } else {
+                    mbar_arrive_expect_tx(bar, 2 * kQHalf + (inf.nr + inf.nc) * 256);
+                    // q: ppt positions x the G query heads of KV head h (rows past the
+                    // request are masked; rows past the tensor are zero-filled)
+                    const int qz = inf.row_base + inf.i0;
+                    tma_load_3d(sh.q[s], &tmQ, bar, 0, inf.h * p.G, qz, pol_q);
+                    tma_load_3d(sh.q[s] + kQHalf, &tmQ, bar, 64, inf.h * p.G, qz, pol_q);
+                    // ring region: 16-aligned position blocks -> 16-slot blocks of the ring
+                    for (int b = 0; b < inf.nr; b += kBox) {
+                        const int y = (rr * p.Hkv + inf.h) * p.W + (inf.a0 + b) % p.W;
+                        tma_load_2d(sh.k[s] + b * 128, &tmRK, bar, 0, y, pol_kv);
+                        tma_load_2d(sh.k[s] + kKvHalf + b * 128, &tmRK, bar, 64, y, pol_kv);
+                    }
+                    // chunk region
+                    for (int b = 0; b < inf.nc; b += kBox) {
+                        const int z = inf.row_base + inf.z0 + b;
+                        const int off = (inf.nr + b) * 128;
+                        tma_load_3d(sh.k[s] + off, &tmNK, bar, 0, inf.h, z, pol_kv);
+                        tma_load_3d(sh.k[s] + kKvHalf + off, &tmNK, bar, 64, inf.h, z, pol_kv);
+                    }
+                }
+                if (k > 0 && !load_v(k - 1, inf_prev, rr_prev)) {
+                    ok = false;
+                    break;
+                }
+                inf_prev = inf;
+                rr_prev = rr;
+            }
+            if (ok && n_my > 0 && !load_v(n_my - 1, inf_prev, rr_prev))
+                ok = false;
+            if (!ok)
+                set_err(p.dev_err, HSA_DEVERR_TIMEOUT);
+            // drain: no TMA write may still be in flight when the CTA exits
+            for (int j = max(0, n_my - 2); j < n_my; ++j) {
+                mbar_wait_sleep(&sh.full_qk[j & 1], (j >> 1) & 1);
+                mbar_wait_sleep(&sh.full_v[j & 1], (j >> 1) & 1);
+            }
+        }
+    } else if (warp == 1) {
+        // ================================================================ MMA issuer
+        if (lane == 0) {
+            const uint32_t dhi = smem_desc_sw128_hi(1024);
+            const uint32_t id_pv = idesc_bf16_f32(kBM, kD, 0, 1);
+            uint32_t q_lo[2], k_lo[2], v_lo[2];
+            for (int s = 0; s < 2; ++s) {
+                q_lo[s] = smem_desc_sw128_lo(smem_u32(sh.q[s]), 16);
+                k_lo[s] = smem_desc_sw128_lo(smem_u32(sh.k[s]), 16);
+                v_lo[s] = smem_desc_sw128_lo(smem_u32(sh.v[s]), kKvHalf);
+            }
+            int n_prev = 0;  // keys of the previous tile (0: invalid, no PV)
+            // O_s = P_s V_s over n keys: P from TMEM over S (k-step ks: 16 keys = 8
+            // columns of bf16 pairs), V the MN-major tile (16 key rows = 2048 bytes)
+            auto issue_pv = [&](int s, int n) {
+                const uint32_t base = tmem + s * kSlotCols;
+                if (n > 0) {
+                    tc_mma_ts_k<0>(base + kColO, base, desc_join(v_lo[s], dhi), id_pv);
+                    for (int ks = 1; ks < n / 16; ++ks)
+                        tc_mma_ts_k<1>(base + kColO, base + ks * 8,
+                                       desc_join(v_lo[s] + ks * (2048 >> 4), dhi), id_pv);
+                }
+                tc_commit(&sh.o_full[s]);
+                tc_commit(&sh.empty_v[s]);
+            };
+            bool ok = true;
+            for (int k = 0; k < n_my && ok; ++k) {
+                const int s = k & 1;
+                const uint32_t ph = (k >> 1) & 1;
+                if (!mbar_wait_sleep(&sh.full_qk[s], ph) || !mbar_wait_sleep(&sh.t_free[s], ph ^ 1)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const TileInfo &inf = sh.info[k & 3];
+                const int n = inf.valid ? inf.nr + inf.nc : 0;
+                if (n > 0) {
+                    // S = Q K^T over d = 128 in 8 k-steps of 16 (32 bytes inside a
+                    // 128-byte swizzle row; steps 4-7 in the second 64-column block)
+                    const uint32_t id_s = idesc_bf16_f32(kBM, n, 0, 0);
+                    const uint32_t d = tmem + s * kSlotCols;
+                    tc_mma_ss_k<0>(d, desc_join(q_lo[s], dhi), desc_join(k_lo[s], dhi), id_s);
+#pragma unroll
+                    for (int ks = 1; ks < kD / 16; ++ks) {
+                        const uint32_t oq = (ks >> 2) * (kQHalf >> 4) + (ks & 3) * 2;
+                        const uint32_t okv = (ks >> 2) * (kKvHalf >> 4) + (ks & 3) * 2;
+                        tc_mma_ss_k<1>(d, desc_join(q_lo[s] + oq, dhi), desc_join(k_lo[s] + okv, dhi),
+                                       id_s);
+                    }
+                }
+                tc_commit(&sh.s_full[s]);
+                tc_commit(&sh.empty_qk[s]);  // q and K of stage s are free once S has run
+                if (k > 0) {
+                    const int sp = (k - 1) & 1;
+                    const uint32_t php = ((k - 1) >> 1) & 1;
+                    if (!mbar_wait_sleep(&sh.p_full[sp], php) ||
+                        !mbar_wait_sleep(&sh.full_v[sp], php)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    issue_pv(sp, n_prev);
+                }
+                n_prev = n;
+            }
+            if (ok) {
+                const int sp = (n_my - 1) & 1;
+                const uint32_t php = ((n_my - 1) >> 1) & 1;
+                if (mbar_wait_sleep(&sh.p_full[sp], php) && mbar_wait_sleep(&sh.full_v[sp], php)) {
+                    tc_fence_after();
+                    issue_pv(sp, n_prev);
+                } else {
+                    ok = false;
+                }
+            }
+            if (!ok)
+                set_err(p.dev_err, HSA_DEVERR_TIMEOUT);
+        }
+    } else {
+        // ================================================================ softmax + epilogue
+        const int wg = (warp - 2) >> 2;  // tiles wg, wg + 2, ...
+        const int wq = warp & 3;         // TMEM lane quarter of this warp
+        const int m = wq * 32 + lane;    // query row of the tile: position m / G, head m % G
+        const int u = m / p.G, g = m % p.G;
+        const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
+        for (int k = wg; k < n_my; k += 2) {
+            const int s = k & 1;
+            const uint32_t ph = (k >> 1) & 1;
+            // the q + K barrier orders the producer's tile description before this read
+            if (!mbar_wait_sleep(&sh.full_qk[s], ph) || !mbar_wait_sleep(&sh.s_full[s], ph)) {
+                set_err(p.dev_err, HSA_DEVERR_TIMEOUT);
+                break;
+            }
+            tc_fence_after();
+            const TileInfo inf = sh.info[k & 3];
+            const int i = inf.i0 + u;
+            const bool row_ok = inf.valid && i < inf.C;
+            const uint32_t base = lane_addr + s * kSlotCols;
+            float l = 0.f;
+            if (inf.valid) {
+                const int n = inf.nr + inf.nc;
+                // visible key columns: ring region [rlo, rhi), chunk region [clo, chi)
+                int rlo = 0, rhi = 0, clo = 0, chi = 0;
+                if (row_ok) {
+                    if (inf.nr > 0) {
+                        rlo = max(0, inf.P + i - p.W + 1) - inf.a0;
+                        rhi = max(rlo, inf.P - inf.a0);
+                    }
+                    clo = inf.nr + max(0, i - p.W + 1) - inf.z0;
+                    chi = inf.nr + i + 1 - inf.z0;
+                }
+                // pass 1: the row maximum over its visible keys, four independent
+                // chains of three-input max.  Invisible scores become -inf in the
+                // registers (a 32-bit mask per 32-column chunk); a chunk that every row
+                // of the warp sees whole skips the mask.
+                // The chunks are unrolled (at most kKvRows / 32) with two register
+                // buffers: chunk c + 1's TMEM load is in flight while chunk c is used
+                // (tcgen05.wait::ld waits for every earlier load of the thread).
+                constexpr int kChunks = kKvRows / 32;
+                const int nch = (n + 31) >> 5;
+                uint32_t buf[2][32];
+                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                tmem_ld32(base, buf[0]);
+                tmem_wait_ld();
+#pragma unroll
+                for (int ci = 0; ci < kChunks; ++ci) {
+                    if (ci < nch) {
+                        uint32_t(&r32)[32] = buf[ci & 1];
+                        if (ci + 1 < nch)
+                            tmem_ld32(base + (ci + 1) * 32, buf[(ci + 1) & 1]);
+                        const int c0 = ci * 32;
+                        mask_chunk(r32, range_mask(c0, rlo, rhi) | range_mask(c0, clo, chi));
+#pragma unroll
+                        for (int c = 0; c < 32; c += 8) {
+                            m4[0] = fmax3(m4[0], __uint_as_float(r32[c + 0]), __uint_as_float(r32[c + 1]));
+                            m4[1] = fmax3(m4[1], __uint_as_float(r32[c + 2]), __uint_as_float(r32[c + 3]));
+                            m4[2] = fmax3(m4[2], __uint_as_float(r32[c + 4]), __uint_as_float(r32[c + 5]));
+                            m4[3] = fmax3(m4[3], __uint_as_float(r32[c + 6]), __uint_as_float(r32[c + 7]));
+                        }
+                        tmem_wait_ld();
+                    }
+                }
+                const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                const float mb = mx == -INFINITY ? 0.f : mx * p.scale_log2;
+                // pass 2: P = 2^(s scale log2e - max) as bf16 pairs over S's first
+                // columns (chunk c writes columns 16 c .. 16 c + 15, all read already; a
+                // masked score gives 2^-inf = 0).  The row sum takes the rounded P the
+                // PV MMA uses, in two independent f32x2 accumulators.
+                const uint64_t sc2 = f2_make(p.scale_log2, p.scale_log2);
+                const uint64_t nb2 = f2_make(-mb, -mb);
+                uint64_t acc2[2] = {f2_make(0.f, 0.f), f2_make(0.f, 0.f)};
+                tmem_ld32(base, buf[0]);
+                tmem_wait_ld();
+#pragma unroll
+                for (int ci = 0; ci < kChunks; ++ci) {
+                    if (ci < nch) {
+                        uint32_t(&r32)[32] = buf[ci & 1];
+                        if (ci + 1 < nch)
+                            tmem_ld32(base + (ci + 1) * 32, buf[(ci + 1) & 1]);
+                        const int c0 = ci * 32;
+                        mask_chunk(r32, range_mask(c0, rlo, rhi) | range_mask(c0, clo, chi));
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) {
+                            const uint64_t x2 = f2_fma(f2_make(__uint_as_float(r32[2 * c]),
+                                                               __uint_as_float(r32[2 * c + 1])),
+                                                       sc2, nb2);
+                            float x0, x1;
+                            f2_split(x2, x0, x1);
+                            pk[c] = pack_bf16(fast_exp2(x0), fast_exp2(x1));
+                            acc2[c & 1] = f2_add(acc2[c & 1], f2_make(bf16_lo(pk[c]), bf16_hi(pk[c])));
+                        }
+                        tmem_st16(base + (c0 >> 1), pk);
+                        tmem_wait_ld();
+                    }
+                }
+                {
+                    float a0, a1, b0, b1;
+                    f2_split(acc2[0], a0, a1);
+                    f2_split(acc2[1], b0, b1);
+                    l = (a0 + a1) + (b0 + b1);
+                }
+                tmem_wait_st();
+            }
+            tc_fence_before();
+            mbar_arrive(&sh.p_full[s]);
+            // ---- epilogue: O / l -> bf16 ------------------------------------------
+            if (!mbar_wait_sleep(&sh.o_full[s], ph)) {
+                set_err(p.dev_err, HSA_DEVERR_TIMEOUT);
+                break;
+            }
+            tc_fence_after();
+            if (inf.valid) {
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+                __nv_bfloat16 *dst =
+                    p.out + ((int64_t)(inf.row_base + i) * p.Hq + inf.h * p.G + g) * kD;
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    uint32_t o32[32];
+                    tmem_ld32(base + kColO + c4 * 32, o32);
+                    tmem_wait_ld();
+                    if (row_ok) {
+#pragma unroll
+                        for (int c = 0; c < 32; c += 8) {
+                            uint4 w;
+                            w.x = pack_bf16(__uint_as_float(o32[c + 0]) * inv, __uint_as_float(o32[c + 1]) * inv);
+                            w.y = pack_bf16(__uint_as_float(o32[c + 2]) * inv, __uint_as_float(o32[c + 3]) * inv);
+                            w.z = pack_bf16(__uint_as_float(o32[c + 4]) * inv, __uint_as_float(o32[c + 5]) * inv);
+                            w.w = pack_bf16(__uint_as_float(o32[c + 6]) * inv, __uint_as_float(o32[c + 7]) * inv);
+                            *reinterpret_cast<uint4 *>(dst + c4 * 32 + c) = w;
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&sh.t_free[s]);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+}  // namespace
+
+bool prefill_swa_supported(int W, int G)
+{
+    return G >= 1 && G <= 8 && kBM % G == 0 && W % kBox == 0 && W + kBM / G + kBox <= kKvRows;
+}
+
+cudaError_t launch_prefill_swa(const CUtensorMap &tmQ, const CUtensorMap &tmNK, const CUtensorMap &tmNV,
+                               const CUtensorMap &tmRK, const CUtensorMap &tmRV, const PrefillParams &p,
+                               int sms, cudaStream_t stream)
+{
+    const size_t smem = sizeof(SwaSmem) + 1024;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(prefill_swa_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess)
+            return e;
+        attr_set = true;
+    }
+    // tiles_per_req_bound bounds sum_r ceil(C_r / 128); a tile here holds 128 / G rows
+    const int64_t tiles = ((int64_t)p.rows / (kBM / p.G) + p.R) * p.Hkv;
+    const int64_t ctas = tiles < sms ? tiles : sms;
+    if (ctas <= 0)
+        return cudaSuccess;
+    prefill_swa_kernel<<<(unsigned)ctas, kThreads, smem, stream>>>(tmQ, tmNK, tmNV, tmRK, tmRV, p);
+    return cudaGetLastError();
+}
+
+}  // namespace hsa

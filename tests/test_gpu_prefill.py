@@ -43,13 +43,26 @@ def _run(hsa, inst, layers, pool=None):
     return pool, outs
 
 
+def _where(inst, got, ref):
+    """Where the largest error sits: request, chunk row, head, dim, both values and
+    the number of keys that row attends (for a failure message)."""
+    idx = np.unravel_index(int(np.argmax(np.abs(got - ref))), got.shape)
+    row = int(idx[0])
+    r = int(np.searchsorted(inst.cu_new, row, side="right")) - 1
+    i = row - int(inst.cu_new[r])
+    return ("request %d (prefix %d, chunk %d) row %d head %d dim %d: got %.5f ref %.5f" %
+            (r, int(inst.prefix[r]), int(inst.new[r]), i, int(idx[1]), int(idx[2]),
+             float(got[idx]), float(ref[idx])))
+
+
 def _check(inst, layers, outs, seqs=None):
     for i, l in enumerate(layers):
         c = harness.oracle_case(inst, l, range(inst.R) if seqs is None else seqs)
         ref = oracle.attention(window=0 if inst.full[l] else inst.cfg.W, scale=inst.cfg.scale, **c)
         got = outs[i].float().cpu().numpy()
         err = float(np.max(np.abs(got - ref)))
-        assert err <= TOL, "layer %d (%s): max abs err %g" % (l, "full" if inst.full[l] else "swa", err)
+        assert err <= TOL, "layer %d (%s): max abs err %g at %s" % (
+            l, "full" if inst.full[l] else "swa", err, _where(inst, got, ref))
 
 
 @pytest.mark.parametrize("heads", [(32, 4), (16, 2)])
@@ -57,6 +70,23 @@ def test_prefill_ragged_small(heads):
     hsa = _cuda()
     inst = workload.draw(_cfg([0, 100, 300, 64, 1000], [1, 130, 257, 128, 70], *heads))
     layers = [6, 0]
+    _, outs = _run(hsa, inst, layers)
+    _check(inst, layers, outs)
+
+
+@pytest.mark.parametrize("W,heads", [(128, (32, 4)), (64, (32, 4)), (64, (16, 4)), (64, (8, 4)),
+                                     (128, (16, 4)), (256, (32, 4))])
+def test_prefill_sliding_windows_and_groups(W, heads):
+    """Sliding layers over windows W = 64 / 128 / 256 and GQA groups G = 8 / 4 / 2:
+    prefixes shorter than, equal to and longer than W (ring partly filled, exactly
+    full, wrapped; lengths on and off 16-row boundaries), chunks whose rows cross
+    i = W - 1 (the last row that still sees the prefix) and end on ragged tiles."""
+    hsa = _cuda()
+    cfg = dataclasses.replace(
+        _cfg([0, 1, 17, W - 1, W, W + 1, 1007, 1008], [300, 2 * W + 3, 40, 129, W, 16, 17, 1],
+             *heads, index=84), W=W)
+    inst = workload.draw(cfg)
+    layers = [0, 6]
     _, outs = _run(hsa, inst, layers)
     _check(inst, layers, outs)
 
@@ -108,18 +138,19 @@ def test_prefill_equals_decode_for_single_rows():
 
 def test_prefill_full_size_sampled():
     """8 requests, prefix 16K-128K, chunk 2K-8K (one full and one sliding layer):
-    a seeded sample of (row, head) outputs against the oracle."""
+    every request's rows 0, 127, 128, 255, 256 and its last row (the window and tile
+    edges) plus seeded random rows, a few query heads each, against the oracle."""
     hsa = _cuda()
     inst = workload.draw(workload.CONFIGS["prefill"])
     layers = [6, 0]
     _, outs = _run(hsa, inst, layers)
     rng = np.random.default_rng(2024)
     for i, l in enumerate(layers):
-        seqs = [0, inst.R - 1]
+        seqs = list(range(inst.R))
         rows = []
         for s in seqs:
             a, b = int(inst.cu_new[s]), int(inst.cu_new[s + 1])
-            rows += [a, a + 127, a + 128, b - 1] + rng.integers(a, b, 12).tolist()
+            rows += [a, a + 127, a + 128, a + 255, a + 256, b - 1] + rng.integers(a, b, 4).tolist()
         items = np.array([(r, int(h)) for r in rows for h in rng.integers(0, inst.cfg.Hq, 2)],
                          np.int32)
         c = harness.oracle_case(inst, l, seqs)

@@ -158,3 +158,111 @@ def test_prefill_schedule_covers_every_visible_key():
                             # chunk rows [max(first - P, 0), i]
                             lo_row = max(first - P, 0)
                             assert chunk_lo <= lo_row and i < chunk_hi, (W, ring, P, C, i)
+
+
+# ---------------------------------------------------------------- sliding-window prefill
+KV_ROWS = 160   # prefill_swa.cu: key capacity of a stage
+BOX = 16        # rows per K / V TMA box
+
+
+def _swa_supported(W, G):
+    return 128 % G == 0 and W % BOX == 0 and W + 128 // G + BOX <= KV_ROWS
+
+
+def _swa_tile(P, C, i0, W, G):
+    """prefill_swa.cu producer: the tile's two key regions (ring: first position a0,
+    nr keys; chunk: first chunk row z0, nc keys)."""
+    ppt = 128 // G
+    nr, a0 = 0, 0
+    if P > 0 and i0 < W - 1:
+        a0 = max(0, P + i0 - W + 1) & ~(BOX - 1)
+        nr = ((P + BOX - 1) & ~(BOX - 1)) - a0
+    z0 = max(0, i0 - W)
+    nc = i0 + ppt - z0
+    return a0, nr, z0, nc
+
+
+def _swa_row_ranges(P, C, i, W, a0, nr, z0):
+    """prefill_swa.cu softmax: visible columns [rlo, rhi) of the ring region and
+    [clo, chi) of the chunk region for chunk row i."""
+    rlo = rhi = 0
+    if nr > 0:
+        rlo = max(0, P + i - W + 1) - a0
+        rhi = max(rlo, P - a0)
+    clo = nr + max(0, i - W + 1) - z0
+    chi = nr + i + 1 - z0
+    return rlo, rhi, clo, chi
+
+
+def test_swa_prefill_tiles_cover_each_row_window_exactly():
+    """Every row of every tile sees, through its two column ranges, exactly the
+    positions of its window [max(0, P + i - W + 1), P + i]; the ring region's columns
+    it sees hold exactly those positions (a 16-aligned position block maps onto one
+    16-slot block of the ring, and the ring -- written in position order up to P --
+    holds position p in slot p mod W for every p it sees); both regions fit a stage
+    and every TMA box stays inside the ring row of its (sequence, head)."""
+    rng = random.Random(5)
+    shapes = [(W, G) for W in (64, 128, 192, 256) for G in (1, 2, 4, 8) if _swa_supported(W, G)]
+    assert (128, 8) in shapes and (64, 8) in shapes
+    for W, G in shapes:
+        ppt = 128 // G
+        cases = [(P, C) for P in (0, 1, 15, 16, 17, W - 1, W, W + 1, 1000, 1007, 1008)
+                 for C in (1, 2, 15, 16, 17, W - 1, W, W + 1, 300)]
+        cases += [(rng.randint(0, 5000), rng.randint(1, 700)) for _ in range(200)]
+        for P, C in cases:
+            held = _ring_after(P, W)
+            for i0 in range(0, C, ppt):
+                a0, nr, z0, nc = _swa_tile(P, C, i0, W, G)
+                assert nr % BOX == 0 and nc % BOX == 0 and nr >= 0 and nc > 0
+                assert nr + nc <= KV_ROWS, (W, G, P, C, i0, nr, nc)
+                assert (nr + nc) // 2 <= 128          # P columns stay below O's
+                for b in range(0, nr, BOX):
+                    slot = (a0 + b) % W
+                    assert slot + BOX <= W            # a box never wraps the ring row
+                assert z0 >= 0
+                for i in range(i0, min(i0 + ppt, C)):
+                    rlo, rhi, clo, chi = _swa_row_ranges(P, C, i, W, a0, nr, z0)
+                    assert 0 <= rlo <= rhi <= nr and nr <= clo <= chi <= nr + nc
+                    seen = []
+                    for c in range(nr + nc):
+                        if rlo <= c < rhi:
+                            pos = a0 + c
+                            assert held[pos % W] == pos, (W, P, i, c)
+                            seen.append(pos)
+                        elif clo <= c < chi:
+                            seen.append(P + z0 + (c - nr))
+                    q = P + i
+                    assert seen == list(range(max(0, q - W + 1), q + 1)), (W, G, P, C, i)
+
+
+def test_swa_prefill_tile_walk_matches_the_grid():
+    """The persistent CTAs walk tiles t = cta + k * grid in request order (KV head
+    fastest); the host grid bound Hkv (rows / ppt + R) never drops a tile, and the
+    walk visits every (request, row block, head) exactly once."""
+    rng = random.Random(3)
+    for _ in range(500):
+        G = rng.choice([2, 4, 8])
+        Hkv = rng.choice([1, 2, 4])
+        ppt = 128 // G
+        R = rng.randint(1, 10)
+        C = [rng.choice([0, 1, ppt - 1, ppt, ppt + 1, rng.randint(0, 3000)]) for _ in range(R)]
+        rows = sum(C)
+        tiles = [((c + ppt - 1) // ppt) * Hkv for c in C]
+        total = sum(tiles)
+        bound = (rows // ppt + R) * Hkv
+        assert bound >= total
+        grid = min(bound, rng.choice([1, 7, 152]))
+        seen = []
+        for cta in range(grid):
+            n_my = (total - 1 - cta) // grid + 1 if cta < total else 0
+            r, acc = 0, 0
+            for k in range(n_my):
+                t = cta + k * grid
+                while t >= acc + tiles[r]:
+                    acc += tiles[r]
+                    r += 1
+                loc = t - acc
+                seen.append((r, loc // Hkv, loc % Hkv))
+        want = [(r, b, h) for r, c in enumerate(C) for b in range((c + ppt - 1) // ppt)
+                for h in range(Hkv)]
+        assert sorted(seen) == want
