@@ -312,12 +312,17 @@ class DecodeStep:
     """All layers: decode attention fused with the append of the step's new tokens
     (hsa_decode_attn_append, one launch per layer)."""
 
-    def __init__(self, inst, device, layers=None, swa_prefetch=False, kv_fp8=False):
+    def __init__(self, inst, device, layers=None, swa_prefetch=False, kv_fp8=False,
+                 early_pool_read=True):
         import full_attention_kv_gb300 as hsa
         import harness
         self.hsa = hsa
         self.inst = inst
         self.kv_fp8 = kv_fp8
+        # each layer's attention is queued right behind the previous layer's, which
+        # writes only its own layer's pool: sliding layers may read their ring before
+        # that kernel ends (HSA_DECODE_EARLY_POOL_READ)
+        self.early = early_pool_read
         cfg = inst.cfg
         self.model_layers = list(range(cfg.n_layers)) if layers is None else list(layers)
         self.layers = list(range(len(self.model_layers)))  # pool layer indices
@@ -359,7 +364,8 @@ class DecodeStep:
         # attention fused with the append of the step's new rows (accept-all for T > 1)
         self.hsa.hsa_decode_attn_append(self.pool, l, self.q[l], self.k[l], self.v[l], self.cl,
                                         self.inst.cfg.scale, out=self.out[l], workspace=self.ws,
-                                        dev_err=self.err, stream=stream)
+                                        dev_err=self.err, stream=stream,
+                                        early_pool_read=self.early)
 
     def prefetch_all(self, stream):
         with torch.cuda.stream(stream):
@@ -660,7 +666,7 @@ def measure(args, inst, ws, rank, local, cpu_repeats=None):
     layers = None if args.layers is None else [int(x) for x in args.layers.split(",")]
     if cfg.kind == "decode":
         step = DecodeStep(inst, device, layers, swa_prefetch=args.swa_prefetch,
-                          kv_fp8=args.kv_fp8)
+                          kv_fp8=args.kv_fp8, early_pool_read=not args.no_early_pool_read)
     else:
         step = PrefillStep(inst, device, layers)
     # the attention stream runs at high priority (a side stream, if any, at the default)
@@ -736,6 +742,8 @@ def measure(args, inst, ws, rank, local, cpu_repeats=None):
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": step.launches_per_step * args.steps,
     }
+    if cfg.kind == "decode":
+        line["config"]["early_pool_read"] = step.early
     line.update(extra)
     if args.kv_fp8:
         line["dtype"] = "e4m3 Full KV Pool (fp16 MMA, fp32 accumulate), bf16 rings / q / out"
@@ -851,6 +859,9 @@ def main():
                          "each step, layer by layer on a side stream")
     ap.add_argument("--kv-fp8", action="store_true",
                     help="decode: full layers as an FP8 (E4M3) Full KV Pool (no CPU baseline)")
+    ap.add_argument("--no-early-pool-read", action="store_true",
+                    help="decode: sliding layers wait for the previous kernel before reading "
+                         "their ring (the default reads it early, HSA_DECODE_EARLY_POOL_READ)")
     ap.add_argument("--layers", default=None,
                     help="comma-separated model layers (profiling sub-stack; default all)")
     ap.add_argument("--profile-step", action="store_true",
@@ -858,7 +869,8 @@ def main():
     args = ap.parse_args()
     head_name = args.workload or "decode"
     single = (args.workload is not None or args.swa_prefetch or args.kv_fp8 or
-              args.layers is not None or args.batch is not None or args.profile_step)
+              args.layers is not None or args.batch is not None or args.profile_step or
+              args.no_early_pool_read)
     if args.kv_fp8 and workload.CONFIGS[head_name].kind != "decode":
         ap.error("--kv-fp8 is a decode variant (prefill reads bf16 pools)")
     if args.warmup < 3 and args.impl == "ours":

@@ -18,6 +18,9 @@ HSA_UNSUPPORTED_SHAPE = 2
 HSA_CUDA_ERROR = 3
 HSA_OUT_OF_RANGE = 4
 
+HSA_DECODE_APPEND = 1
+HSA_DECODE_EARLY_POOL_READ = 2
+
 HSA_DEVERR_BAD_BLOCK = 1
 HSA_DEVERR_BAD_PAGE = 2
 HSA_DEVERR_BAD_SEQ = 4
@@ -27,7 +30,8 @@ HSA_DEVERR_TIMEOUT = 32
 
 # every symbol include/hsa.h declares
 EXPORTS = ("hsa_kv_append", "hsa_decode_workspace_bytes", "hsa_decode_attn",
-           "hsa_decode_attn_append", "hsa_decode_attn_noalloc", "hsa_prefill_attn",
+           "hsa_decode_attn_append", "hsa_decode_attn_ex", "hsa_decode_attn_noalloc",
+           "hsa_prefill_attn",
            "hsa_swa_prefetch",
            "hsa_window_safe_len", "hsa_window_safe_len_bitmap", "hsa_status_string")
 # every symbol include/hsa_tree.h declares
@@ -86,6 +90,9 @@ def lib():
         L.hsa_decode_attn_append.restype = ctypes.c_int
         L.hsa_decode_attn_append.argtypes = [pp, i32, vp, vp, vp, vp, i32, i32, f32, vp, vp, sz,
                                              i32, vp, vp]
+        L.hsa_decode_attn_ex.restype = ctypes.c_int
+        L.hsa_decode_attn_ex.argtypes = [pp, i32, vp, vp, vp, vp, i32, i32, f32, vp, vp, sz,
+                                         i32, i32, vp, vp]
         L.hsa_decode_attn_noalloc.restype = ctypes.c_int
         L.hsa_decode_attn_noalloc.argtypes = [pp, i32, vp, vp, vp, vp, i32, i32, f32, vp, i32,
                                               vp, vp]
@@ -323,7 +330,11 @@ def _decode_shapes(pool, q, k_new, v_new, cached_len):
 
 
 def hsa_decode_attn(pool, layer, q, k_new, v_new, cached_len, scale, out=None, workspace=None,
-                    max_ctas=0, dev_err=None, stream=None, append=False):
+                    max_ctas=0, dev_err=None, stream=None, append=False, early_pool_read=False):
+    """Decode attention (hsa_decode_attn; with append=True hsa_decode_attn_append).
+    early_pool_read=True calls hsa_decode_attn_ex with HSA_DECODE_EARLY_POOL_READ: the
+    caller guarantees that the kernel queued just before on the stream does not write
+    cached_len, ring_row or this layer's ring."""
     _need(q, "q", torch.bfloat16, ndim=4)
     _need(k_new, "k_new", torch.bfloat16, ndim=4)
     _need(v_new, "v_new", torch.bfloat16, ndim=4)
@@ -339,20 +350,26 @@ def hsa_decode_attn(pool, layer, q, k_new, v_new, cached_len, scale, out=None, w
     _need(workspace, "workspace", torch.uint8)
     _need_err(dev_err)
     _same_device(q, out, workspace, dev_err)
-    fn = lib().hsa_decode_attn_append if append else lib().hsa_decode_attn
-    s = fn(pool.ref(), int(layer), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(cached_len), B, T,
-           float(scale), _ptr(out), _ptr(workspace), workspace.numel(), int(max_ctas),
-           _ptr(dev_err), _stream(stream))
-    _check("hsa_decode_attn_append" if append else "hsa_decode_attn", s)
+    args = (pool.ref(), int(layer), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(cached_len), B, T,
+            float(scale), _ptr(out), _ptr(workspace), workspace.numel(), int(max_ctas))
+    if early_pool_read:
+        opts = HSA_DECODE_EARLY_POOL_READ | (HSA_DECODE_APPEND if append else 0)
+        name = "hsa_decode_attn_ex"
+        s = lib().hsa_decode_attn_ex(*args, opts, _ptr(dev_err), _stream(stream))
+    else:
+        name = "hsa_decode_attn_append" if append else "hsa_decode_attn"
+        s = getattr(lib(), name)(*args, _ptr(dev_err), _stream(stream))
+    _check(name, s)
     return out
 
 
 def hsa_decode_attn_append(pool, layer, q, k_new, v_new, cached_len, scale, out=None,
-                           workspace=None, max_ctas=0, dev_err=None, stream=None):
+                           workspace=None, max_ctas=0, dev_err=None, stream=None,
+                           early_pool_read=False):
     """Decode attention, then the T new K/V rows of every sequence appended."""
     return hsa_decode_attn(pool, layer, q, k_new, v_new, cached_len, scale, out=out,
                            workspace=workspace, max_ctas=max_ctas, dev_err=dev_err,
-                           stream=stream, append=True)
+                           stream=stream, append=True, early_pool_read=early_pool_read)
 
 
 def hsa_decode_attn_noalloc(pool, layer, q, k_new, v_new, cached_len, scale, out, max_ctas=0,

@@ -70,9 +70,16 @@ constexpr int kMaxStages = 8;
 constexpr int kStageRegion = kFp8Stages * kFp8StageStride > kStages * kStageBytes
                                  ? kFp8Stages * kFp8StageStride
                                  : kStages * kStageBytes;
+// Sliding layers (a unit is at most the ring's two 64-key tiles) run a kernel of
+// their own with two stages: ~107 KB of shared memory and (T <= 2) <= 168 registers
+// a thread, so two CTAs fit on an SM and the next layer's CTAs can be resident --
+// and load their rings -- while this layer's run.
+constexpr int kRingStages = 2;
+constexpr int kRingStageRegion = kRingStages * kStageBytes;
 
-struct SharedStorage {
-    alignas(1024) uint8_t stage[kStageRegion];  // bf16: [K lo|K hi|V lo|V hi] per stage
+template <int kRegion>
+struct SharedStorageT {
+    alignas(1024) uint8_t stage[kRegion];  // bf16: [K lo|K hi|V lo|V hi] per stage
     alignas(16) uint8_t new_k[kNewRows * kD * 2];
     alignas(16) uint8_t new_v[kNewRows * kD * 2];
     alignas(16) float comb[kConsumerWarps][kCombFloats];
@@ -536,14 +543,22 @@ __device__ __forceinline__ void append_unit(const DecodeParams &p, int b, int h,
     }
 }
 
-template <int MT, bool FP8>
-__global__ void __launch_bounds__(kThreads, 1)
+template <bool RING>
+using SharedStorage = SharedStorageT<RING ? kRingStageRegion : kStageRegion>;
+
+// MT: 16-row m-tiles of query rows (1: T <= 2, 2: T = 3, 4); FP8: an FP8 full
+// layer; RING: a sliding layer (its own instantiation with two stages; at MT = 1 it
+// is held to 168 registers so that two CTAs fit on an SM -- at MT = 2 that limit
+// spilled ~170 bytes a thread, so MTP rings keep one CTA an SM).
+template <int MT, bool FP8, bool RING>
+__global__ void __launch_bounds__(kThreads, (RING && MT == 1) ? 2 : 1)
     decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const DecodeParams p)
 {
-    constexpr int NS = FP8 ? kFp8Stages : kStages;
+    static_assert(!(FP8 && RING), "the rings stay bf16");
+    constexpr int NS = RING ? kRingStages : (FP8 ? kFp8Stages : kStages);
     extern __shared__ uint8_t smem_raw[];
-    SharedStorage &sh = *reinterpret_cast<SharedStorage *>(
+    SharedStorage<RING> &sh = *reinterpret_cast<SharedStorage<RING> *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -552,7 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < NS; ++s) {
             mbar_init(&sh.full[s], 1);
             // released by the warps of the stage's owning group: MT (full layers), 2 (rings)
-            mbar_init(&sh.empty[s], (p.flags & kDecodeRing) ? 2 : MT);
+            mbar_init(&sh.empty[s], RING ? 2 : MT);
         }
         fence_barrier_init();
     }
@@ -560,9 +575,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
     }
-    // Everything above touches no global memory that an earlier kernel writes.
-    grid_dependency_wait();
-    grid_launch_dependents();
+    // Everything above touches no global memory that an earlier kernel writes.  With
+    // kDecodeEarly (sliding layers) the item walk and the producer's ring loads below
+    // also run before the wait -- they read cached_len, ring_row and this layer's ring,
+    // which the caller guarantees the kernel just before does not write -- and only
+    // the consumers wait, before they read q / k_new / v_new or write anything.
+    const bool early = RING && (p.flags & kDecodeEarly) != 0;
+    if (!early) {
+        grid_dependency_wait();
+        grid_launch_dependents();
+    }
 
     // ---- locate this CTA's contiguous range of items ------------------------
     {
@@ -603,8 +625,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const int64_t N = (int64_t)sh.total_items * p.Hkv;
     const int64_t C = N < (int64_t)gridDim.x ? N : (int64_t)gridDim.x;
-    if ((int64_t)blockIdx.x >= C)
+    if ((int64_t)blockIdx.x >= C) {
+        if (early)
+            grid_dependency_wait();  // every CTA's exit stays ordered after the previous grid
         return;
+    }
     const int64_t i0 = (int64_t)blockIdx.x * N / C;
     const int64_t i1 = ((int64_t)blockIdx.x + 1) * N / C;
     {
@@ -634,6 +659,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == kConsumerWarps) {
         // ---------------------------------------------------------------- producer
+#ifdef HSA_TEST_WITHHOLD_LOADS
+        // Test-only builds (never the product library): the producer issues no load
+        // and no arrival, so every consumer's first stage wait runs out after
+        // HSA_WAIT_NS and the kernel must flag HSA_DEVERR_TIMEOUT and return.
+        return;
+#endif
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
             Walk w = w0;
@@ -696,10 +727,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     // two run side by side -- MT = 1: two warps per tile, 32 keys each; MT = 2: one
     // warp per m-tile with all 64 keys.
     constexpr int kGroups = kConsumerWarps / MT;
-    static_assert(NS % kGroups == 0 && NS % 2 == 0, "each stage belongs to one group");
-    const bool ring = (p.flags & kDecodeRing) != 0;
-    const int wt = (ring && MT == 1) ? 2 : 1;  // warps per m-tile sharing a tile
-    const int groups = ring ? 2 : kGroups;
+    static_assert(RING ? NS % 2 == 0 : (NS % kGroups == 0 && NS % 2 == 0),
+                  "each stage belongs to one group");
+    constexpr bool ring = RING;
+    constexpr int wt = (ring && MT == 1) ? 2 : 1;  // warps per m-tile sharing a tile
+    constexpr int groups = ring ? 2 : kGroups;
+    if (early) {
+        // the consumers read q / k_new / v_new, which the previous kernel writes
+        grid_dependency_wait();
+        grid_launch_dependents();
+    }
     const int key0 = (slice % wt) * (kTileKeys / wt);
     const int g = lane >> 2, tq = lane & 3;
     const int r0 = mt * 16 + g, r1 = r0 + 8;
@@ -776,13 +813,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int c = w.c;
         const int j = w.j;
         bool any = loaded;
-        if (loaded && !(p.flags & kDecodeRing))
+        if (loaded && !ring)
             any = key0 < c - j * kTileKeys;  // this warp's keys hold a cached position
         if (any) {
             const uint32_t sK = smem_u32(sh.stage + stg * kStageBytes);
             const uint32_t sV = sK + kTileBytes;
             const int W = p.W, T = p.T;
-            const bool ring = (p.flags & kDecodeRing) != 0;
             auto vis = [&](int rr, int key) -> bool {
                 const int t = rr == g ? t0 : t1;
                 if (t >= T)
@@ -965,18 +1001,25 @@ size_t decode_workspace_bytes(int num_sms, int B, int Hkv)
 cudaError_t launch_decode(const CUtensorMap &tmK, const CUtensorMap &tmV, const DecodeParams &p,
                           int ctas, cudaStream_t stream)
 {
-    const size_t smem = sizeof(SharedStorage) + 1024;
     const int MT = (p.G * p.T + 15) / 16;
     const bool fp8 = (p.flags & kDecodeFp8) != 0;
+    const bool ring = (p.flags & kDecodeRing) != 0;
+    const size_t smem = (ring ? sizeof(SharedStorage<true>) : sizeof(SharedStorage<false>)) + 1024;
     // the opt-in shared-memory size is set once per process (the API is not a stream
     // operation, but setting it once keeps graph capture free of extra calls)
-    static bool attr_set[4] = {false, false, false, false};
-    auto k1 = decode_kernel<1, false>;
-    auto k2 = decode_kernel<2, false>;
-    auto f1 = decode_kernel<1, true>;
-    auto f2 = decode_kernel<2, true>;
-    auto kern = fp8 ? (MT == 1 ? f1 : f2) : (MT == 1 ? k1 : k2);
-    const int which = (fp8 ? 2 : 0) + MT - 1;
+    static bool attr_set[6] = {false, false, false, false, false, false};
+    void (*kern)(CUtensorMap, CUtensorMap, DecodeParams);
+    int which;
+    if (ring) {
+        kern = MT == 1 ? decode_kernel<1, false, true> : decode_kernel<2, false, true>;
+        which = 4 + MT - 1;
+    } else if (fp8) {
+        kern = MT == 1 ? decode_kernel<1, true, false> : decode_kernel<2, true, false>;
+        which = 2 + MT - 1;
+    } else {
+        kern = MT == 1 ? decode_kernel<1, false, false> : decode_kernel<2, false, false>;
+        which = MT - 1;
+    }
     if (!attr_set[which]) {
         cudaError_t e =
             cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -179,6 +179,34 @@ hsa_status hsa_decode_attn_append(const hsa_pools *pools, int32_t layer, const v
                                   int32_t *dev_err, void *stream);
 
 /*
+ * Decode attention with options (a bit mask; other bits give HSA_INVALID_ARG):
+ *  HSA_DECODE_APPEND           append the new rows as hsa_decode_attn_append does.
+ *  HSA_DECODE_EARLY_POOL_READ  sliding layers: the kernel starts reading cached_len,
+ *      ring_row and this layer's ring before the kernel queued just before it on
+ *      `stream` has finished.  The decode kernels are launched with programmatic
+ *      dependent launch: they may start once the previous kernel signals its
+ *      dependents (this library's decode kernels signal at their start), and they
+ *      read q, k_new, v_new and write out / the pools only after it has completed.
+ *      With this option the caller guarantees that the kernel just before does not
+ *      write cached_len, ring_row or this layer's ring: in a model that kernel is the
+ *      layer's QKV projection (it writes q, k_new, v_new only); in a run of decode
+ *      calls layer after layer it is the previous layer's attention.  A kernel that
+ *      does not signal its dependents early (hsa_kv_append, for one) has completed
+ *      before this one starts, so it may write anything.  The option lets the next
+ *      layer's ring loads overlap the current layer's kernel (two sliding-layer CTAs
+ *      fit on an SM for T <= 2).  Results are those of the same call without it.
+ *      Full layers ignore it.
+ * Same arguments and results as hsa_decode_attn otherwise.
+ */
+#define HSA_DECODE_APPEND 1
+#define HSA_DECODE_EARLY_POOL_READ 2
+hsa_status hsa_decode_attn_ex(const hsa_pools *pools, int32_t layer, const void *q,
+                              const void *k_new, const void *v_new, const int32_t *cached_len,
+                              int32_t B, int32_t T, float scale, void *out, void *workspace,
+                              size_t ws_bytes, int32_t max_ctas, int32_t options,
+                              int32_t *dev_err, void *stream);
+
+/*
  * hsa_decode_attn without a caller workspace.  The pages have no counterpart: this
  * is a convenience of this library for callers that cannot allocate device memory
  * where they run decode (while a stream is being captured, inside a host runtime

@@ -233,3 +233,24 @@ def test_noalloc_unit_cap_is_refused_on_the_host():
         hsa.HSA_UNSUPPORTED_SHAPE
     assert na(p, 0, 256, 256, 256, 256, 1025, 1, 0.1, 256, 0, None, None) == \
         hsa.HSA_UNSUPPORTED_SHAPE
+
+
+def test_decode_ex_options_are_checked_on_the_host():
+    """hsa_decode_attn_ex accepts only the documented option bits (append, early
+    pool read); any other bit, and every malformed pool or argument the other decode
+    entry points refuse, is refused before any CUDA call."""
+    import full_attention_kv_gb300 as hsa
+    L = hsa.lib()
+    ex = L.hsa_decode_attn_ex
+    p = ctypes.byref(_pools(hsa))
+    for bad in (4, 8, 1 << 30, -1):
+        assert ex(p, 0, 256, 256, 256, 256, 1, 1, 0.1, 256, 256, 1 << 20, 0, bad, None,
+                  None) == hsa.HSA_INVALID_ARG
+    for opts in (0, hsa.HSA_DECODE_APPEND, hsa.HSA_DECODE_EARLY_POOL_READ, 3):
+        assert ex(p, 0, 256, 256, 256, 256, 1, 5, 0.1, 256, 256, 1 << 20, 0, opts, None,
+                  None) == hsa.HSA_UNSUPPORTED_SHAPE
+        assert ex(p, 0, None, None, None, None, 0, 1, 0.1, None, None, 0, 0, opts, None,
+                  None) == hsa.HSA_OK
+    bad = ctypes.byref(_pools(hsa, W=96))
+    assert ex(bad, 0, 256, 256, 256, 256, 1, 1, 0.1, 256, 256, 1 << 20, 0, 2, None,
+              None) == hsa.HSA_UNSUPPORTED_SHAPE

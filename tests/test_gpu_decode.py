@@ -261,3 +261,68 @@ def test_fused_append_matches_attention_then_append(T, max_ctas):
         c = harness.oracle_case(inst, l, range(B))
         refo = oracle.attention(window=0 if inst.full[l] else cfg.W, scale=cfg.scale, **c)
         assert np.max(np.abs(out.float().cpu().numpy().reshape(refo.shape) - refo)) <= TOL
+
+
+def _extended_case(inst, layer, k1, v1, q2, k2, v2, T):
+    """Oracle inputs for a second decode step on `layer`: the history of every
+    sequence extended by the T rows (k1, v1) the first step appended, and the second
+    step's new rows.  Histories come from the generator, never from a pool."""
+    c = harness.oracle_case(inst, layer, range(inst.R))
+    B = inst.R
+    hk, hv, off = [], [], [0]
+    for s in range(B):
+        a, b = int(c["hist_off"][s]), int(c["hist_off"][s + 1])
+        hk.append(torch.cat([c["hist_k"][a:b], k1[s].cpu()]))
+        hv.append(torch.cat([c["hist_v"][a:b], v1[s].cpu()]))
+        off.append(off[-1] + hk[-1].shape[0])
+    return dict(cu_rows=c["cu_rows"], prefix_len=inst.prefix + T,
+                q=q2.reshape(B * T, inst.cfg.Hq, inst.cfg.d).cpu(),
+                k_new=k2.reshape(B * T, inst.cfg.Hkv, inst.cfg.d).cpu(),
+                v_new=v2.reshape(B * T, inst.cfg.Hkv, inst.cfg.d).cpu(),
+                hist_k=torch.cat(hk), hist_v=torch.cat(hv), hist_off=np.array(off, np.int64),
+                hist_start=c["hist_start"])
+
+
+@pytest.mark.parametrize("T", [1, 2, 4])
+def test_early_pool_read_equals_plain_and_ordering_holds(T):
+    """HSA_DECODE_EARLY_POOL_READ on sliding layers.
+
+    (1) Queued right after a fused decode + append on another sliding layer (a
+    kernel that signals its dependents early and writes that layer's ring), the
+    early decode of layer B gives bit for bit the result of B's decode without the
+    option.  (2) The hazard the option must not be used for, checked without it: a
+    fused decode + append on layer A, then at once A's next decode step (cached
+    length + T) -- the second call must see the rows the first just wrote (the
+    oracle's history includes them)."""
+    hsa = _cuda()
+    cfg = dataclasses.replace(workload.CONFIGS["tiny"], Hq=32, Hkv=4, T=T,
+                              contexts=(0, 1, 63, 126, 127, 128, 700, 5000, 130, 255),
+                              B=10, index=60 + T)
+    inst = workload.draw(cfg)
+    layers = [0, 1]  # both sliding
+    pool = harness.make_pool(inst, layers)
+    qa, ka, va, cl = harness.decode_inputs(inst, 0)
+    qb, kb, vb, _ = harness.decode_inputs(inst, 1)
+    ref_b = hsa.hsa_decode_attn(pool, 1, qb, kb, vb, cl, cfg.scale)
+    torch.cuda.synchronize()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for _ in range(3):
+        # (1) ring A written just before; B read early
+        hsa.hsa_decode_attn_append(pool, 0, qa, ka, va, cl, cfg.scale, dev_err=err)
+        out_b = hsa.hsa_decode_attn(pool, 1, qb, kb, vb, cl, cfg.scale, dev_err=err,
+                                    early_pool_read=True)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        assert torch.equal(out_b, ref_b)
+    # (2) A's ring now holds the appended rows at c .. c+T-1; the next step on A,
+    # queued right behind a fused append on A, without the option
+    pool2 = harness.make_pool(inst, layers)
+    q2, k2, v2, _ = harness.decode_inputs(inst, 1)  # stand-ins for the next step's rows
+    hsa.hsa_decode_attn_append(pool2, 0, qa, ka, va, cl, cfg.scale, dev_err=err)
+    out2 = hsa.hsa_decode_attn(pool2, 0, q2, k2, v2, cl + T, cfg.scale, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ref2 = oracle.attention(window=cfg.W, scale=cfg.scale,
+                            **_extended_case(inst, 0, ka, va, q2, k2, v2, T))
+    got = out2.float().cpu().numpy().reshape(ref2.shape)
+    assert np.max(np.abs(got - ref2)) <= TOL
