@@ -46,8 +46,8 @@ def _stale(target, deps):
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def _compile(src, extra):
-    obj = os.path.join(OUT_DIR, os.path.basename(src) + ".o")
+def _compile(src, extra, out_dir=OUT_DIR):
+    obj = os.path.join(out_dir, os.path.basename(src) + ".o")
     if not _stale(obj, [src] + _headers()):
         return obj, ""
     cmd = [nvcc()] + ARCH + NVCC_FLAGS + extra + ["-c", src, "-o", obj]
@@ -57,30 +57,39 @@ def _compile(src, extra):
     return obj, r.stderr
 
 
-def build(force: bool = False, verbose_ptxas: bool = False) -> str:
-    os.makedirs(OUT_DIR, exist_ok=True)
+def build(force: bool = False, verbose_ptxas: bool = False, out_dir: str = None,
+          defines=()) -> str:
+    """Compile and link the library; returns its path.
+
+    out_dir / defines build a variant elsewhere (a test-only build with other
+    compile-time settings, e.g. a short HSA_WAIT_NS); the product library is
+    ``_build/libhsa.so`` with no extra defines."""
+    out = OUT_DIR if out_dir is None else out_dir
+    lib = os.path.join(out, "libhsa.so")
+    os.makedirs(out, exist_ok=True)
     srcs = _sources()
     if force:
-        for o in glob.glob(os.path.join(OUT_DIR, "*.o")):
+        for o in glob.glob(os.path.join(out, "*.o")):
             os.remove(o)
     extra = ["-Xptxas", "-v"] if verbose_ptxas else []
+    extra += ["-D" + d for d in defines]
     with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
-        results = list(ex.map(lambda s: _compile(s, extra), srcs))
+        results = list(ex.map(lambda s: _compile(s, extra, out), srcs))
     objs = [o for o, _ in results]
     if verbose_ptxas:
         for o, log in results:
             if log:
                 sys.stderr.write(log)
-    if force or _stale(LIB, objs):
-        tmp = LIB + ".tmp%d" % os.getpid()
+    if force or _stale(lib, objs):
+        tmp = lib + ".tmp%d" % os.getpid()
         # cudart is linked statically; the driver API (tensor-map encoding) is reached
         # through cudaGetDriverEntryPointByVersion, so libcuda is not a link dependency
         cmd = [nvcc()] + ARCH + ["-shared", "-o", tmp] + objs
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError("link failed:\n%s\n%s" % (" ".join(cmd), r.stderr))
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

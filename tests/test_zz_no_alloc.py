@@ -47,6 +47,33 @@ def test_noalloc_matches_workspace_entry_twice(T):
             assert diff <= TOL, "layer %d call %d: %g" % (l, call, diff)
 
 
+def test_noalloc_caps_ctas_on_a_wide_sliding_layer():
+    """64 sequences x 4 KV heads = 256 sliding-layer units: hsa_decode_attn gives each
+    its own CTA, while the fixed scratch holds partial slots for about 250 CTAs, so
+    the no-workspace call caps the grid and some rings are split across CTAs and
+    merged through the scratch.  Both calls must agree, twice in a row."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import full_attention_kv_gb300 as hsa
+    hsa.lib()
+    ctx = tuple((37 * b) % 300 for b in range(64))  # short contexts: 0 .. 299
+    cfg = dataclasses.replace(workload.CONFIGS["tiny"], Hq=32, Hkv=4, T=1, contexts=ctx, B=64,
+                              index=97)
+    inst = workload.draw(cfg)
+    layers = [0]
+    pool = harness.make_pool(inst, layers)
+    q, k, v, cl = harness.decode_inputs(inst, 0)
+    ref = hsa.hsa_decode_attn(pool, 0, q, k, v, cl, cfg.scale)
+    for call in range(2):
+        out = torch.full_like(q, float("nan"))
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        hsa.hsa_decode_attn_noalloc(pool, 0, q, k, v, cl, cfg.scale, out, dev_err=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        diff = torch.max(torch.abs(out.float() - ref.float())).item()
+        assert diff <= TOL, "call %d: %g" % (call, diff)
+
+
 def test_noalloc_rejects_too_many_units():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
