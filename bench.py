@@ -313,7 +313,7 @@ class DecodeStep:
     (hsa_decode_attn_append, one launch per layer)."""
 
     def __init__(self, inst, device, layers=None, swa_prefetch=False, kv_fp8=False,
-                 early_pool_read=True):
+                 early_pool_read=True, swa_prefetch_frac=1.0):
         import full_attention_kv_gb300 as hsa
         import harness
         self.hsa = hsa
@@ -335,11 +335,18 @@ class DecodeStep:
         if swa_prefetch:
             self.host_k = {i: self.pool.k[i].cpu().pin_memory() for i in self.swa}
             self.host_v = {i: self.pool.v[i].cpu().pin_memory() for i in self.swa}
-            self.host_rows = torch.from_numpy(inst.ring_row).to(device)
-            self.seqs = torch.arange(inst.R, dtype=torch.int32, device=device)
+            # the sequences whose rings come back from the host tier each step: all of
+            # them, or a seeded fraction (requests returning to a cached conversation)
+            n = max(1, int(round(swa_prefetch_frac * inst.R)))
+            seqs = (np.arange(inst.R) if n >= inst.R else
+                    np.sort(np.random.default_rng(inst.cfg.seed).choice(inst.R, n, replace=False)))
+            self.host_rows = torch.from_numpy(inst.ring_row[seqs].astype(np.int32)).to(device)
+            self.seqs = torch.from_numpy(seqs.astype(np.int32)).to(device)
             self.side = torch.cuda.Stream(device, priority=0)  # below the attention stream
             self.ready = {i: torch.cuda.Event() for i in self.swa}
-            self.prefetch_bytes = sum(t.numel() * t.element_size() * 2 for t in self.host_k.values())
+            ring_bytes = cfg.Hkv * cfg.W * cfg.d * 2 * 2  # K and V of one sequence's ring
+            self.prefetch_bytes = len(seqs) * ring_bytes * len(self.swa)
+            self.prefetch_frac = len(seqs) / inst.R
         self.q, self.k, self.v = [], [], []
         for l in self.model_layers:
             q, k, v, cl = harness.decode_inputs(inst, l, device)
@@ -666,7 +673,8 @@ def measure(args, inst, ws, rank, local, cpu_repeats=None):
     layers = None if args.layers is None else [int(x) for x in args.layers.split(",")]
     if cfg.kind == "decode":
         step = DecodeStep(inst, device, layers, swa_prefetch=args.swa_prefetch,
-                          kv_fp8=args.kv_fp8, early_pool_read=not args.no_early_pool_read)
+                          kv_fp8=args.kv_fp8, early_pool_read=not args.no_early_pool_read,
+                          swa_prefetch_frac=args.swa_prefetch_frac)
     else:
         step = PrefillStep(inst, device, layers)
     # the attention stream runs at high priority (a side stream, if any, at the default)
@@ -751,8 +759,9 @@ def measure(args, inst, ws, rank, local, cpu_repeats=None):
                                     "(token, KV head) row; sliding rings bf16")
     if prefetch_info is not None:
         line["swa_prefetch"] = prefetch_info
-        line["config"]["swa_prefetch"] = ("every step reloads all sliding layers' rings from a "
-                                          "pinned host tier on a side stream, layer by layer")
+        line["config"]["swa_prefetch"] = ("every step reloads the sliding layers' rings of %.0f%% "
+                                          "of the sequences from a pinned host tier on a side "
+                                          "stream, layer by layer" % (100 * step.prefetch_frac))
     del graph, step
     gc.collect()
     torch.cuda.empty_cache()
@@ -857,6 +866,9 @@ def main():
     ap.add_argument("--swa-prefetch", action="store_true",
                     help="decode: reload every sliding layer's rings from pinned host memory "
                          "each step, layer by layer on a side stream")
+    ap.add_argument("--swa-prefetch-frac", type=float, default=1.0,
+                    help="with --swa-prefetch: the seeded fraction of sequences whose rings "
+                         "come back each step (default: all)")
     ap.add_argument("--kv-fp8", action="store_true",
                     help="decode: full layers as an FP8 (E4M3) Full KV Pool (no CPU baseline)")
     ap.add_argument("--no-early-pool-read", action="store_true",

@@ -499,9 +499,12 @@ __device__ __forceinline__ void append_unit_fp8(const DecodeParams &p, int b, in
 }
 
 // Append the T new K/V rows of unit (b, h) to this layer's pool or ring.  Called by
-// the CTA that completes the unit, after every read of the unit has finished.
+// the CTA that completes the unit, after every read of the unit has finished.  With
+// new_k / new_v (the rows this CTA staged in shared memory, bf16, 128-byte swizzle)
+// the rows are copied from there instead of being read again from k_new / v_new.
 __device__ __forceinline__ void append_unit(const DecodeParams &p, int b, int h, int c, int tid,
-                                            int nthreads)
+                                            int nthreads, const uint8_t *new_k = nullptr,
+                                            const uint8_t *new_v = nullptr)
 {
     constexpr int kChunks = kD * 2 / 16;  // 16-byte chunks per row
     const int total = 2 * p.T * kChunks;
@@ -536,10 +539,15 @@ __device__ __forceinline__ void append_unit(const DecodeParams &p, int b, int h,
             }
             dst_row = ((int64_t)blk * p.Hkv + h) * kTileKeys + pos % kTileKeys;
         }
-        const int64_t src = ((int64_t)(b * p.T + t) * p.Hkv + h) * kChunks + ch;
-        const uint4 *from = reinterpret_cast<const uint4 *>(kv ? p.v_new : p.k_new);
         uint4 *to = kv ? p.v_dst : p.k_dst;
-        to[dst_row * kChunks + ch] = __ldg(from + src);
+        if (new_k) {
+            to[dst_row * kChunks + ch] = *reinterpret_cast<const uint4 *>(
+                (kv ? new_v : new_k) + swz128_offset(t, ch * 8, kNewRows));
+        } else {
+            const int64_t src = ((int64_t)(b * p.T + t) * p.Hkv + h) * kChunks + ch;
+            const uint4 *from = reinterpret_cast<const uint4 *>(kv ? p.v_new : p.k_new);
+            to[dst_row * kChunks + ch] = __ldg(from + src);
+        }
     }
 }
 
@@ -674,6 +682,17 @@ __global__ void __launch_bounds__(kThreads, (RING && MT == 1) ? 2 : 1)
             // stage, so its latency hides behind the wait
             int64_t row = i0 < i1 ? tile_row(p, w, true) : -1;
             for (int64_t i = i0; i < i1; ++i, ++k) {
+                if (early && (w.j == 0 || i == i0)) {
+                    // before the grid-dependency wait: pull the unit's q rows and new
+                    // K / V rows towards L2 (a hint; the consumers read them after it)
+                    const int Hq = p.G * p.Hkv;
+                    for (int t = 0; t < p.T; ++t) {
+                        const int64_t r = (int64_t)w.b * p.T + t;
+                        prefetch_l2(p.q + (r * Hq + (int64_t)w.h * p.G) * kD, p.G * kD * 2);
+                        prefetch_l2(p.k_new + (r * p.Hkv + w.h) * kD, kD * 2);
+                        prefetch_l2(p.v_new + (r * p.Hkv + w.h) * kD, kD * 2);
+                    }
+                }
                 const int st = (int)(k % NS);
                 const uint32_t ph = (uint32_t)((k / NS) & 1);
                 if (!mbar_wait(&sh.empty[st], ph ^ 1)) {
@@ -932,10 +951,11 @@ __global__ void __launch_bounds__(kThreads, (RING && MT == 1) ? 2 : 1)
             }
         }
         if (whole && (p.flags & kDecodeAppend)) {
+            // a whole unit's new rows were staged by this CTA (it owns the last tile)
             if constexpr (FP8)
                 append_unit_fp8(p, cur.b, cur.h, cur.c, warp, lane, kConsumerWarps);
             else
-                append_unit(p, cur.b, cur.h, cur.c, tid, kConsumerWarps * 32);
+                append_unit(p, cur.b, cur.h, cur.c, tid, kConsumerWarps * 32, sh.new_k, sh.new_v);
         }
         if (!whole) {
             // count this part in; the last CTA of the unit merges every part
