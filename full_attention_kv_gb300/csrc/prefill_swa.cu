@@ -29,12 +29,14 @@
 //    At most W + 128/G + 16 keys (160 for W = 128, G = 8), so S = Q K^T is one MMA
 //    chain of N <= 160 columns and each row's softmax is exact: the row maximum is
 //    known before any exponential, no running max, no rescale of O.
-//  * Two shared-memory stages (q, K, V of one tile) and two TMEM slots (S, P, O of
-//    one tile); tile n uses stage and slot n mod 2.  Warp 0 = TMA producer; warp 1 =
-//    TMEM owner and single-thread MMA issuer; warps 2-5 / 6-9 = softmax and epilogue
-//    of the even / odd tiles, one query row per thread (TMEM lane = row).  The MMA
-//    thread issues S(n) and then PV(n-1), so the tensor cores run one tile while the
-//    other tile's warps compute softmax or write their output.
+//  * Two shared-memory stages (q + K, and V, of one tile, each freed as soon as the
+//    MMA that reads it has run) and two TMEM slots (S, P, O of one tile); tile n uses
+//    stage and slot n mod 2.  Warp 0 = TMA producer; warp 1 = TMEM owner and
+//    single-thread MMA issuer (S(n), then PV(n-1)); warps 2-5 = softmax and epilogue,
+//    one query row per thread (TMEM lane = row): the softmax of tile n reads the
+//    row's scores from TMEM once and keeps them in registers for both passes (six
+//    warps, so 255 registers a thread), then the epilogue of tile n - 1 runs while
+//    PV(n) is on the tensor cores.
 //  * TMEM slot (256 columns): S at [0, N); P as bf16 pairs over S's first N/2
 //    columns; O at [128, 256), written by the PV MMA once the softmax has read all of
 //    S.  The epilogue divides O by the row sum (of the bf16 P the MMA used) and
@@ -51,7 +53,7 @@ constexpr int kKvRows = 160;               // key capacity of a stage
 constexpr int kBox = 16;                   // rows per K / V TMA box
 constexpr int kQHalf = kBM * 128;          // 128 rows x 64 bf16 (one swizzle column block)
 constexpr int kKvHalf = kKvRows * 128;
-constexpr int kThreads = 320;
+constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSlotCols = 256;
 constexpr uint32_t kColO = 128;
@@ -73,10 +75,16 @@ struct SwaSmem {
     // stage s: q + K loaded / free (free once S has read them), V loaded / free
     alignas(8) uint64_t full_qk[2], empty_qk[2], full_v[2], empty_v[2];
     uint64_t s_full[2], p_full[2], o_full[2], t_free[2];  // per TMEM slot
-    // description of tile k in info[k mod 4]: the producer writes tile k + 4's once
-    // stage k mod 2 frees for it, i.e. after S(k + 2), which waits for tile k's
-    // epilogue -- so no slot is overwritten while its tile's warps may still read it
+    // description of tile k in info[k mod 4], published by info_full[k mod 4]: the
+    // producer writes tile k + 4's once stage k mod 2 frees for it, i.e. after
+    // S(k + 2), which waits for tile k's epilogue -- so no slot is overwritten while
+    // its tile's warps may still read it, and its barrier cannot complete the next
+    // phase before they have waited on this one.  (The softmax warps must not wait on
+    // full_qk for this: that barrier completes again for tile k + 2 as soon as S(k)
+    // has read stage k mod 2, possibly before a late waiter looks, and a parity wait
+    // cannot tell two completions from none.)
     TileInfo info[4];
+    uint64_t info_full[4];
     uint32_t tmem_base;
     int32_t total;
     int32_t red[kThreads / 32];
@@ -219,6 +227,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&sh.o_full[s], 1);
             mbar_init(&sh.t_free[s], 4 * 32);
         }
+        for (int j = 0; j < 4; ++j)
+            mbar_init(&sh.info_full[j], 1);
         fence_barrier_init();
     }
     if (warp == 1) {
@@ -284,7 +294,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = false;
                     break;
                 }
-                sh.info[k & 3] = inf;  // released to the consumers by the q + K barrier
+                sh.info[k & 3] = inf;
+                mbar_arrive(&sh.info_full[k & 3]);  // publishes it to the softmax warps
                 uint64_t *bar = &sh.full_qk[s];
                 if (!inf.valid) {
                     mbar_arrive(bar);
@@ -406,143 +417,155 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ================================================================ softmax + epilogue
-        const int wg = (warp - 2) >> 2;  // tiles wg, wg + 2, ...
-        const int wq = warp & 3;         // TMEM lane quarter of this warp
-        const int m = wq * 32 + lane;    // query row of the tile: position m / G, head m % G
+        // Warps 2-5 (one per TMEM lane quarter), one query row per thread, every tile
+        // in turn: the softmax of tile k, then the epilogue of tile k - 1 while PV(k)
+        // runs on the tensor cores.
+        const int wq = warp & 3;       // TMEM lane quarter of this warp
+        const int m = wq * 32 + lane;  // query row of the tile: position m / G, head m % G
         const int u = m / p.G, g = m % p.G;
         const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
-        for (int k = wg; k < n_my; k += 2) {
-            const int s = k & 1;
-            const uint32_t ph = (k >> 1) & 1;
-            // the q + K barrier orders the producer's tile description before this read
-            if (!mbar_wait_sleep(&sh.full_qk[s], ph) || !mbar_wait_sleep(&sh.s_full[s], ph)) {
-                set_err(p.dev_err, HSA_DEVERR_TIMEOUT);
-                break;
-            }
-            tc_fence_after();
-            const TileInfo inf = sh.info[k & 3];
-            const int i = inf.i0 + u;
-            const bool row_ok = inf.valid && i < inf.C;
-            const uint32_t base = lane_addr + s * kSlotCols;
+        TileInfo prev{};
+        float prev_l = 0.f;
+        bool ok = true;
+        for (int k = 0; k <= n_my && ok; ++k) {
             float l = 0.f;
-            if (inf.valid) {
-                const int n = inf.nr + inf.nc;
-                // visible key columns: ring region [rlo, rhi), chunk region [clo, chi)
-                int rlo = 0, rhi = 0, clo = 0, chi = 0;
-                if (row_ok) {
-                    if (inf.nr > 0) {
-                        rlo = max(0, inf.P + i - p.W + 1) - inf.a0;
-                        rhi = max(rlo, inf.P - inf.a0);
-                    }
-                    clo = inf.nr + max(0, i - p.W + 1) - inf.z0;
-                    chi = inf.nr + i + 1 - inf.z0;
+            TileInfo inf{};
+            if (k < n_my) {
+                const int s = k & 1;
+                const uint32_t ph = (k >> 1) & 1;
+                if (!mbar_wait_sleep(&sh.info_full[k & 3], (k >> 2) & 1) ||
+                    !mbar_wait_sleep(&sh.s_full[s], ph)) {
+                    ok = false;
+                    break;
                 }
-                // pass 1: the row maximum over its visible keys, four independent
-                // chains of three-input max.  Invisible scores become -inf in the
-                // registers (a 32-bit mask per 32-column chunk); a chunk that every row
-                // of the warp sees whole skips the mask.
-                // The chunks are unrolled (at most kKvRows / 32) with two register
-                // buffers: chunk c + 1's TMEM load is in flight while chunk c is used
-                // (tcgen05.wait::ld waits for every earlier load of the thread).
-                constexpr int kChunks = kKvRows / 32;
-                const int nch = (n + 31) >> 5;
-                uint32_t buf[2][32];
-                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-                tmem_ld32(base, buf[0]);
-                tmem_wait_ld();
-#pragma unroll
-                for (int ci = 0; ci < kChunks; ++ci) {
-                    if (ci < nch) {
-                        uint32_t(&r32)[32] = buf[ci & 1];
-                        if (ci + 1 < nch)
-                            tmem_ld32(base + (ci + 1) * 32, buf[(ci + 1) & 1]);
-                        const int c0 = ci * 32;
-                        mask_chunk(r32, range_mask(c0, rlo, rhi) | range_mask(c0, clo, chi));
-#pragma unroll
-                        for (int c = 0; c < 32; c += 8) {
-                            m4[0] = fmax3(m4[0], __uint_as_float(r32[c + 0]), __uint_as_float(r32[c + 1]));
-                            m4[1] = fmax3(m4[1], __uint_as_float(r32[c + 2]), __uint_as_float(r32[c + 3]));
-                            m4[2] = fmax3(m4[2], __uint_as_float(r32[c + 4]), __uint_as_float(r32[c + 5]));
-                            m4[3] = fmax3(m4[3], __uint_as_float(r32[c + 6]), __uint_as_float(r32[c + 7]));
+                tc_fence_after();
+                inf = sh.info[k & 3];
+                const int i = inf.i0 + u;
+                const bool row_ok = inf.valid && i < inf.C;
+                const uint32_t base = lane_addr + s * kSlotCols;
+                if (inf.valid) {
+                    const int n = inf.nr + inf.nc;
+                    // visible key columns: ring region [rlo, rhi), chunk region [clo, chi)
+                    int rlo = 0, rhi = 0, clo = 0, chi = 0;
+                    if (row_ok) {
+                        if (inf.nr > 0) {
+                            rlo = max(0, inf.P + i - p.W + 1) - inf.a0;
+                            rhi = max(rlo, inf.P - inf.a0);
                         }
-                        tmem_wait_ld();
+                        clo = inf.nr + max(0, i - p.W + 1) - inf.z0;
+                        chi = inf.nr + i + 1 - inf.z0;
                     }
-                }
-                const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-                const float mb = mx == -INFINITY ? 0.f : mx * p.scale_log2;
-                // pass 2: P = 2^(s scale log2e - max) as bf16 pairs over S's first
-                // columns (chunk c writes columns 16 c .. 16 c + 15, all read already; a
-                // masked score gives 2^-inf = 0).  The row sum takes the rounded P the
-                // PV MMA uses, in two independent f32x2 accumulators.
-                const uint64_t sc2 = f2_make(p.scale_log2, p.scale_log2);
-                const uint64_t nb2 = f2_make(-mb, -mb);
-                uint64_t acc2[2] = {f2_make(0.f, 0.f), f2_make(0.f, 0.f)};
-                tmem_ld32(base, buf[0]);
-                tmem_wait_ld();
+                    // The row's n <= kKvRows scores: one TMEM read of every chunk, then a
+                    // single wait, kept in registers for both passes (a TMEM read's
+                    // latency is paid once a tile).  Invisible scores become -inf (a
+                    // 32-bit mask per chunk; a chunk every row of the warp sees whole
+                    // skips it).
+                    constexpr int kChunks = kKvRows / 32;
+                    const int nch = (n + 31) >> 5;
+                    uint32_t sr[kChunks][32];
 #pragma unroll
-                for (int ci = 0; ci < kChunks; ++ci) {
-                    if (ci < nch) {
-                        uint32_t(&r32)[32] = buf[ci & 1];
-                        if (ci + 1 < nch)
-                            tmem_ld32(base + (ci + 1) * 32, buf[(ci + 1) & 1]);
-                        const int c0 = ci * 32;
-                        mask_chunk(r32, range_mask(c0, rlo, rhi) | range_mask(c0, clo, chi));
-                        uint32_t pk[16];
+                    for (int ci = 0; ci < kChunks; ++ci)
+                        if (ci < nch)
+                            tmem_ld32(base + ci * 32, sr[ci]);
+                    tmem_wait_ld();
+                    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                        for (int c = 0; c < 16; ++c) {
-                            const uint64_t x2 = f2_fma(f2_make(__uint_as_float(r32[2 * c]),
-                                                               __uint_as_float(r32[2 * c + 1])),
-                                                       sc2, nb2);
-                            float x0, x1;
-                            f2_split(x2, x0, x1);
-                            pk[c] = pack_bf16(fast_exp2(x0), fast_exp2(x1));
-                            acc2[c & 1] = f2_add(acc2[c & 1], f2_make(bf16_lo(pk[c]), bf16_hi(pk[c])));
+                    for (int ci = 0; ci < kChunks; ++ci) {
+                        if (ci < nch) {
+                            const int c0 = ci * 32;
+                            mask_chunk(sr[ci], range_mask(c0, rlo, rhi) | range_mask(c0, clo, chi));
+#pragma unroll
+                            for (int c = 0; c < 32; c += 8) {
+                                m4[0] = fmax3(m4[0], __uint_as_float(sr[ci][c + 0]), __uint_as_float(sr[ci][c + 1]));
+                                m4[1] = fmax3(m4[1], __uint_as_float(sr[ci][c + 2]), __uint_as_float(sr[ci][c + 3]));
+                                m4[2] = fmax3(m4[2], __uint_as_float(sr[ci][c + 4]), __uint_as_float(sr[ci][c + 5]));
+                                m4[3] = fmax3(m4[3], __uint_as_float(sr[ci][c + 6]), __uint_as_float(sr[ci][c + 7]));
+                            }
                         }
-                        tmem_st16(base + (c0 >> 1), pk);
-                        tmem_wait_ld();
                     }
-                }
-                {
+                    const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                    const float mb = mx == -INFINITY ? 0.f : mx * p.scale_log2;
+                    // P = 2^(s scale log2e - max) as bf16 pairs over S's first columns
+                    // (chunk c writes columns 16 c .. 16 c + 15; a masked score gives
+                    // 2^-inf = 0).  The row sum takes the rounded P the PV MMA uses, in
+                    // two independent f32x2 accumulators.
+                    const uint64_t sc2 = f2_make(p.scale_log2, p.scale_log2);
+                    const uint64_t nb2 = f2_make(-mb, -mb);
+                    uint64_t acc2[2] = {f2_make(0.f, 0.f), f2_make(0.f, 0.f)};
+#pragma unroll
+                    for (int ci = 0; ci < kChunks; ++ci) {
+                        if (ci < nch) {
+                            uint32_t pk[16];
+#pragma unroll
+                            for (int c = 0; c < 16; ++c) {
+                                const uint64_t x2 = f2_fma(f2_make(__uint_as_float(sr[ci][2 * c]),
+                                                                   __uint_as_float(sr[ci][2 * c + 1])),
+                                                           sc2, nb2);
+                                float x0, x1;
+                                f2_split(x2, x0, x1);
+                                pk[c] = pack_bf16(fast_exp2(x0), fast_exp2(x1));
+                                acc2[c & 1] = f2_add(acc2[c & 1], f2_make(bf16_lo(pk[c]), bf16_hi(pk[c])));
+                            }
+                            tmem_st16(base + ci * 16, pk);
+                        }
+                    }
                     float a0, a1, b0, b1;
                     f2_split(acc2[0], a0, a1);
                     f2_split(acc2[1], b0, b1);
                     l = (a0 + a1) + (b0 + b1);
+                    tmem_wait_st();
                 }
-                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&sh.p_full[s]);
             }
-            tc_fence_before();
-            mbar_arrive(&sh.p_full[s]);
-            // ---- epilogue: O / l -> bf16 ------------------------------------------
-            if (!mbar_wait_sleep(&sh.o_full[s], ph)) {
-                set_err(p.dev_err, HSA_DEVERR_TIMEOUT);
-                break;
-            }
-            tc_fence_after();
-            if (inf.valid) {
-                const float inv = l > 0.f ? 1.f / l : 0.f;
-                __nv_bfloat16 *dst =
-                    p.out + ((int64_t)(inf.row_base + i) * p.Hq + inf.h * p.G + g) * kD;
+            // ---- epilogue of tile k - 1: O / l -> bf16 ---------------------------
+            if (k > 0) {
+                const int j = k - 1;
+                const int s = j & 1;
+                if (!mbar_wait_sleep(&sh.o_full[s], (j >> 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (prev.valid) {
+                    const int i = prev.i0 + u;
+                    const bool row_ok = i < prev.C;
+                    const float inv = prev_l > 0.f ? 1.f / prev_l : 0.f;
+                    const uint32_t base = lane_addr + s * kSlotCols + kColO;
+                    __nv_bfloat16 *dst =
+                        p.out + ((int64_t)(prev.row_base + i) * p.Hq + prev.h * p.G + g) * kD;
+                    // two halves of 64 columns (128 at once would share the registers
+                    // the softmax holds and spill)
 #pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) {
-                    uint32_t o32[32];
-                    tmem_ld32(base + kColO + c4 * 32, o32);
-                    tmem_wait_ld();
-                    if (row_ok) {
+                    for (int hf = 0; hf < 2; ++hf) {
+                        uint32_t o32[2][32];
+                        tmem_ld32(base + hf * 64, o32[0]);
+                        tmem_ld32(base + hf * 64 + 32, o32[1]);
+                        tmem_wait_ld();
+                        if (row_ok) {
 #pragma unroll
-                        for (int c = 0; c < 32; c += 8) {
-                            uint4 w;
-                            w.x = pack_bf16(__uint_as_float(o32[c + 0]) * inv, __uint_as_float(o32[c + 1]) * inv);
-                            w.y = pack_bf16(__uint_as_float(o32[c + 2]) * inv, __uint_as_float(o32[c + 3]) * inv);
-                            w.z = pack_bf16(__uint_as_float(o32[c + 4]) * inv, __uint_as_float(o32[c + 5]) * inv);
-                            w.w = pack_bf16(__uint_as_float(o32[c + 6]) * inv, __uint_as_float(o32[c + 7]) * inv);
-                            *reinterpret_cast<uint4 *>(dst + c4 * 32 + c) = w;
+                            for (int c2 = 0; c2 < 2; ++c2) {
+#pragma unroll
+                                for (int c = 0; c < 32; c += 8) {
+                                    uint4 w;
+                                    w.x = pack_bf16(__uint_as_float(o32[c2][c + 0]) * inv, __uint_as_float(o32[c2][c + 1]) * inv);
+                                    w.y = pack_bf16(__uint_as_float(o32[c2][c + 2]) * inv, __uint_as_float(o32[c2][c + 3]) * inv);
+                                    w.z = pack_bf16(__uint_as_float(o32[c2][c + 4]) * inv, __uint_as_float(o32[c2][c + 5]) * inv);
+                                    w.w = pack_bf16(__uint_as_float(o32[c2][c + 6]) * inv, __uint_as_float(o32[c2][c + 7]) * inv);
+                                    *reinterpret_cast<uint4 *>(dst + hf * 64 + c2 * 32 + c) = w;
+                                }
+                            }
                         }
                     }
                 }
+                tc_fence_before();
+                mbar_arrive(&sh.t_free[s]);
             }
-            tc_fence_before();
-            mbar_arrive(&sh.t_free[s]);
+            prev = inf;
+            prev_l = l;
         }
+        if (!ok)
+            set_err(p.dev_err, HSA_DEVERR_TIMEOUT);
     }
 
     tc_fence_before();

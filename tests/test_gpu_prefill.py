@@ -35,11 +35,13 @@ def _cfg(prefixes, chunks, Hq=32, Hkv=4, index=80):
 def _run(hsa, inst, layers, pool=None):
     pool = pool or harness.make_pool(inst, layers)
     outs = []
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
     for i, l in enumerate(layers):
         q, k, v, cu, pl, seq = harness.prefill_inputs(inst, l)
         outs.append(hsa.hsa_prefill_attn(pool, i, q, k, v, cu, pl, seq, int(inst.new.max()),
-                                         inst.cfg.scale))
+                                         inst.cfg.scale, dev_err=err))
     torch.cuda.synchronize()
+    assert int(err.item()) == 0, "device error bits %d" % int(err.item())
     return pool, outs
 
 
@@ -89,6 +91,27 @@ def test_prefill_sliding_windows_and_groups(W, heads):
     layers = [0, 6]
     _, outs = _run(hsa, inst, layers)
     _check(inst, layers, outs)
+
+
+def test_prefill_sliding_many_tiles_per_cta():
+    """Three requests of 2.5K-5K rows (about 17 sliding-kernel tiles per CTA, across
+    request boundaries; one request without a prefix): every barrier phase of the
+    persistent kernel's pipeline wraps several times.  Sampled rows at the window and
+    tile edges of every request against the oracle, and no device error."""
+    hsa = _cuda()
+    cfg = _cfg([20000, 300, 0], [3000, 5000, 2500], index=85)
+    inst = workload.draw(cfg)
+    layers = [0]
+    _, outs = _run(hsa, inst, layers)
+    rows = []
+    for r in range(inst.R):
+        a, b = int(inst.cu_new[r]), int(inst.cu_new[r + 1])
+        rows += [a + i for i in (0, 1, 15, 16, 127, 128, 129, 1500, b - a - 17, b - a - 1)]
+    items = np.array([(ri, h) for ri in rows for h in (0, 7, 8, 31)], np.int32)
+    c = harness.oracle_case(inst, 0, range(inst.R))
+    ref = oracle.attention(window=cfg.W, scale=cfg.scale, items=items, **c)
+    got = outs[0].float().cpu().numpy()[items[:, 0], items[:, 1]]
+    assert float(np.max(np.abs(got - ref))) <= TOL
 
 
 def test_prefill_multi_tile_prefix_and_chunk():
