@@ -820,6 +820,8 @@ TRAFFIC = {
     ("mtp", "full"): ("decode.cu", "8968219e5757c4b2", 11701335556),
     # prefill_kernel, full layer: 4.552 GB on 2 requests, scaled by flops
     ("prefill", "full"): ("prefill.cu", "0e97e900cd7e5029", 14340211242),
+    # prefill_swa_kernel, sliding layer: full-size launch
+    ("prefill", "sliding"): ("prefill_swa.cu", "487bd58bef03179b", 809082368),
     # append_kernel, full-size launches (writes still held in L2 at the kernel's end
     # reach DRAM after it)
     ("prefill", "append_full"): ("append.cu", "5b0ffb5eddb0d066", 146275328),

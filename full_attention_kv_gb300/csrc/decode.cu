@@ -83,6 +83,8 @@ struct SharedStorageT {
     alignas(16) uint8_t new_k[kNewRows * kD * 2];
     alignas(16) uint8_t new_v[kNewRows * kD * 2];
     alignas(16) float comb[kConsumerWarps][kCombFloats];
+    float mscale[kMaxRows][kConsumerWarps];  // merge: each slice's weight per row
+    float mrow[kMaxRows][2];                 // merge: each row's combined max and sum
     alignas(8) uint64_t full[kMaxStages];
     alignas(8) uint64_t empty[kMaxStages];
     int32_t tile_ok[kMaxStages];  // the producer loaded the stage's tile (else: masked)
@@ -156,20 +158,6 @@ __device__ __forceinline__ int64_t tile_row(const DecodeParams &p, const Walk &w
         return -1;
     }
     return ((int64_t)blk * p.Hkv + w.h) * kTileKeys;
-}
-
-// Position held by key k (0..63) of tile j, or -1 if that key is not cached.
-__device__ __forceinline__ int key_pos(const DecodeParams &p, int c, int j, int k)
-{
-    int s = j * kTileKeys + k;
-    if (!(p.flags & kDecodeRing))
-        return s < c ? s : -1;
-    // ring: slot s holds the latest position below c congruent to s mod W
-    int back = (c - 1 - s) % p.W;
-    if (back < 0)
-        back += p.W;
-    int pos = c - 1 - back;
-    return pos;  // may be negative: never written
 }
 
 // Per-warp attention state for one m-tile of 16 query rows.
@@ -838,14 +826,19 @@ __global__ void __launch_bounds__(kThreads, (RING && MT == 1) ? 2 : 1)
             const uint32_t sK = smem_u32(sh.stage + stg * kStageBytes);
             const uint32_t sV = sK + kTileBytes;
             const int W = p.W, T = p.T;
+            // ring slot s holds position c - 1 - back(s), back(s) = (r0 - s) mod W with
+            // r0 = (c - 1) mod W (one modulo a tile, not one a key); query row t sees it
+            // iff back(s) <= c - 1 - max(0, c + t - W + 1)
+            const int r0 = ring ? (c - 1) % W : 0;
             auto vis = [&](int rr, int key) -> bool {
                 const int t = rr == g ? t0 : t1;
                 if (t >= T)
                     return false;
-                const int pos = key_pos(p, c, j, key);
-                if (pos < 0)
-                    return false;
-                return !ring || pos >= c + t - W + 1;
+                const int slot = j * kTileKeys + key;
+                if (!ring)
+                    return slot < c;
+                const int back = r0 - slot + (slot > r0 ? W : 0);
+                return back <= c - 1 - max(0, c + t - W + 1);
             };
             // full layers: every key of a complete page is visible to every query
             const bool all_vis = !ring && (j + 1) * kTileKeys <= c;
@@ -919,35 +912,69 @@ __global__ void __launch_bounds__(kThreads, (RING && MT == 1) ? 2 : 1)
             slot = 2 * (int)blockIdx.x + (i0 < unit_start ? 1 : 0);  // 1 = CTA's last unit
         constexpr int kSlices = kConsumerWarps / MT;
         float *part = ws_part + (int64_t)(slot < 0 ? 0 : slot) * kPartFloats;
-        for (int e = tid; e < MT * 16 * kD; e += kConsumerWarps * 32) {
-            const int rr = e / kD, dim = e % kD;
+        // (a) per row: the combined max M, sum L and each slice's weight 2^(m_s - M)
+        // (with 1 / L folded in for a unit written straight to out)
+        for (int rr = tid; rr < MT * 16; rr += kConsumerWarps * 32) {
             const int m_t = rr / 16, rl = rr % 16;
             float M = -INFINITY;
 #pragma unroll
             for (int s = 0; s < kSlices; ++s)
                 M = fmaxf(M, sh.comb[m_t + MT * s][rl]);
             const float base = M == -INFINITY ? 0.f : M;
-            float L = 0.f, O = 0.f;
+            float a[kSlices], L = 0.f;
 #pragma unroll
             for (int s = 0; s < kSlices; ++s) {
-                const float *cb = sh.comb[m_t + MT * s];
-                const float a = fast_exp2(cb[rl] - base);
-                L += cb[16 + rl] * a;
-                O += cb[32 + rl * kD + dim] * a;
+                a[s] = fast_exp2(sh.comb[m_t + MT * s][rl] - base);
+                L += sh.comb[m_t + MT * s][16 + rl] * a[s];
             }
+            const float norm = whole ? (L > 0.f ? 1.f / L : 0.f) : 1.f;
+#pragma unroll
+            for (int s = 0; s < kSlices; ++s)
+                sh.mscale[rr][s] = a[s] * norm;
+            sh.mrow[rr][0] = M;
+            sh.mrow[rr][1] = L;
+        }
+        named_bar_sync(1, kConsumerWarps * 32);
+        // (b) eight output dimensions a thread: O = sum_s o_s * weight_s, written as
+        // 16 bytes of bf16 (a whole unit) or two 16-byte fp32 partials (a split one)
+        for (int e = tid; e < MT * 16 * (kD / 8); e += kConsumerWarps * 32) {
+            const int rr = e / (kD / 8), d0 = (e % (kD / 8)) * 8;
             if (rr >= rows_valid)
                 continue;
+            const int m_t = rr / 16, rl = rr % 16;
+            float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int s = 0; s < kSlices; ++s) {
+                const float w = sh.mscale[rr][s];
+                const float4 *src =
+                    reinterpret_cast<const float4 *>(&sh.comb[m_t + MT * s][32 + rl * kD + d0]);
+                const float4 x = src[0], y = src[1];
+                o[0] += x.x * w;
+                o[1] += x.y * w;
+                o[2] += x.z * w;
+                o[3] += x.w * w;
+                o[4] += y.x * w;
+                o[5] += y.y * w;
+                o[6] += y.z * w;
+                o[7] += y.w * w;
+            }
             if (whole) {
                 const int t = rr / p.G, hh = rr % p.G;
-                const float val = L > 0.f ? O / L : 0.f;
-                p.out[((int64_t)(cur.b * p.T + t) * Hq + cur.h * p.G + hh) * kD + dim] =
-                    __float2bfloat16_rn(val);
+                uint4 v;
+                v.x = pack_bf16(o[0], o[1]);
+                v.y = pack_bf16(o[2], o[3]);
+                v.z = pack_bf16(o[4], o[5]);
+                v.w = pack_bf16(o[6], o[7]);
+                *reinterpret_cast<uint4 *>(
+                    p.out + ((int64_t)(cur.b * p.T + t) * Hq + cur.h * p.G + hh) * kD + d0) = v;
             } else {
-                if (dim == 0) {
-                    __stcg(part + rr, M);
-                    __stcg(part + kMaxRows + rr, L);
+                if (d0 == 0) {
+                    __stcg(part + rr, sh.mrow[rr][0]);
+                    __stcg(part + kMaxRows + rr, sh.mrow[rr][1]);
                 }
-                __stcg(part + 2 * kMaxRows + rr * kD + dim, O);
+                float4 *dst = reinterpret_cast<float4 *>(part + 2 * kMaxRows + rr * kD + d0);
+                __stcg(dst, make_float4(o[0], o[1], o[2], o[3]));
+                __stcg(dst + 1, make_float4(o[4], o[5], o[6], o[7]));
             }
         }
         if (whole && (p.flags & kDecodeAppend)) {
