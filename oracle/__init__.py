@@ -67,11 +67,17 @@ def lib():
         L.orc_e4m3_encode.argtypes = [ctypes.c_float]
         L.orc_quantize_e4m3.restype = None
         L.orc_quantize_e4m3.argtypes = [ctypes.c_int64, ctypes.c_int, u16p, u8p, fp]
-        L.orc_attention_fp8hist.restype = ctypes.c_int
-        L.orc_attention_fp8hist.argtypes = [
+        L.orc_e5m2_value.restype = ctypes.c_double
+        L.orc_e5m2_value.argtypes = [ctypes.c_uint8]
+        L.orc_e5m2_encode.restype = ctypes.c_uint8
+        L.orc_e5m2_encode.argtypes = [ctypes.c_float]
+        L.orc_quantize_e5m2.restype = None
+        L.orc_quantize_e5m2.argtypes = [ctypes.c_int64, ctypes.c_int, u16p, u8p, fp]
+        L.orc_attention_fp8hist_fmt.restype = ctypes.c_int
+        L.orc_attention_fp8hist_fmt.argtypes = [
             ctypes.c_int, i32p, i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
             u16p, u16p, u16p, u8p, fp, u8p, fp, i64p, ctypes.c_int64, i32p, i32p, dp,
-            ctypes.c_int]
+            ctypes.c_int, ctypes.c_int]
         _lib = L
     return _lib
 
@@ -226,7 +232,7 @@ def kv_ratio(layer_is_full, W, L):
     return kv_bytes(layer_is_full, W, L, 1.0) / kv_bytes([1] * n, W, L, 1.0)
 
 
-# ---------------------------------------------------------------- FP8 KV (E4M3)
+# ---------------------------------------------------------------- FP8 KV (E4M3, E5M2)
 # hotdry.top "MiMo inference optimization, edge deployment": FP8 KV with
 # quantisation groups aligned to the window; one fp32 scale per (position, KV
 # head) row here.  Arithmetic in hsa_oracle.c.
@@ -241,8 +247,43 @@ def e4m3_encode(x):
     return int(lib().orc_e4m3_encode(float(np.float32(x))))
 
 
+def e5m2_value(code):
+    """Value of one E5M2 code (OCP 8-bit float, bias 15, infinities at 0x7C / 0xFC)."""
+    return float(lib().orc_e5m2_value(int(code) & 0xFF))
+
+
+def e5m2_encode(x):
+    """Nearest finite E5M2 code of a float32 value (ties to even, saturating)."""
+    return int(lib().orc_e5m2_encode(float(np.float32(x))))
+
+
+FP8_FORMATS = ("e4m3", "e5m2")
+
+
+def fp8_value(code, fmt="e4m3"):
+    """Value of one code of an FP8 format ("e4m3" or "e5m2")."""
+    return e5m2_value(code) if fmt == "e5m2" else e4m3_value(code)
+
+
+def quantize_e5m2(rows):
+    """bf16 rows [..., d] -> (E5M2 codes uint8 [..., d], scales float32 [...]):
+    scale = amax / 57344 per row."""
+    return _quantize(rows, lib().orc_quantize_e5m2)
+
+
+def quantize_fp8(rows, fmt="e4m3"):
+    """quantize_e4m3 or quantize_e5m2 by format name."""
+    if fmt not in FP8_FORMATS:
+        raise ValueError("unknown FP8 format %r" % (fmt,))
+    return quantize_e5m2(rows) if fmt == "e5m2" else quantize_e4m3(rows)
+
+
 def quantize_e4m3(rows):
     """bf16 rows [..., d] -> (codes uint8 [..., d], scales float32 [...])."""
+    return _quantize(rows, lib().orc_quantize_e4m3)
+
+
+def _quantize(rows, fn):
     xb = bf16_bits(rows)
     shape = xb.shape
     d = shape[-1]
@@ -251,16 +292,18 @@ def quantize_e4m3(rows):
     codes = np.zeros((max(n, 1), d), np.uint8)
     scales = np.zeros(max(n, 1), np.float32)
     if n:
-        lib().orc_quantize_e4m3(n, d, _p(flat, ctypes.c_uint16), _p(codes, ctypes.c_uint8),
-                                _p(scales, ctypes.c_float))
+        fn(n, d, _p(flat, ctypes.c_uint16), _p(codes, ctypes.c_uint8), _p(scales, ctypes.c_float))
     return codes[:n].reshape(shape), scales[:n].reshape(shape[:-1])
 
 
 def attention_fp8hist(cu_rows, prefix_len, q, k_new, v_new, hk, hks, hv, hvs, hist_off, scale,
-                      items=None, nthreads=None):
+                      items=None, nthreads=None, fmt="e4m3"):
     """Full causal attention of new rows over an FP8 history (codes + scales,
     dequantised exactly in float64) followed by the bf16 new rows.  History of
-    request r: rows hist_off[r]:hist_off[r+1] = positions 0 .. prefix_len[r]-1."""
+    request r: rows hist_off[r]:hist_off[r+1] = positions 0 .. prefix_len[r]-1.
+    fmt names the codes' format ("e4m3" or "e5m2")."""
+    if fmt not in FP8_FORMATS:
+        raise ValueError("unknown FP8 format %r" % (fmt,))
     L = lib()
     qb, kb, vb = bf16_bits(q), bf16_bits(k_new), bf16_bits(v_new)
     rows, Hq, d = qb.shape
@@ -287,12 +330,12 @@ def attention_fp8hist(cu_rows, prefix_len, q, k_new, v_new, hk, hks, hv, hvs, hi
             return out
     nt = num_threads() if nthreads is None else int(nthreads)
     fp = ctypes.c_float
-    rc = L.orc_attention_fp8hist(
+    rc = L.orc_attention_fp8hist_fmt(
         R, _p(cu, ctypes.c_int32), _p(pl, ctypes.c_int32), Hq, Hkv, d, float(scale),
         _p(qb, ctypes.c_uint16), _p(kb, ctypes.c_uint16), _p(vb, ctypes.c_uint16),
         _p(hk, ctypes.c_uint8), _p(hks, fp), _p(hv, ctypes.c_uint8), _p(hvs, fp),
         _p(ho, ctypes.c_int64), n, _p(ir, ctypes.c_int32), _p(ih, ctypes.c_int32),
-        _p(out, ctypes.c_double), nt)
+        _p(out, ctypes.c_double), 1 if fmt == "e5m2" else 0, nt)
     if rc != 0:
         raise ValueError("oracle fp8 attention failed: %d" % rc)
     return out

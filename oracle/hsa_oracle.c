@@ -401,18 +401,77 @@ void orc_quantize_e4m3(int64_t rows, int d, const uint16_t *x, uint8_t *codes, f
     }
 }
 
+/* E5M2 (OCP 8-bit floating point), the second FP8 format [P5 "KV Cache 量化策略的
+ * 技术选型" weighs both]: sign bit, 5 exponent bits with bias 15, 2 mantissa bits,
+ * subnormals at exponent field 0; exponent field 31 holds the infinities (mantissa
+ * 0) and the NaNs; the largest finite magnitude is 57344.  Reading: the same row
+ * groups as E4M3, scale = amax / 57344, code = E5M2 of x / scale (round to nearest
+ * even, saturating to the largest finite magnitude).                          */
+double orc_e5m2_value(uint8_t c)
+{
+    const int e = (c >> 2) & 31, m = c & 3;
+    double v;
+    if (e == 31)
+        v = m == 0 ? INFINITY : NAN;
+    else
+        v = e == 0 ? ldexp((double)m / 4.0, -14) : ldexp(1.0 + (double)m / 4.0, e - 15);
+    return (c & 0x80) ? -v : v;
+}
+
+/* Nearest finite E5M2 code (ties to the even mantissa, saturating): plain search
+ * over the 124 non-negative finite codes.                                      */
+uint8_t orc_e5m2_encode(float x)
+{
+    const double a = fabs((double)x);
+    int best = 0;
+    double best_err = INFINITY;
+    for (int c = 0; c <= 123; ++c) {
+        const double err = fabs(orc_e5m2_value((uint8_t)c) - a);
+        if (err < best_err || (err == best_err && (c & 1) == 0 && (best & 1) == 1)) {
+            best = c;
+            best_err = err;
+        }
+    }
+    return (uint8_t)(signbit(x) ? (best | 0x80) : best);
+}
+
+/* Quantise rows of d bf16 values to E5M2: codes [rows, d], scales [rows].     */
+void orc_quantize_e5m2(int64_t rows, int d, const uint16_t *x, uint8_t *codes, float *scales)
+{
+    for (int64_t r = 0; r < rows; ++r) {
+        float amax = 0.0f;
+        for (int c = 0; c < d; ++c) {
+            const float v = fabsf((float)bf16_to_double(x[r * d + c]));
+            if (v > amax)
+                amax = v;
+        }
+        const float scale = amax / 57344.0f;
+        scales[r] = amax > 0.0f ? scale : 0.0f;
+        for (int c = 0; c < d; ++c) {
+            const float v = (float)bf16_to_double(x[r * d + c]);
+            codes[r * d + c] = amax > 0.0f ? orc_e5m2_encode(v / scale) : 0;
+        }
+    }
+}
+
+/* Value of a code of format fmt (0 = E4M3, 1 = E5M2).                          */
+static double fp8_value(uint8_t c, int fmt)
+{
+    return fmt ? orc_e5m2_value(c) : orc_e4m3_value(c);
+}
+
 /* attend_row for an FP8 history: keys / values with index < n_hist are
  * (codes, scale) rows dequantised exactly to double; the rest are bf16 rows.   */
 static void attend_row_fp8(const double *q, int d, double scale, int nkeys, int n_hist,
                            const uint8_t *const *kc, const float *ks, const uint8_t *const *vc,
                            const float *vs, const uint16_t *const *krow,
-                           const uint16_t *const *vrow, double *score, double *out)
+                           const uint16_t *const *vrow, int fmt, double *score, double *out)
 {
     double mx = -INFINITY;
     for (int j = 0; j < nkeys; ++j) {
         double s = 0.0;
         for (int c = 0; c < d; ++c)
-            s += q[c] * (j < n_hist ? orc_e4m3_value(kc[j][c]) * (double)ks[j]
+            s += q[c] * (j < n_hist ? fp8_value(kc[j][c], fmt) * (double)ks[j]
                                     : bf16_to_double(krow[j][c]));
         s *= scale;
         score[j] = s;
@@ -429,7 +488,7 @@ static void attend_row_fp8(const double *q, int d, double scale, int nkeys, int 
     for (int j = 0; j < nkeys; ++j) {
         const double w = score[j] / den;
         for (int c = 0; c < d; ++c)
-            out[c] += w * (j < n_hist ? orc_e4m3_value(vc[j][c]) * (double)vs[j]
+            out[c] += w * (j < n_hist ? fp8_value(vc[j][c], fmt) * (double)vs[j]
                                       : bf16_to_double(vrow[j][c]));
     }
 }
@@ -440,17 +499,18 @@ static void attend_row_fp8(const double *q, int d, double scale, int nkeys, int 
  * cached positions, history rows hist_off[r] .. hist_off[r+1]-1 holding positions
  * 0 .. prefix_len[r]-1 as codes [rows, Hkv, d] with scales [rows, Hkv]; its new
  * rows cu_rows[r] .. cu_rows[r+1]-1 (bf16) sit at positions prefix_len[r] + i.
- * Items as in orc_attention.  Returns 0, -1 if an asked row's request lacks its
- * history, or -2 on bad arguments.
+ * fmt: 0 = E4M3 codes, 1 = E5M2.  Items as in orc_attention.  Returns 0, -1 if an
+ * asked row's request lacks its history, or -2 on bad arguments.
  */
-int orc_attention_fp8hist(int R, const int32_t *cu_rows, const int32_t *prefix_len, int Hq,
-                          int Hkv, int d, double scale, const uint16_t *q,
-                          const uint16_t *k_new, const uint16_t *v_new, const uint8_t *hk,
-                          const float *hks, const uint8_t *hv, const float *hvs,
-                          const int64_t *hist_off, int64_t n_items, const int32_t *item_row,
-                          const int32_t *item_head, double *out, int nthreads)
+int orc_attention_fp8hist_fmt(int R, const int32_t *cu_rows, const int32_t *prefix_len,
+                              int Hq, int Hkv, int d, double scale, const uint16_t *q,
+                              const uint16_t *k_new, const uint16_t *v_new, const uint8_t *hk,
+                              const float *hks, const uint8_t *hv, const float *hvs,
+                              const int64_t *hist_off, int64_t n_items,
+                              const int32_t *item_row, const int32_t *item_head, double *out,
+                              int fmt, int nthreads)
 {
-    if (R < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || d <= 0)
+    if (R < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || d <= 0 || (fmt != 0 && fmt != 1))
         return -2;
     const int group = Hq / Hkv;
     const int64_t rows = cu_rows[R];
@@ -511,7 +571,7 @@ int orc_attention_fp8hist(int R, const int32_t *cu_rows, const int32_t *prefix_l
             }
             for (int c = 0; c < d; ++c)
                 qd[c] = bf16_to_double(q[(row * Hq + h) * d + c]);
-            attend_row_fp8(qd, d, scale, nk, (int)P, kc, ks, vc, vs, krow, vrow, score, o);
+            attend_row_fp8(qd, d, scale, nk, (int)P, kc, ks, vc, vs, krow, vrow, fmt, score, o);
         }
         free(kc);
         free(vc);
@@ -523,4 +583,17 @@ int orc_attention_fp8hist(int R, const int32_t *cu_rows, const int32_t *prefix_l
         free(qd);
     }
     return status;
+}
+
+/* orc_attention_fp8hist_fmt of an E4M3 history.                                */
+int orc_attention_fp8hist(int R, const int32_t *cu_rows, const int32_t *prefix_len, int Hq,
+                          int Hkv, int d, double scale, const uint16_t *q,
+                          const uint16_t *k_new, const uint16_t *v_new, const uint8_t *hk,
+                          const float *hks, const uint8_t *hv, const float *hvs,
+                          const int64_t *hist_off, int64_t n_items, const int32_t *item_row,
+                          const int32_t *item_head, double *out, int nthreads)
+{
+    return orc_attention_fp8hist_fmt(R, cu_rows, prefix_len, Hq, Hkv, d, scale, q, k_new, v_new,
+                                     hk, hks, hv, hvs, hist_off, n_items, item_row, item_head,
+                                     out, 0, nthreads);
 }

@@ -509,6 +509,112 @@ def test_fp8_history_attention_equals_bf16_oracle_on_exact_values():
     assert np.max(np.abs(a2 - b2)) == 0.0
 
 
+# E5M2, the second FP8 format (hotdry.top "MiMo inference optimization, edge
+# deployment", "KV Cache 量化策略的技术选型"): OCP E5M2, bias 15, 2 mantissa bits.
+
+def test_e5m2_hand_values():
+    enc = oracle.e5m2_encode
+    assert enc(57344.0) == 0x7B and enc(1.0) == 0x3C and enc(-2.0) == 0xC0
+    assert enc(2.0 ** -16) == 0x01           # smallest subnormal
+    assert enc(2.0 ** -17) == 0x00           # tie with 0 -> even code
+    assert enc(2.0 ** -14) == 0x04           # smallest normal
+    assert enc(1.125) == 0x3C                # tie between 1 and 1.25 -> even
+    assert enc(1.375) == 0x3E                # tie between 1.25 and 1.5 -> even
+    assert enc(61440.0) == 0x7B and enc(1e6) == 0x7B and enc(-1e9) == 0xFB   # saturating
+    assert enc(-0.0) == 0x80 and enc(0.0) == 0x00
+    assert oracle.e5m2_value(0x7B) == 57344.0 and oracle.e5m2_value(0x01) == 2.0 ** -16
+    assert oracle.e5m2_value(0x7C) == math.inf and oracle.e5m2_value(0xFC) == -math.inf
+    assert np.isnan(oracle.e5m2_value(0x7D)) and np.isnan(oracle.e5m2_value(0xFF))
+
+
+def test_e5m2_values_are_the_top_byte_of_fp16():
+    """An E5M2 code is an IEEE binary16 with its low 8 bits zero: numpy's float16
+    decoding (an independent routine) gives every finite code's value."""
+    for c in range(256):
+        if (c & 0x7F) >= 0x7C:
+            continue
+        ref = float(np.array([c << 8], np.uint16).view(np.float16)[0])
+        assert oracle.e5m2_value(c) == ref, hex(c)
+
+
+def test_e5m2_round_trip_and_order():
+    finite = [c for c in range(256) if (c & 0x7F) < 0x7C]
+    for c in finite:
+        assert oracle.e5m2_encode(oracle.e5m2_value(c)) == c, hex(c)
+    pos = [oracle.e5m2_value(c) for c in range(0x7C)]
+    assert all(a < b for a, b in zip(pos, pos[1:]))
+
+
+def test_e5m2_matches_torch_cast():
+    """torch's float8_e5m2 cast (round to nearest even) inside the finite range."""
+    if not hasattr(torch, "float8_e5m2"):
+        pytest.skip("no float8 dtype in this torch")
+    rng = np.random.default_rng(12)
+    x = np.concatenate([rng.standard_normal(3000) * 3000, rng.standard_normal(1000) * 1e-3,
+                        rng.uniform(-57344, 57344, 1000),
+                        rng.standard_normal(500) * 2.0 ** -15]).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.float8_e5m2).view(torch.uint8).numpy()
+    got = np.array([oracle.e5m2_encode(v) for v in x], np.uint8)
+    assert np.array_equal(got, ref)
+
+
+def test_quantize_e5m2_rows_scale_and_extremes():
+    g = torch.Generator().manual_seed(13)
+    x = torch.randn(64, 128, generator=g).to(torch.bfloat16)
+    x[5] = 0
+    codes, scales = oracle.quantize_e5m2(x)
+    xf = x.float().numpy()
+    amax = np.abs(xf).max(axis=1).astype(np.float32)
+    assert np.array_equal(scales, (amax / np.float32(57344.0)).astype(np.float32))
+    assert scales[5] == 0 and not codes[5].any()
+    c2, s2 = oracle.quantize_fp8(x, "e5m2")
+    assert np.array_equal(c2, codes) and np.array_equal(s2, scales)
+    for r in range(64):
+        if r == 5:
+            continue
+        j = int(np.argmax(np.abs(xf[r])))
+        assert codes[r, j] & 0x7F == 0x7B            # the row maximum maps to 57344
+        deq = np.array([oracle.e5m2_value(c) for c in codes[r]]) * scales[r]
+        # E5M2 keeps 2 mantissa bits: relative error <= 2^-3 above the subnormals
+        big = np.abs(xf[r]) > scales[r] * 2.0 ** -14
+        assert np.all(np.abs(deq - xf[r])[big] <= np.abs(xf[r])[big] * 2.0 ** -3 + 1e-12)
+
+
+def test_e5m2_history_attention_equals_bf16_oracle_on_exact_values():
+    """Every E5M2 value is exact in bf16: with unit scales the E5M2 history must
+    give orc_attention fed those values, and the format switch must matter."""
+    rng = np.random.default_rng(14)
+    Hq, Hkv, d, R = 8, 2, 32, 2
+    P, T = [9, 33], [2, 1]
+    hist = sum(P)
+    codes_k = (rng.integers(0x30, 0x44, (hist, Hkv, d)).astype(np.uint8) |
+               (rng.integers(0, 2, (hist, Hkv, d)).astype(np.uint8) << 7))
+    codes_v = rng.integers(0x28, 0x48, (hist, Hkv, d)).astype(np.uint8)
+    ones = np.ones((hist, Hkv), np.float32)
+    val_k = np.vectorize(oracle.e5m2_value)(codes_k).astype(np.float32)
+    val_v = np.vectorize(oracle.e5m2_value)(codes_v).astype(np.float32)
+    bk = torch.from_numpy(val_k).to(torch.bfloat16)
+    bv = torch.from_numpy(val_v).to(torch.bfloat16)
+    assert np.array_equal(bk.float().numpy(), val_k)
+    rows = sum(T)
+    g = torch.Generator().manual_seed(15)
+    q = (torch.randn(rows, Hq, d, generator=g) * 0.05).to(torch.bfloat16)
+    kn = torch.randn(rows, Hkv, d, generator=g).to(torch.bfloat16)
+    vn = torch.randn(rows, Hkv, d, generator=g).to(torch.bfloat16)
+    cu = np.array([0, T[0], rows], np.int32)
+    pl = np.array(P, np.int32)
+    ho = np.array([0, P[0], hist], np.int64)
+    a = oracle.attention_fp8hist(cu, pl, q, kn, vn, codes_k, ones, codes_v, ones, ho, 0.3,
+                                 fmt="e5m2")
+    b = oracle.attention(cu, pl, q, kn, vn, bk, bv, ho, np.zeros(R, np.int32), 0, 0.3)
+    assert np.max(np.abs(a - b)) == 0.0
+    e4 = oracle.attention_fp8hist(cu, pl, q, kn, vn, codes_k, ones, codes_v, ones, ho, 0.3)
+    assert np.max(np.abs(e4 - b)) > 0.1          # read as E4M3 the codes mean other values
+    with pytest.raises(ValueError):
+        oracle.attention_fp8hist(cu, pl, q, kn, vn, codes_k, ones, codes_v, ones, ho, 0.3,
+                                 fmt="e3m4")
+
+
 # ---------------------------------------------------------------- prefix model
 # youleyou.com s2 "KVCache系统重构": a hit counts up to the window-safe length; the
 # Full index is authoritative; SWA is kept for a finished request's last window.
