@@ -155,8 +155,9 @@ def decode_bytes(inst, layer_full, fp8=False):
     KV: every key some query of the step may see, once (2048 B per token per
     layer: K and V, 4 KV heads, d = 128, bf16): full layers c + T tokens, sliding
     layers min(c + T, W + T - 1).  Plus q read and out written.  An FP8 full layer
-    holds its c cached tokens as E4M3 codes plus one fp32 scale per (token, head)
-    row: 2 * Hkv * (d + 4) bytes per token; the T new rows are read as bf16.
+    holds its c cached tokens as FP8 codes (E4M3 or E5M2) plus one fp32 scale per
+    (token, head) row: 2 * Hkv * (d + 4) bytes per token; the T new rows are read
+    as bf16.
     """
     cfg = inst.cfg
     per_tok = 2 * cfg.Hkv * cfg.d * 2
@@ -411,8 +412,10 @@ class DecodeStep:
         swa = [i for i, l in enumerate(self.model_layers) if not self.inst.full[l]]
         out = []
         if full:
-            out.append(("full_fp8" if self.kv_fp8 else "full",
-                        "decode_kernel (full layers%s)" % (", FP8 KV" if self.kv_fp8 else ""),
+            key = {"e4m3": "full_fp8", "e5m2": "full_e5m2"}.get(self.kv_fp8, "full")
+            out.append((key,
+                        "decode_kernel (full layers%s)" % (
+                            ", FP8 %s KV" % self.kv_fp8.upper() if self.kv_fp8 else ""),
                         full, decode_bytes(self.inst, True, self.kv_fp8), "hbm", self.attn))
         if swa:
             out.append(("sliding", "decode_kernel (sliding layers, ring)", swa,
@@ -754,9 +757,11 @@ def measure(args, inst, ws, rank, local, cpu_repeats=None):
         line["config"]["early_pool_read"] = step.early
     line.update(extra)
     if args.kv_fp8:
-        line["dtype"] = "e4m3 Full KV Pool (fp16 MMA, fp32 accumulate), bf16 rings / q / out"
-        line["config"]["kv_fp8"] = ("full layers stored as E4M3 codes + one fp32 scale per "
-                                    "(token, KV head) row; sliding rings bf16")
+        line["dtype"] = ("%s Full KV Pool (fp16 MMA, fp32 accumulate), bf16 rings / q / out"
+                         % args.kv_fp8)
+        line["config"]["kv_fp8"] = ("full layers stored as %s codes + one fp32 scale per "
+                                    "(token, KV head) row; sliding rings bf16"
+                                    % args.kv_fp8.upper())
     if prefetch_info is not None:
         line["swa_prefetch"] = prefetch_info
         line["config"]["swa_prefetch"] = ("every step reloads the sliding layers' rings of %.0f%% "
@@ -808,18 +813,22 @@ def _ctx_desc(cfg):
 # kernel whose source has changed since reports None.  Captures of fewer
 # sequences / requests are scaled to the full launch by the units processed.
 TRAFFIC = {
-    # decode_kernel, full layer: 389.6 MB on 4 sequences, scaled by units
-    ("decode", "full"): ("decode.cu", "8968219e5757c4b2", 2832812948),
+    # decode_kernel, full layer: 388.9 MB on 4 sequences, scaled by units
+    ("decode", "full"): ("decode.cu", "053937bc5c4fa8b2", 2827638725),
     # decode_kernel, sliding layer: full-size launch (32 sequences)
-    ("decode", "sliding"): ("decode.cu", "8968219e5757c4b2", 8785408),
-    # decode_kernel, FP8 full layer: 202.6 MB on 4 sequences, scaled by units
-    ("decode", "full_fp8"): ("decode.cu", "8968219e5757c4b2", 1472737897),
+    ("decode", "sliding"): ("decode.cu", "053937bc5c4fa8b2", 8854528),
+    # decode_kernel, FP8 full layer: 202.5 MB (E4M3) / 202.1 MB (E5M2) on 4
+    # sequences, scaled by units
+    ("decode", "full_fp8"): ("decode.cu", "053937bc5c4fa8b2", 1471985925),
+    ("decode", "full_e5m2"): ("decode.cu", "053937bc5c4fa8b2", 1469482449),
     # decode_kernel, full layer: 1.608 GB on 1 sequence, scaled by units
-    ("long", "full"): ("decode.cu", "8968219e5757c4b2", 5675719535),
+    ("long", "full"): ("decode.cu", "053937bc5c4fa8b2", 5674756107),
+    ("long", "sliding"): ("decode.cu", "053937bc5c4fa8b2", 1181184),
     # decode_kernel, full layer, T = 4: 1.658 GB on 8 sequences, scaled by units
-    ("mtp", "full"): ("decode.cu", "8968219e5757c4b2", 11701335556),
-    # prefill_kernel, full layer: 4.552 GB on 2 requests, scaled by flops
-    ("prefill", "full"): ("prefill.cu", "0e97e900cd7e5029", 14340211242),
+    ("mtp", "full"): ("decode.cu", "053937bc5c4fa8b2", 11699352313),
+    ("mtp", "sliding"): ("decode.cu", "053937bc5c4fa8b2", 14617344),
+    # prefill_kernel, full layer: 4.720 GB on 2 requests, scaled by flops
+    ("prefill", "full"): ("prefill.cu", "5df8d9b43c75a2fc", 14869832402),
     # prefill_swa_kernel, sliding layer: full-size launch
     ("prefill", "sliding"): ("prefill_swa.cu", "487bd58bef03179b", 809082368),
     # append_kernel, full-size launches (writes still held in L2 at the kernel's end
@@ -871,8 +880,9 @@ def main():
     ap.add_argument("--swa-prefetch-frac", type=float, default=1.0,
                     help="with --swa-prefetch: the seeded fraction of sequences whose rings "
                          "come back each step (default: all)")
-    ap.add_argument("--kv-fp8", action="store_true",
-                    help="decode: full layers as an FP8 (E4M3) Full KV Pool (no CPU baseline)")
+    ap.add_argument("--kv-fp8", nargs="?", const="e4m3", default=None, choices=["e4m3", "e5m2"],
+                    help="decode: full layers as an FP8 Full KV Pool of that format (default "
+                         "e4m3; no CPU baseline)")
     ap.add_argument("--no-early-pool-read", action="store_true",
                     help="decode: sliding layers wait for the previous kernel before reading "
                          "their ring (the default reads it early, HSA_DECODE_EARLY_POOL_READ)")

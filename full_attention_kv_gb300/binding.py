@@ -184,6 +184,23 @@ def _check(fn, status):
         raise HsaError(fn, status)
 
 
+HSA_KV_E4M3 = 1
+HSA_KV_E5M2 = 2
+
+
+def fp8_code(fmt):
+    """layer_kv_fp8 value of a format: False / None / 0 -> 0 (bf16), True / 1 / "e4m3"
+    -> HSA_KV_E4M3, 2 / "e5m2" -> HSA_KV_E5M2."""
+    if fmt is None or fmt is False or (isinstance(fmt, int) and not isinstance(fmt, bool)
+                                       and fmt == 0):
+        return 0
+    if fmt is True or fmt == "e4m3" or (isinstance(fmt, int) and fmt == HSA_KV_E4M3):
+        return HSA_KV_E4M3
+    if fmt == "e5m2" or (isinstance(fmt, int) and fmt == HSA_KV_E5M2):
+        return HSA_KV_E5M2
+    raise ValueError("unknown FP8 format %r" % (fmt,))
+
+
 class DualPool:
     """The dual KV pool of one model: the C struct plus the tensors it points at.
 
@@ -194,15 +211,16 @@ class DualPool:
 
     def __init__(self, layer_is_full, k, v, block_tables, ring_row, Hq, W=128, page=64,
                  kv_fp8=None, Hkv=None, d=None, num_blocks=None):
-        """kv_fp8[l] marks an FP8 full layer: k[l], v[l] are then flat uint8 buffers of
-        num_blocks * Hkv * page * (d + 4) bytes (E4M3 codes, then fp32 scales;
+        """kv_fp8[l] marks an FP8 full layer (True or "e4m3": E4M3 codes; "e5m2":
+        E5M2 codes; False / None: bf16): k[l], v[l] are then flat uint8 buffers of
+        num_blocks * Hkv * page * (d + 4) bytes (codes, then fp32 scales;
         include/hsa.h gives the layout), and Hkv, d, num_blocks must be passed."""
         self.layer_is_full = [bool(x) for x in layer_is_full]
         self.k, self.v = list(k), list(v)
         self.block_tables, self.ring_row = block_tables, ring_row
         n = len(self.layer_is_full)
         assert len(self.k) == n and len(self.v) == n
-        self.kv_fp8 = [bool(x) for x in kv_fp8] if kv_fp8 is not None else [False] * n
+        self.kv_fp8 = [fp8_code(x) for x in kv_fp8] if kv_fp8 is not None else [0] * n
         assert len(self.kv_fp8) == n
         _need(block_tables, "block_tables", torch.int32, ndim=2)
         _need(ring_row, "ring_row", torch.int32, ndim=1)
@@ -240,7 +258,7 @@ class DualPool:
             if hk != Hkv or dd != d:
                 raise ValueError("layers disagree on Hkv / d")
         self._full = (ctypes.c_uint8 * n)(*[1 if f else 0 for f in self.layer_is_full])
-        self._fp8 = (ctypes.c_uint8 * n)(*[1 if f else 0 for f in self.kv_fp8])
+        self._fp8 = (ctypes.c_uint8 * n)(*self.kv_fp8)
         self._k = (ctypes.c_void_p * n)(*[t.data_ptr() for t in self.k])
         self._v = (ctypes.c_void_p * n)(*[t.data_ptr() for t in self.v])
         self.c = HsaPools(
@@ -272,9 +290,10 @@ class DualPool:
     def allocate(cls, layer_is_full, num_blocks, n_ring_rows, block_tables, ring_row, Hq, Hkv,
                  d=128, W=128, page=64, device="cuda", kv_fp8=False):
         """Zero-filled pools (rows past a sequence's length must hold finite values).
-        kv_fp8=True stores every full layer as an FP8 layer (sliding rings stay bf16)."""
+        kv_fp8=True / "e4m3" / "e5m2" stores every full layer as an FP8 layer of that
+        format (sliding rings stay bf16)."""
         k, v = [], []
-        fp8 = [bool(kv_fp8) and bool(f) for f in layer_is_full]
+        fp8 = [fp8_code(kv_fp8) if f else 0 for f in layer_is_full]
         for f, q8 in zip(layer_is_full, fp8):
             if q8:
                 nbytes = num_blocks * Hkv * page * (d + 4)

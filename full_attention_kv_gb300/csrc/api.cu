@@ -84,9 +84,11 @@ bool encode_2d_u8(CUtensorMap *map, const void *base, uint64_t cols, uint64_t ro
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
-bool layer_fp8(const hsa_pools *p, int32_t layer)
+// FP8 format of a layer: 0 bf16, HSA_KV_E4M3, HSA_KV_E5M2 (other values are
+// rejected by check_pools)
+int layer_fp8(const hsa_pools *p, int32_t layer)
 {
-    return p->layer_kv_fp8 && p->layer_kv_fp8[layer];
+    return p->layer_kv_fp8 ? p->layer_kv_fp8[layer] : 0;
 }
 
 int device_sms()
@@ -116,7 +118,10 @@ hsa_status check_pools(const hsa_pools *p, int32_t layer)
         return HSA_INVALID_ARG;
     if (!p->k[layer] || !p->v[layer] || !aligned16(p->k[layer]) || !aligned16(p->v[layer]))
         return HSA_INVALID_ARG;
-    if (layer_fp8(p, layer) && !p->layer_is_full[layer])
+    const int fmt = layer_fp8(p, layer);
+    if (fmt != 0 && fmt != HSA_KV_E4M3 && fmt != HSA_KV_E5M2)
+        return HSA_INVALID_ARG;
+    if (fmt && !p->layer_is_full[layer])
         return HSA_UNSUPPORTED_SHAPE;  // the ring (newest W tokens) stays bf16
     if (p->layer_is_full[layer]) {
         if (!p->block_tables || p->num_blocks <= 0 || p->max_blocks <= 0)
@@ -187,7 +192,7 @@ hsa_status hsa_kv_append(const hsa_pools *pools, int32_t layer, const void *k_ne
     a.n_ring_rows = pools->n_ring_rows;
     a.W = pools->W;
     a.ring_mode = pools->layer_is_full[layer] ? 0 : 1;
-    a.fp8 = layer_fp8(pools, layer) ? 1 : 0;
+    a.fp8 = layer_fp8(pools, layer) == HSA_KV_E5M2 ? 2 : layer_fp8(pools, layer) ? 1 : 0;
     return hsa::launch_append(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? HSA_OK
                                                                                   : HSA_CUDA_ERROR;
 }
@@ -270,7 +275,8 @@ hsa_status decode_common(const hsa_pools *pools, int32_t layer, const void *q, c
         return HSA_INVALID_ARG;
 
     CUtensorMap tmK, tmV;
-    const bool fp8 = layer_fp8(pools, layer);
+    const int fmt = layer_fp8(pools, layer);
+    const bool fp8 = fmt != 0;
     const uint64_t rows = full ? (uint64_t)pools->num_blocks * pools->Hkv * pools->page_size
                                : (uint64_t)pools->n_ring_rows * pools->Hkv * pools->W;
     if (fp8) {
@@ -305,7 +311,7 @@ hsa_status decode_common(const hsa_pools *pools, int32_t layer, const void *q, c
     p.T = (int16_t)T;
     p.G = (int16_t)G;
     p.flags = (full ? 0 : hsa::kDecodeRing) | (append ? hsa::kDecodeAppend : 0) |
-              (fp8 ? hsa::kDecodeFp8 : 0) |
+              (fp8 ? hsa::kDecodeFp8 : 0) | (fmt == HSA_KV_E5M2 ? hsa::kDecodeE5M2 : 0) |
               ((!full && (options & HSA_DECODE_EARLY_POOL_READ)) ? hsa::kDecodeEarly : 0);
     p.scale_log2 = scale * 1.4426950408889634f;
     return hsa::launch_decode(tmK, tmV, p, ctas, static_cast<cudaStream_t>(stream)) == cudaSuccess

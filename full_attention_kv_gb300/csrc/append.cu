@@ -11,8 +11,9 @@
 // written once per call (deterministic, race-free) and the result equals
 // appending the tokens one by one in position order.
 // An FP8 full layer (fp8_kv.cuh) is written by append_fp8_kernel instead: one warp
-// per (token, KV head, K or V) row quantises the row to E4M3 codes plus one fp32
-// scale (amax / 448, found by a warp reduction) and stores them in the page layout.
+// per (token, KV head, K or V) row quantises the row to E4M3 or E5M2 codes plus one
+// fp32 scale (amax / 448 or amax / 57344, the amax found by a warp reduction) and
+// stores them in the page layout.
 #include "fp8_kv.cuh"
 #include "hsa_device.cuh"
 #include "hsa_internal.h"
@@ -86,7 +87,7 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendParams p)
 }
 
 // FP8 Full KV Pool layer: one warp per (token, KV head, K or V) row, quantised
-// into the layer's E4M3 layout (fp8_kv.cuh).
+// into the layer's E4M3 or E5M2 codes (fp8_kv.cuh).
 __global__ void __launch_bounds__(256) append_fp8_kernel(const AppendParams p)
 {
     const int lane = threadIdx.x & 31;
@@ -134,7 +135,7 @@ __global__ void __launch_bounds__(256) append_fp8_kernel(const AppendParams p)
         const __nv_bfloat16 *src =
             reinterpret_cast<const __nv_bfloat16 *>(kv ? p.v_new : p.k_new) + ((int64_t)tok * p.Hkv + h) * 128;
         fp8_store_row(src, kv ? vc : kc, kv ? vs : ks, blk, h, p.Hkv, (int)(pos % p.page_size), kv,
-                      lane);
+                      lane, p.fp8 == 2);
     }
 }
 

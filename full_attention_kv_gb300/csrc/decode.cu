@@ -325,11 +325,14 @@ __device__ __forceinline__ void run_tile(RowState &st, const uint32_t (&qa)[kD /
 
 // One key tile of an FP8 full layer (fp8_kv.cuh layout) on tensor cores, fp16
 // MMAs.  K: one 32-bit shared load per (key, 16-dim step) holds a thread's four
-// E4M3 codes of the B fragment, converted exactly to fp16; the key's scale is then
+// codes of the B fragment, converted exactly to fp16 (E4M3: cvt; E5M2: a byte
+// permute, an E5M2 code being the high byte of its fp16); the key's scale is then
 // applied to its S column.  V (stored transposed): one 32-bit load per (dimension,
 // 16-key step); each key's scale is folded into P, while the row sum takes P
-// itself.  qa holds fp16 Q fragments.
-template <int NT, typename Vis>
+// itself.  An E5M2 scale (amax / 57344) is folded in times 256, so that the fp16 P
+// stays clear of fp16's subnormals; the accumulator then holds 256 O, which the
+// kernel divides out at the end of the unit.  qa holds fp16 Q fragments.
+template <int NT, bool E5M2, typename Vis>
 __device__ __forceinline__ void run_tile_fp8(RowState &st, const uint32_t (&qa)[kD / 16][4],
                                              const uint8_t *sK, const uint8_t *sV,
                                              const float *k_scale, const float *v_scale, int key0,
@@ -352,8 +355,7 @@ __device__ __forceinline__ void run_tile_fp8(RowState &st, const uint32_t (&qa)[
 #pragma unroll
         for (int ks = 0; ks < kD / 16; ++ks) {
             const uint32_t w = *reinterpret_cast<const uint32_t *>(row + ((ks ^ (key & 7)) << 4));
-            mma_f16_16816((ks & 1) ? s2[nt] : s[nt], qa[ks], e4m3x2_to_f16x2(w & 0xffffu),
-                          e4m3x2_to_f16x2(w >> 16));
+            mma_f16_16816((ks & 1) ? s2[nt] : s[nt], qa[ks], fp8x2_lo<E5M2>(w), fp8x2_hi<E5M2>(w));
         }
     }
 #pragma unroll
@@ -437,8 +439,9 @@ __device__ __forceinline__ void run_tile_fp8(RowState &st, const uint32_t (&qa)[
 #pragma unroll
     for (int ks = 0; ks < NT / 2; ++ks) {
         const int kb = key0 + ks * 16 + 2 * tq;
-        const float va0 = v_scale[kb], va1 = v_scale[kb + 1];
-        const float vb0 = v_scale[kb + 8], vb1 = v_scale[kb + 9];
+        constexpr float f = E5M2 ? 256.f : 1.f;
+        const float va0 = v_scale[kb] * f, va1 = v_scale[kb + 1] * f;
+        const float vb0 = v_scale[kb + 8] * f, vb1 = v_scale[kb + 9] * f;
         uint32_t pa[4];
         pa[0] = pack_f16(s[2 * ks][0] * va0, s[2 * ks][1] * va1);
         pa[1] = pack_f16(s[2 * ks][2] * va0, s[2 * ks][3] * va1);
@@ -450,7 +453,7 @@ __device__ __forceinline__ void run_tile_fp8(RowState &st, const uint32_t (&qa)[
             const int dim = n * 8 + g;
             const uint32_t w = *reinterpret_cast<const uint32_t *>(
                 sV + dim * 64 + ((grp ^ ((dim >> 1) & 3)) << 4) + 4 * tq);
-            mma_f16_16816(st.o[n], pa, e4m3x2_to_f16x2(w & 0xffffu), e4m3x2_to_f16x2(w >> 16));
+            mma_f16_16816(st.o[n], pa, fp8x2_lo<E5M2>(w), fp8x2_hi<E5M2>(w));
         }
     }
     st.l[0] += sum0;
@@ -459,7 +462,7 @@ __device__ __forceinline__ void run_tile_fp8(RowState &st, const uint32_t (&qa)[
 
 // Append of unit (b, h) into an FP8 full layer: one warp per new K or V row.
 __device__ __forceinline__ void append_unit_fp8(const DecodeParams &p, int b, int h, int c, int warp,
-                                                int lane, int nwarps)
+                                                int lane, int nwarps, bool e5m2)
 {
     uint8_t *const kc = reinterpret_cast<uint8_t *>(p.k_dst);
     uint8_t *const vc = reinterpret_cast<uint8_t *>(p.v_dst);
@@ -482,7 +485,7 @@ __device__ __forceinline__ void append_unit_fp8(const DecodeParams &p, int b, in
         const __nv_bfloat16 *src = (kv ? p.v_new : p.k_new) + ((int64_t)(b * p.T + t) * p.Hkv + h) * kD;
         uint8_t *codes = kv ? vc : kc;
         fp8_store_row(src, codes, reinterpret_cast<float *>(codes + cb), blk, h, p.Hkv,
-                      (int)(pos % kTileKeys), kv, lane);
+                      (int)(pos % kTileKeys), kv, lane, e5m2);
     }
 }
 
@@ -546,7 +549,7 @@ using SharedStorage = SharedStorageT<RING ? kRingStageRegion : kStageRegion>;
 // layer; RING: a sliding layer (its own instantiation with two stages; at MT = 1 it
 // is held to 168 registers so that two CTAs fit on an SM -- at MT = 2 that limit
 // spilled ~170 bytes a thread, so MTP rings keep one CTA an SM).
-template <int MT, bool FP8, bool RING>
+template <int MT, int FP8, bool RING>
 __global__ void __launch_bounds__(kThreads, (RING && MT == 1) ? 2 : 1)
     decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const DecodeParams p)
@@ -760,6 +763,18 @@ __global__ void __launch_bounds__(kThreads, (RING && MT == 1) ? 2 : 1)
     bool fresh = true;
     bool timed_out = false;
 
+    // the unit's new tokens (staged in new_k / new_v): positions c .. c+T-1, causal
+    // among themselves
+    auto run_new_tile = [&]() {
+        const int T = p.T;
+        auto vis_new = [&](int rr, int key) -> bool {
+            const int t = rr == g ? t0 : t1;
+            return t < T && key <= t;
+        };
+        run_tile<2, (FP8 != 0)>(st, qa, smem_u32(sh.new_k), smem_u32(sh.new_v), kNewRows, 0,
+                                p.scale_log2, false, t0 < T, t1 < T, vis_new);
+    };
+
     for (int64_t i = i0, k = 0; i < i1; ++i, ++k) {
         if (fresh) {
             fresh = false;
@@ -786,10 +801,15 @@ __global__ void __launch_bounds__(kThreads, (RING && MT == 1) ? 2 : 1)
                         qa[ks][e] = bf16x2_to_f16x2(qa[ks][e]);
                 }
             }
-            // stage this unit's new tokens now when this CTA owns the unit's last
-            // tile; rows >= T are zero
-            if (unit_start + w.n <= i1) {
-                for (int e = tid; e < kNewRows * kD / 8; e += kConsumerWarps * 32) {
+            // when this CTA owns the unit's last tile, stage the unit's new rows (rows
+            // >= T zero).  Rings (a unit is two tiles): the slice-0 warps (one per
+            // m-tile) stage them and run them as a 16-key tile now, while the other
+            // warps wait for their stage (the online softmax takes tiles in any
+            // order).  Full layers: every consumer warp stages, and the slice-0 warps
+            // run the tile at the end of the unit, so that no group starts late.
+            if (unit_start + w.n <= i1 && (!RING || slice == 0)) {
+                constexpr int kStagers = (RING ? MT : kConsumerWarps) * 32;
+                for (int e = tid; e < kNewRows * kD / 8; e += kStagers) {
                     const int rr = e / (kD / 8), col = (e % (kD / 8)) * 8;
                     uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
                     if (rr < p.T) {
@@ -806,6 +826,13 @@ __global__ void __launch_bounds__(kThreads, (RING && MT == 1) ? 2 : 1)
                     }
                     *reinterpret_cast<uint4 *>(sh.new_k + swz128_offset(rr, col, kNewRows)) = kv;
                     *reinterpret_cast<uint4 *>(sh.new_v + swz128_offset(rr, col, kNewRows)) = vv;
+                }
+                if constexpr (RING) {
+                    if (MT == 1)
+                        __syncwarp();
+                    else
+                        named_bar_sync(2, MT * 32);
+                    run_new_tile();
                 }
             }
         }
@@ -845,8 +872,9 @@ __global__ void __launch_bounds__(kThreads, (RING && MT == 1) ? 2 : 1)
             if constexpr (FP8) {  // full layers only: tile-parallel
                 const uint8_t *base = sh.stage + stg * kFp8StageStride;
                 const float *ksc = reinterpret_cast<const float *>(base + 2 * kFp8TileBytes);
-                run_tile_fp8<kTileKeys / 8>(st, qa, base, base + kFp8TileBytes, ksc, ksc + 64,
-                                            key0, p.scale_log2, all_vis, t0 < T, t1 < T, vis);
+                run_tile_fp8<kTileKeys / 8, FP8 == 2>(st, qa, base, base + kFp8TileBytes, ksc,
+                                                      ksc + 64, key0, p.scale_log2, all_vis,
+                                                      t0 < T, t1 < T, vis);
             } else if (wt == 1) {
                 run_tile<kTileKeys / 8>(st, qa, sK, sV, kTileKeys, key0, p.scale_log2, all_vis,
                                         t0 < T, t1 < T, vis);
@@ -867,20 +895,18 @@ __global__ void __launch_bounds__(kThreads, (RING && MT == 1) ? 2 : 1)
 
         // ---- end of this CTA's share of unit (cur.b, cur.h) ------------------
         const int64_t unit_end = unit_start + cur.n;  // one past its last item
-        if (unit_last_tile) {
-            // new tokens (staged at unit start): positions c .. c+T-1, causal
-            named_bar_sync(1, kConsumerWarps * 32);
-            if (slice == 0) {
-                const int T = p.T;
-                auto vis_new = [&](int rr, int key) -> bool {
-                    const int t = rr == g ? t0 : t1;
-                    return t < T && key <= t;
-                };
-                run_tile<2, FP8>(st, qa, smem_u32(sh.new_k), smem_u32(sh.new_v), kNewRows, 0,
-                                 p.scale_log2, false, t0 < T, t1 < T, vis_new);
-            }
+        if constexpr (FP8 == 2) {  // the E5M2 tiles accumulate 256 O
+#pragma unroll
+            for (int n = 0; n < kD / 8; ++n)
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    st.o[n][e] *= 1.f / 256.f;
         }
-
+        if (!RING && unit_last_tile) {
+            named_bar_sync(1, kConsumerWarps * 32);  // new rows staged by every warp
+            if (slice == 0)
+                run_new_tile();
+        }
         // merge the warps' states (same m-tile, different key slices)
         {
             float l0 = st.l[0], l1 = st.l[1];
@@ -980,7 +1006,7 @@ __global__ void __launch_bounds__(kThreads, (RING && MT == 1) ? 2 : 1)
         if (whole && (p.flags & kDecodeAppend)) {
             // a whole unit's new rows were staged by this CTA (it owns the last tile)
             if constexpr (FP8)
-                append_unit_fp8(p, cur.b, cur.h, cur.c, warp, lane, kConsumerWarps);
+                append_unit_fp8(p, cur.b, cur.h, cur.c, warp, lane, kConsumerWarps, FP8 == 2);
             else
                 append_unit(p, cur.b, cur.h, cur.c, tid, kConsumerWarps * 32, sh.new_k, sh.new_v);
         }
@@ -1022,7 +1048,8 @@ __global__ void __launch_bounds__(kThreads, (RING && MT == 1) ? 2 : 1)
                 }
                 if (p.flags & kDecodeAppend) {
                     if constexpr (FP8)
-                        append_unit_fp8(p, cur.b, cur.h, cur.c, warp, lane, kConsumerWarps);
+                        append_unit_fp8(p, cur.b, cur.h, cur.c, warp, lane, kConsumerWarps,
+                                        FP8 == 2);
                     else
                         append_unit(p, cur.b, cur.h, cur.c, tid, kConsumerWarps * 32);
                 }
@@ -1054,17 +1081,20 @@ cudaError_t launch_decode(const CUtensorMap &tmK, const CUtensorMap &tmV, const 
     const size_t smem = (ring ? sizeof(SharedStorage<true>) : sizeof(SharedStorage<false>)) + 1024;
     // the opt-in shared-memory size is set once per process (the API is not a stream
     // operation, but setting it once keeps graph capture free of extra calls)
-    static bool attr_set[6] = {false, false, false, false, false, false};
+    static bool attr_set[8] = {false, false, false, false, false, false, false, false};
     void (*kern)(CUtensorMap, CUtensorMap, DecodeParams);
     int which;
     if (ring) {
-        kern = MT == 1 ? decode_kernel<1, false, true> : decode_kernel<2, false, true>;
+        kern = MT == 1 ? decode_kernel<1, 0, true> : decode_kernel<2, 0, true>;
         which = 4 + MT - 1;
+    } else if (fp8 && (p.flags & kDecodeE5M2)) {
+        kern = MT == 1 ? decode_kernel<1, 2, false> : decode_kernel<2, 2, false>;
+        which = 6 + MT - 1;
     } else if (fp8) {
-        kern = MT == 1 ? decode_kernel<1, true, false> : decode_kernel<2, true, false>;
+        kern = MT == 1 ? decode_kernel<1, 1, false> : decode_kernel<2, 1, false>;
         which = 2 + MT - 1;
     } else {
-        kern = MT == 1 ? decode_kernel<1, false, false> : decode_kernel<2, false, false>;
+        kern = MT == 1 ? decode_kernel<1, 0, false> : decode_kernel<2, 0, false>;
         which = MT - 1;
     }
     if (!attr_set[which]) {

@@ -1,14 +1,17 @@
-// fp8_kv.cuh -- layout of an FP8 (E4M3) Full KV Pool layer and the warp routine
-// that quantises one (token, KV head) row into it.
+// fp8_kv.cuh -- layout of an FP8 (E4M3 or E5M2) Full KV Pool layer and the warp
+// routine that quantises one (token, KV head) row into it.
 //
 // [hotdry.top "MiMo inference optimization, edge deployment", "KV Cache 量化策略的
 // 技术选型": FP8 KV, with quantisation groups aligned to the window so that no
 // group straddles a window boundary; "边缘部署的工程权衡与参数清单": FP8 as the
 // baseline KV format, the newest 128 tokens kept at the original precision.]
 // Here a group is one (position, KV head) row of d = 128 values with one fp32
-// scale = amax / 448; code = E4M3(x / scale) (round to nearest even, saturating);
-// an all-zero row stores scale 0 and zero codes.  Only full layers use FP8: a
-// sliding layer's ring holds exactly the newest W = 128 tokens and stays bf16.
+// scale = amax / F, code = FP8(x / scale) (round to nearest even, saturating), F
+// the format's largest finite magnitude: 448 for E4M3 (4 exponent, 3 mantissa
+// bits), 57344 for E5M2 (5 exponent, 2 mantissa bits; the section weighs the
+// range of one against the precision of the other).  An all-zero row stores scale
+// 0 and zero codes.  Only full layers use FP8: a sliding layer's ring holds
+// exactly the newest W = 128 tokens and stays bf16.  Both formats share the layout.
 //
 // Layer buffer for K (and, separately, for V) of num_blocks pages:
 //   codes  [num_blocks * Hkv * 64 * 128] bytes, then
@@ -37,10 +40,10 @@ __host__ __device__ inline int64_t fp8_codes_bytes(int64_t num_blocks, int Hkv)
 
 // Quantise one row of 128 bf16 values (src) into page (blk, h), row `off`, of an
 // FP8 layer (codes base `codes`, scales base `scales`).  Called by a full warp;
-// kv = 0 writes the K layout, 1 the V layout.
+// kv = 0 writes the K layout, 1 the V layout; e5m2 picks the format (else E4M3).
 __device__ __forceinline__ void fp8_store_row(const __nv_bfloat16 *src, uint8_t *codes,
                                               float *scales, int64_t blk, int h, int Hkv, int off,
-                                              int kv, int lane)
+                                              int kv, int lane, bool e5m2)
 {
     float x[4];
     if (kv == 0) {
@@ -64,11 +67,13 @@ __device__ __forceinline__ void fp8_store_row(const __nv_bfloat16 *src, uint8_t 
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1)
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const float scale = __fdiv_rn(amax, 448.0f);
+    const float scale = __fdiv_rn(amax, e5m2 ? 57344.0f : 448.0f);
     uint32_t c01 = 0, c23 = 0;
     if (amax > 0.f) {
-        c01 = f32x2_to_e4m3x2(__fdiv_rn(x[0], scale), __fdiv_rn(x[1], scale));
-        c23 = f32x2_to_e4m3x2(__fdiv_rn(x[2], scale), __fdiv_rn(x[3], scale));
+        const float y0 = __fdiv_rn(x[0], scale), y1 = __fdiv_rn(x[1], scale);
+        const float y2 = __fdiv_rn(x[2], scale), y3 = __fdiv_rn(x[3], scale);
+        c01 = e5m2 ? f32x2_to_e5m2x2(y0, y1) : f32x2_to_e4m3x2(y0, y1);
+        c23 = e5m2 ? f32x2_to_e5m2x2(y2, y3) : f32x2_to_e4m3x2(y2, y3);
     }
     const int64_t page = blk * Hkv + h;
     if (kv == 0) {

@@ -203,6 +203,20 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t threads)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+// Named barrier that also ANDs a predicate over its threads: every participant
+// gets the same answer, so a group can leave a loop together (no participant left
+// waiting at a later barrier for one that has gone).
+__device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t threads, bool pred)
+{
+    uint32_t r;
+    asm volatile("{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\t"
+                 "bar.red.and.pred po, %2, %3, pi;\n\tselp.u32 %0, 1, 0, po;\n\t}"
+                 : "=r"(r)
+                 : "r"((uint32_t)pred), "r"(id), "r"(threads)
+                 : "memory");
+    return r != 0;
+}
+
 // ---------------------------------------------------------------- warp MMA
 __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t &r0, uint32_t &r1,
                                             uint32_t &r2, uint32_t &r3)
@@ -271,6 +285,36 @@ __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi)
 {
     unsigned short d;
     asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
+// Two E5M2 codes -> two fp16, exact: an E5M2 code is the high byte of the binary16
+// of the same value (same exponent bias, 2 of fp16's 10 mantissa bits).  HI picks
+// the codes in bytes 2, 3 of w, else those in bytes 0, 1 (low byte -> low half).
+template <bool HI>
+__device__ __forceinline__ uint32_t e5m2x2_to_f16x2(uint32_t w)
+{
+    return __byte_perm(w, 0u, HI ? 0x3424 : 0x1404);
+}
+
+// The fp16 pairs of the FP8 codes in bytes 0, 1 (lo) and 2, 3 (hi) of w.
+template <bool E5M2>
+__device__ __forceinline__ uint32_t fp8x2_lo(uint32_t w)
+{
+    return E5M2 ? e5m2x2_to_f16x2<false>(w) : e4m3x2_to_f16x2(w & 0xffffu);
+}
+template <bool E5M2>
+__device__ __forceinline__ uint32_t fp8x2_hi(uint32_t w)
+{
+    return E5M2 ? e5m2x2_to_f16x2<true>(w) : e4m3x2_to_f16x2(w >> 16);
+}
+
+// Two fp32 -> two E5M2 codes (lo -> low byte), round to nearest even, saturating
+// to the largest finite magnitude.
+__device__ __forceinline__ uint32_t f32x2_to_e5m2x2(float lo, float hi)
+{
+    unsigned short d;
+    asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
     return d;
 }
 
@@ -426,6 +470,23 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
                  : "r"(taddr));
+}
+
+// 16 consecutive 32-bit TMEM columns of this thread's lane (warp-collective).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16])
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+                 : "r"(taddr));
+}
+
+// Store 8 consecutive 32-bit TMEM columns of this thread's lane (warp-collective).
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                 :
+                 : "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
 }
 
 // Store 32 consecutive 32-bit TMEM columns of this thread's lane (warp-collective).

@@ -31,14 +31,15 @@ struct DecodeParams {
     int32_t max_blocks, num_blocks, n_ring_rows;
     int32_t B, Hkv, W;
     int16_t T, G;                // query tokens per sequence; query heads per KV head
-    int32_t flags;               // kDecodeRing | kDecodeAppend
+    int32_t flags;               // kDecode* bits below
     float scale_log2;            // softmax scale * log2(e)
 };
 constexpr int32_t kDecodeRing = 1;    // sliding layer: read the SWA ring
 constexpr int32_t kDecodeAppend = 2;  // append the T new rows (hsa_decode_attn_append)
-constexpr int32_t kDecodeFp8 = 4;     // full layer stored as E4M3 codes + scales (fp8_kv.cuh)
+constexpr int32_t kDecodeFp8 = 4;     // full layer stored as FP8 codes + scales (fp8_kv.cuh)
 constexpr int32_t kDecodeEarly = 8;   // sliding layer: walk and load the ring before the
                                       // grid-dependency wait (HSA_DECODE_EARLY_POOL_READ)
+constexpr int32_t kDecodeE5M2 = 16;   // with kDecodeFp8: the codes are E5M2 (else E4M3)
 static_assert(sizeof(DecodeParams) <= 128, "keep the decode parameter struct <= 128 bytes");
 
 // Bytes of the arrival-counter region at the start of a decode workspace.
@@ -70,7 +71,8 @@ struct AppendParams {
     int32_t R, ntok, Hkv, chunks_per_row;  // chunks_per_row = d * 2 / 16
     int32_t batch, max_blocks, num_blocks, page_size, n_ring_rows, W;
     int32_t ring_mode;
-    int32_t fp8;                 // full layer stored as E4M3 codes + scales (fp8_kv.cuh)
+    int32_t fp8;                 // full layer stored as FP8 codes + scales (fp8_kv.cuh):
+                                 // 0 bf16, 1 E4M3, 2 E5M2
 };
 
 cudaError_t launch_append(const AppendParams &p, cudaStream_t stream);

@@ -18,8 +18,8 @@ def make_pool(inst, layers=None, device="cuda", stale="random", max_bytes=1 << 3
 
     Pool layer i is model layer layers[i].  `stale` = "random" fills unwritten pool
     rows with random bf16 (so that reading them would show), "zero" zero-fills.
-    fp8=True stores the full layers as FP8 layers (zero-filled, quantised on
-    append by the library); sliding rings stay bf16.
+    fp8=True / "e4m3" / "e5m2" stores the full layers as FP8 layers of that format
+    (zero-filled, quantised on append by the library); sliding rings stay bf16.
     """
     cfg = inst.cfg
     layers = list(range(cfg.n_layers)) if layers is None else list(layers)
@@ -29,7 +29,7 @@ def make_pool(inst, layers=None, device="cuda", stale="random", max_bytes=1 << 3
         rr = torch.from_numpy(inst.ring_row).to(device)
         pool = hsa.DualPool.allocate(full, inst.num_blocks, inst.n_ring_rows, bt, rr, cfg.Hq,
                                      cfg.Hkv, d=cfg.d, W=cfg.W, page=cfg.page, device=device,
-                                     kv_fp8=True)
+                                     kv_fp8=fp8)
         for i, l in enumerate(layers):
             fill_layer(inst, pool, i, l, device, max_bytes=max_bytes)
         return pool

@@ -61,6 +61,10 @@ typedef int hsa_status;
 #define HSA_DEVERR_TIMEOUT 32    /* a bounded wait inside a kernel (2 s) gave up: the kernel
                                     stopped early and its outputs are incomplete */
 
+/* FP8 formats of a Full KV Pool layer (hsa_pools.layer_kv_fp8). */
+#define HSA_KV_E4M3 1
+#define HSA_KV_E5M2 2
+
 /*
  * The dual KV pool of one model (host struct of device pointers).
  *  layer_is_full[l]  host uint8: 1 = full layer (Full KV Pool), 0 = sliding layer.
@@ -74,14 +78,16 @@ typedef int hsa_status;
  *                    allocation are never read.
  *  ring_row          device int32 [batch]: the SWA ring row of each sequence,
  *                    shared by every sliding layer.
- *  layer_kv_fp8      host uint8 [n_layers] or NULL: 1 = this full layer is an FP8
- *                    Full KV Pool layer [hotdry.top "MiMo inference optimization, edge
- *                    deployment", "KV Cache 量化策略的技术选型": FP8 KV, quantisation
+ *  layer_kv_fp8      host uint8 [n_layers] or NULL: HSA_KV_E4M3 (1) or HSA_KV_E5M2
+ *                    (2) = this full layer is an FP8 Full KV Pool layer of that
+ *                    format, 0 = bf16, any other value HSA_INVALID_ARG
+ *                    [hotdry.top "MiMo inference optimization, edge deployment",
+ *                    "KV Cache 量化策略的技术选型": FP8 KV (E4M3 / E5M2), quantisation
  *                    groups aligned to the window; "边缘部署的工程权衡与参数清单": the
  *                    newest 128 tokens at the original precision -- a sliding
  *                    layer's ring, which holds exactly those, stays bf16].  Then k[l]
  *                    and v[l] each point to num_blocks * Hkv * 64 * (d + 4) bytes:
- *                    E4M3 codes, then one fp32 scale per (block, head, row):
+ *                    FP8 codes, then one fp32 scale per (block, head, row):
  *                      codes  [num_blocks * Hkv * 64 * d] bytes, then
  *                      scales [num_blocks * Hkv * 64] fp32, index (block*Hkv + h)*64 + row
  *                    K codes: page (block, h) = 64 rows of d bytes; dimension c of a
@@ -89,13 +95,15 @@ typedef int hsa_status;
  *                    page (block, h) = d rows of 64 bytes; key row r of dimension c at
  *                    byte 16*(r/16) + perm16(r%16) of row c.
  *                    perm16(l) = 4*((l%8)/2) + (l%2) + 2*(l/8).
- *                    scale = amax / 448 of the row's d values (fp32 division), code =
- *                    E4M3 of value / scale (round to nearest even, saturating); an
- *                    all-zero row stores scale 0.  hsa_kv_append and
+ *                    scale = amax / F of the row's d values (fp32 division), F = 448
+ *                    (E4M3) or 57344 (E5M2), the format's largest finite magnitude;
+ *                    code = FP8 of value / scale (round to nearest even, saturating);
+ *                    an all-zero row stores scale 0.  hsa_kv_append and
  *                    hsa_decode_attn_append quantise on write; decode reads such
  *                    layers; prefill rejects them (HSA_UNSUPPORTED_SHAPE), as does a
  *                    sliding layer flagged FP8.  Decode multiplies in fp16 there:
- *                    q, the new rows and |v| * 256 / 448 must stay within fp16 range.
+ *                    q, the new rows and |v| * 256 / 448 (E4M3) or |v| * 256 / 57344
+ *                    (E5M2) must stay within fp16 range.
  * Supported shape: d = 128, page_size = 64, W a multiple of 64 in [64, 256],
  * Hq a multiple of Hkv with Hq / Hkv in {1, 2, 4, 8}.
  */

@@ -135,6 +135,8 @@ _BAD_POOLS = [
     (dict(ring_row=None), 0, "HSA_INVALID_ARG"),    # sliding layer without ring rows
     (dict(n_ring_rows=0), 0, "HSA_INVALID_ARG"),
     (dict(fp8=[1, 0]), 0, "HSA_UNSUPPORTED_SHAPE"),  # a sliding layer flagged FP8
+    (dict(fp8=[2, 0]), 0, "HSA_UNSUPPORTED_SHAPE"),  # ... flagged E5M2
+    (dict(fp8=[0, 3]), 1, "HSA_INVALID_ARG"),        # no FP8 format 3
     (dict(), 2, "HSA_INVALID_ARG"),                 # layer index past n_layers
     (dict(), -1, "HSA_INVALID_ARG"),
 ]

@@ -1,4 +1,4 @@
-"""FP8 (E4M3) Full KV Pool variant for decode, through the C ABI.
+"""FP8 (E4M3 and E5M2) Full KV Pool variant for decode, through the C ABI.
 
 Pools: the codes and scales the library writes (hsa_kv_append and the fused
 append of hsa_decode_attn_append) equal the oracle's quantisation of the same
@@ -54,52 +54,59 @@ def _gather(inst, arr, s, n):
     return arr[blk, :, off]
 
 
-def _fp8_case(inst, layer, seqs):
+FORMATS = oracle.FP8_FORMATS
+
+
+def _fp8_case(inst, layer, seqs, fmt):
     c = harness.oracle_case(inst, layer, seqs)
-    hk, hks = oracle.quantize_e4m3(c["hist_k"])
-    hv, hvs = oracle.quantize_e4m3(c["hist_v"])
+    hk, hks = oracle.quantize_fp8(c["hist_k"], fmt)
+    hv, hvs = oracle.quantize_fp8(c["hist_v"], fmt)
     return dict(cu_rows=c["cu_rows"], prefix_len=c["prefix_len"], q=c["q"], k_new=c["k_new"],
-                v_new=c["v_new"], hk=hk, hks=hks, hv=hv, hvs=hvs, hist_off=c["hist_off"])
+                v_new=c["v_new"], hk=hk, hks=hks, hv=hv, hvs=hvs, hist_off=c["hist_off"],
+                fmt=fmt)
 
 
+@pytest.mark.parametrize("fmt", FORMATS)
 @pytest.mark.parametrize("name,R", [("tiny", None), ("decode", 3)])
-def test_fp8_append_bit_exact(name, R):
+def test_fp8_append_bit_exact(name, R, fmt):
     _cuda()
     inst = workload.draw(workload.CONFIGS[name], R=R)
     full_layer = next(l for l in range(inst.cfg.n_layers) if inst.full[l])
-    pool = harness.make_pool(inst, [full_layer], fp8=True)
+    pool = harness.make_pool(inst, [full_layer], fp8=fmt)
     kc, ks, vc, vs = _logical(pool, 0)
     for s in range(inst.R):
         hk, hv, st = workload.history(inst, full_layer, s, "cuda")
         assert st == 0
         n = hk.shape[0]
-        ek, eks = oracle.quantize_e4m3(hk.cpu())
-        ev, evs = oracle.quantize_e4m3(hv.cpu())
+        ek, eks = oracle.quantize_fp8(hk.cpu(), fmt)
+        ev, evs = oracle.quantize_fp8(hv.cpu(), fmt)
         assert np.array_equal(_gather(inst, kc, s, n), ek), "K codes, seq %d" % s
         assert np.array_equal(_gather(inst, ks, s, n), eks), "K scales, seq %d" % s
         assert np.array_equal(_gather(inst, vc, s, n), ev), "V codes, seq %d" % s
         assert np.array_equal(_gather(inst, vs, s, n), evs), "V scales, seq %d" % s
 
 
-def test_fp8_decode_parity_tiny_all_rows():
+@pytest.mark.parametrize("fmt", FORMATS)
+def test_fp8_decode_parity_tiny_all_rows(fmt):
     hsa = _cuda()
     inst = workload.draw(workload.CONFIGS["tiny"])
     l = 6
-    pool = harness.make_pool(inst, [l], fp8=True)
+    pool = harness.make_pool(inst, [l], fp8=fmt)
     q, k, v, cl = harness.decode_inputs(inst, l)
     out = hsa.hsa_decode_attn(pool, 0, q, k, v, cl, inst.cfg.scale)
     torch.cuda.synchronize()
-    ref = oracle.attention_fp8hist(scale=inst.cfg.scale, **_fp8_case(inst, l, range(inst.R)))
+    ref = oracle.attention_fp8hist(scale=inst.cfg.scale,
+                                   **_fp8_case(inst, l, range(inst.R), fmt))
     got = out.view(-1, inst.cfg.Hq, inst.cfg.d).float().cpu().numpy()
     err = float(np.max(np.abs(got - ref)))
     assert err <= TOL, err
 
 
-def _sampled(hsa, name, R=None, seed=0):
+def _sampled(hsa, name, R=None, seed=0, fmt="e4m3"):
     cfg = workload.CONFIGS[name]
     inst = workload.draw(cfg, R=R)
     l = 6
-    pool = harness.make_pool(inst, [l], fp8=True)
+    pool = harness.make_pool(inst, [l], fp8=fmt)
     B, T = inst.R, cfg.T
     q, k, v, cl = harness.decode_inputs(inst, l)
     ws = hsa.decode_workspace(pool, B, T)
@@ -115,7 +122,8 @@ def _sampled(hsa, name, R=None, seed=0):
                   {int(x) for x in rng.choice(B, size=min(2, B), replace=False)})
     items = np.array([(s * T + t, int(h)) for s in seqs for t in range(T)
                       for h in rng.choice(cfg.Hq, size=4, replace=False)], np.int32)
-    ref = oracle.attention_fp8hist(scale=cfg.scale, items=items, **_fp8_case(inst, l, seqs))
+    ref = oracle.attention_fp8hist(scale=cfg.scale, items=items,
+                                   **_fp8_case(inst, l, seqs, fmt))
     got = out.view(B * T, cfg.Hq, cfg.d).float().cpu().numpy()[items[:, 0], items[:, 1]]
     e = float(np.max(np.abs(got - ref)))
     assert e <= TOL, "%s: max abs err %g" % (name, e)
@@ -123,8 +131,8 @@ def _sampled(hsa, name, R=None, seed=0):
     kc, ks, vc, vs = _logical(pool, 0)
     pg = cfg.page
     for s in seqs:
-        ek, eks = oracle.quantize_e4m3(k[s].cpu())
-        ev, evs = oracle.quantize_e4m3(v[s].cpu())
+        ek, eks = oracle.quantize_fp8(k[s].cpu(), fmt)
+        ev, evs = oracle.quantize_fp8(v[s].cpu(), fmt)
         for t in range(T):
             pos = int(inst.prefix[s]) + t
             blk = int(inst.block_tables[s, pos // pg])
@@ -134,12 +142,14 @@ def _sampled(hsa, name, R=None, seed=0):
             assert np.array_equal(vs[blk, :, pos % pg], evs[t])
 
 
-def test_fp8_decode_full_size_sampled():
-    _sampled(_cuda(), "decode")
+@pytest.mark.parametrize("fmt", FORMATS)
+def test_fp8_decode_full_size_sampled(fmt):
+    _sampled(_cuda(), "decode", fmt=fmt)
 
 
-def test_fp8_mtp_verify_sampled():
-    _sampled(_cuda(), "mtp", R=8)
+@pytest.mark.parametrize("fmt", FORMATS)
+def test_fp8_mtp_verify_sampled(fmt):
+    _sampled(_cuda(), "mtp", R=8, fmt=fmt)
 
 
 def test_fp8_layers_are_decode_only():
@@ -162,10 +172,17 @@ def test_fp8_layers_are_decode_only():
     with pytest.raises(hsa.HsaError) as e:
         hsa.hsa_decode_attn(both, 0, q, k, v, cl, inst.cfg.scale)
     assert e.value.status == hsa.HSA_UNSUPPORTED_SHAPE
+    both._fp8[0] = 0
+    both._fp8[1] = 3  # no such format
+    q, k, v, cl = harness.decode_inputs(inst, 6)
+    with pytest.raises(hsa.HsaError) as e:
+        hsa.hsa_decode_attn(both, 1, q, k, v, cl, inst.cfg.scale)
+    assert e.value.status == hsa.HSA_INVALID_ARG
 
 
+@pytest.mark.parametrize("fmt", FORMATS)
 @pytest.mark.parametrize("T", [1, 2, 4])
-def test_fp8_ragged_contexts(T):
+def test_fp8_ragged_contexts(T, fmt):
     """Empty, one-token, page-edge and partial-page contexts with 1, 2 and 4 new
     tokens on an FP8 full layer, every row against the oracle; the fused append's
     codes bit-exact."""
@@ -176,20 +193,20 @@ def test_fp8_ragged_contexts(T):
                               index=70 + T)
     inst = workload.draw(cfg)
     l = 6
-    pool = harness.make_pool(inst, [l], fp8=True)
+    pool = harness.make_pool(inst, [l], fp8=fmt)
     q, k, v, cl = harness.decode_inputs(inst, l)
     ws = hsa.decode_workspace(pool, inst.R, T)
     out = hsa.hsa_decode_attn_append(pool, 0, q, k, v, cl, cfg.scale, workspace=ws)
     torch.cuda.synchronize()
-    ref = oracle.attention_fp8hist(scale=cfg.scale, **_fp8_case(inst, l, range(inst.R)))
+    ref = oracle.attention_fp8hist(scale=cfg.scale, **_fp8_case(inst, l, range(inst.R), fmt))
     got = out.view(-1, cfg.Hq, cfg.d).float().cpu().numpy()
     err = float(np.max(np.abs(got - ref)))
     assert err <= TOL, "T=%d: %g" % (T, err)
     kc, ks, vc, vs = _logical(pool, 0)
     pg = cfg.page
     for s in range(inst.R):
-        ek, eks = oracle.quantize_e4m3(k[s].cpu())
-        ev, evs = oracle.quantize_e4m3(v[s].cpu())
+        ek, eks = oracle.quantize_fp8(k[s].cpu(), fmt)
+        ev, evs = oracle.quantize_fp8(v[s].cpu(), fmt)
         for t in range(T):
             pos = int(inst.prefix[s]) + t
             blk = int(inst.block_tables[s, pos // pg])
