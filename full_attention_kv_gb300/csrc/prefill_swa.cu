@@ -32,11 +32,13 @@
 //  * Two shared-memory stages (q + K, and V, of one tile, each freed as soon as the
 //    MMA that reads it has run) and two TMEM slots (S, P, O of one tile); tile n uses
 //    stage and slot n mod 2.  Warp 0 = TMA producer; warp 1 = TMEM owner and
-//    single-thread MMA issuer (S(n), then PV(n-1)); warps 2-5 = softmax and epilogue,
-//    one query row per thread (TMEM lane = row): the softmax of tile n reads the
-//    row's scores from TMEM once and keeps them in registers for both passes (six
-//    warps, so 255 registers a thread), then the epilogue of tile n - 1 runs while
-//    PV(n) is on the tensor cores.
+//    single-thread MMA issuer (S(n), then PV(n-1)); warps 2-9 = softmax and epilogue,
+//    two warps per TMEM lane quarter (TMEM lane = query row), each taking half of
+//    the row's key columns and half of its output columns, so that every SM
+//    sub-partition has two softmax warps to interleave: the softmax of tile n reads
+//    the half-row's scores from TMEM once and keeps them in registers for both
+//    passes, the pair combines the row max and sum through shared memory, then the
+//    epilogue of tile n - 1 runs while PV(n) is on the tensor cores.
 //  * TMEM slot (256 columns): S at [0, N); P as bf16 pairs over S's first N/2
 //    columns; O at [128, 256), written by the PV MMA once the softmax has read all of
 //    S.  The epilogue divides O by the row sum (of the bf16 P the MMA used) and
@@ -53,10 +55,16 @@ constexpr int kKvRows = 160;               // key capacity of a stage
 constexpr int kBox = 16;                   // rows per K / V TMA box
 constexpr int kQHalf = kBM * 128;          // 128 rows x 64 bf16 (one swizzle column block)
 constexpr int kKvHalf = kKvRows * 128;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSlotCols = 256;
 constexpr uint32_t kColO = 128;
+// Columns of a TMEM slot the two halves of a row pass values through (per lane, so
+// per row): the halves' maxima of tile n sit in O's columns past S (O is written
+// only by PV(n), after the softmax), their row sums in S's columns past P (free
+// once both halves have read S, until S(n + 2) -- after tile n's epilogue).
+constexpr uint32_t kColMax = kKvRows;         // + half
+constexpr uint32_t kColSum = kKvRows / 2;     // + half
 
 struct TileInfo {
     int32_t valid;     // 0: a bad request -- nothing loaded, nothing written
@@ -111,16 +119,16 @@ __device__ __forceinline__ uint32_t range_mask(int c0, int lo, int hi)
     return below_b & ~((1u << a) - 1u);  // a < b <= 32, so a < 32
 }
 
-// Scores of the columns whose bit in vm is clear become -inf; skipped when every
+// Scores of the 16 columns whose bit in vm is clear become -inf; skipped when every
 // lane of the warp sees the whole chunk (the common case inside a tile).
-__device__ __forceinline__ void mask_chunk(uint32_t (&r32)[32], uint32_t vm)
+__device__ __forceinline__ void mask_chunk16(uint32_t (&r)[16], uint32_t vm)
 {
-    if (__all_sync(0xffffffffu, vm == 0xffffffffu))
+    if (__all_sync(0xffffffffu, (vm & 0xffffu) == 0xffffu))
         return;
 #pragma unroll
-    for (int c = 0; c < 32; ++c)
+    for (int c = 0; c < 16; ++c)
         if (!(vm & (1u << c)))
-            r32[c] = __float_as_uint(-INFINITY);
+            r[c] = __float_as_uint(-INFINITY);
 }
 
 // Request cursor of the producer's tile walk (tiles are dealt in request order).
@@ -223,9 +231,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&sh.full_v[s], 1);
             mbar_init(&sh.empty_v[s], 1);
             mbar_init(&sh.s_full[s], 1);
-            mbar_init(&sh.p_full[s], 4 * 32);
+            mbar_init(&sh.p_full[s], 8 * 32);
             mbar_init(&sh.o_full[s], 1);
-            mbar_init(&sh.t_free[s], 4 * 32);
+            mbar_init(&sh.t_free[s], 8 * 32);
         }
         for (int j = 0; j < 4; ++j)
             mbar_init(&sh.info_full[j], 1);
@@ -417,87 +425,109 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ================================================================ softmax + epilogue
-        // Warps 2-5 (one per TMEM lane quarter), one query row per thread, every tile
-        // in turn: the softmax of tile k, then the epilogue of tile k - 1 while PV(k)
+        // Warps 2-9: two per TMEM lane quarter, one query row per pair of threads.
+        // Half 0 (warps 2-5) takes key columns [0, 80) and output columns [0, 64),
+        // half 1 (warps 6-9) key columns [80, 160) and output columns [64, 128); the
+        // two warps of a quarter meet at a 64-thread barrier of their own to combine
+        // the row max (every tile) and the row sum (for the epilogue).  Every tile in
+        // turn: the softmax of tile k, then the epilogue of tile k - 1 while PV(k)
         // runs on the tensor cores.
-        const int wq = warp & 3;       // TMEM lane quarter of this warp
-        const int m = wq * 32 + lane;  // query row of the tile: position m / G, head m % G
+        const int wq = warp & 3;             // TMEM lane quarter of this warp
+        const int half = (warp - 2) >> 2;    // key / output column half
+        const int m = wq * 32 + lane;        // query row of the tile: position m / G, head m % G
         const int u = m / p.G, g = m % p.G;
         const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
+        const uint32_t pair_bar = 1 + wq;    // named barrier of the quarter's two warps
         TileInfo prev{};
-        float prev_l = 0.f;
+        // A wait that gives up never leaves one warp of a pair behind at a barrier:
+        // `ok` (this warp's waits so far) goes into the pair barrier of the next tile,
+        // which both warps reach and leave with the same answer.
         bool ok = true;
-        for (int k = 0; k <= n_my && ok; ++k) {
-            float l = 0.f;
+        for (int k = 0; k <= n_my; ++k) {
             TileInfo inf{};
-            if (k < n_my) {
-                const int s = k & 1;
-                const uint32_t ph = (k >> 1) & 1;
-                if (!mbar_wait_sleep(&sh.info_full[k & 3], (k >> 2) & 1) ||
-                    !mbar_wait_sleep(&sh.s_full[s], ph)) {
-                    ok = false;
-                    break;
-                }
+            const int s = k & 1;
+            const uint32_t base = lane_addr + s * kSlotCols;
+            bool w_ok = ok;
+            if (k < n_my && w_ok)
+                w_ok = mbar_wait_sleep(&sh.info_full[k & 3], (k >> 2) & 1) &&
+                       mbar_wait_sleep(&sh.s_full[s], (k >> 1) & 1);
+            w_ok = __all_sync(0xffffffffu, w_ok);  // the TMEM reads below are warp-wide
+            // This half's <= 80 scores: one TMEM read of each 16-column chunk, one
+            // wait, kept in registers for both passes.  Invisible scores become -inf
+            // (skipped for a chunk every row of the warp sees whole).
+            constexpr int kChunks = kKvRows / 32;  // 16-column chunks per half
+            const int c_base = half * kChunks * 16;
+            uint32_t sr[kChunks][16];
+            int n = 0;
+            if (k < n_my && w_ok) {
                 tc_fence_after();
                 inf = sh.info[k & 3];
                 const int i = inf.i0 + u;
                 const bool row_ok = inf.valid && i < inf.C;
-                const uint32_t base = lane_addr + s * kSlotCols;
-                if (inf.valid) {
-                    const int n = inf.nr + inf.nc;
-                    // visible key columns: ring region [rlo, rhi), chunk region [clo, chi)
-                    int rlo = 0, rhi = 0, clo = 0, chi = 0;
-                    if (row_ok) {
-                        if (inf.nr > 0) {
-                            rlo = max(0, inf.P + i - p.W + 1) - inf.a0;
-                            rhi = max(rlo, inf.P - inf.a0);
-                        }
-                        clo = inf.nr + max(0, i - p.W + 1) - inf.z0;
-                        chi = inf.nr + i + 1 - inf.z0;
+                n = inf.valid ? inf.nr + inf.nc : 0;
+                // visible key columns: ring region [rlo, rhi), chunk region [clo, chi)
+                int rlo = 0, rhi = 0, clo = 0, chi = 0;
+                if (row_ok) {
+                    if (inf.nr > 0) {
+                        rlo = max(0, inf.P + i - p.W + 1) - inf.a0;
+                        rhi = max(rlo, inf.P - inf.a0);
                     }
-                    // The row's n <= kKvRows scores: one TMEM read of every chunk, then a
-                    // single wait, kept in registers for both passes (a TMEM read's
-                    // latency is paid once a tile).  Invisible scores become -inf (a
-                    // 32-bit mask per chunk; a chunk every row of the warp sees whole
-                    // skips it).
-                    constexpr int kChunks = kKvRows / 32;
-                    const int nch = (n + 31) >> 5;
-                    uint32_t sr[kChunks][32];
+                    clo = inf.nr + max(0, i - p.W + 1) - inf.z0;
+                    chi = inf.nr + i + 1 - inf.z0;
+                }
 #pragma unroll
-                    for (int ci = 0; ci < kChunks; ++ci)
-                        if (ci < nch)
-                            tmem_ld32(base + ci * 32, sr[ci]);
+                for (int ci = 0; ci < kChunks; ++ci)
+                    if (c_base + ci * 16 < n)
+                        tmem_ld16(base + c_base + ci * 16, sr[ci]);
+                tmem_wait_ld();
+                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                for (int ci = 0; ci < kChunks; ++ci) {
+                    const int c0 = c_base + ci * 16;
+                    if (c0 < n) {
+                        mask_chunk16(sr[ci], range_mask(c0, rlo, rhi) | range_mask(c0, clo, chi));
+#pragma unroll
+                        for (int c = 0; c < 16; c += 8) {
+                            m4[0] = fmax3(m4[0], __uint_as_float(sr[ci][c + 0]), __uint_as_float(sr[ci][c + 1]));
+                            m4[1] = fmax3(m4[1], __uint_as_float(sr[ci][c + 2]), __uint_as_float(sr[ci][c + 3]));
+                            m4[2] = fmax3(m4[2], __uint_as_float(sr[ci][c + 4]), __uint_as_float(sr[ci][c + 5]));
+                            m4[3] = fmax3(m4[3], __uint_as_float(sr[ci][c + 6]), __uint_as_float(sr[ci][c + 7]));
+                        }
+                    }
+                }
+                tmem_st1(base + kColMax + half,
+                         __float_as_uint(fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]))));
+                tmem_wait_st();
+            }
+            // the pair meets: both halves' maxima (and, for the epilogue below, the
+            // other half's row sum of tile k - 1) are in TMEM, and both have read
+            // their S before either writes P over S's first columns
+            tc_fence_before();
+            if (!named_bar_and(pair_bar, 64, w_ok)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            if (k < n_my) {
+                if (n > 0) {
+                    uint32_t m0, m1;
+                    tmem_ld2(base + kColMax, m0, m1);
                     tmem_wait_ld();
-                    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-                    for (int ci = 0; ci < kChunks; ++ci) {
-                        if (ci < nch) {
-                            const int c0 = ci * 32;
-                            mask_chunk(sr[ci], range_mask(c0, rlo, rhi) | range_mask(c0, clo, chi));
-#pragma unroll
-                            for (int c = 0; c < 32; c += 8) {
-                                m4[0] = fmax3(m4[0], __uint_as_float(sr[ci][c + 0]), __uint_as_float(sr[ci][c + 1]));
-                                m4[1] = fmax3(m4[1], __uint_as_float(sr[ci][c + 2]), __uint_as_float(sr[ci][c + 3]));
-                                m4[2] = fmax3(m4[2], __uint_as_float(sr[ci][c + 4]), __uint_as_float(sr[ci][c + 5]));
-                                m4[3] = fmax3(m4[3], __uint_as_float(sr[ci][c + 6]), __uint_as_float(sr[ci][c + 7]));
-                            }
-                        }
-                    }
-                    const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                    const float mx = fmaxf(__uint_as_float(m0), __uint_as_float(m1));
                     const float mb = mx == -INFINITY ? 0.f : mx * p.scale_log2;
-                    // P = 2^(s scale log2e - max) as bf16 pairs over S's first columns
-                    // (chunk c writes columns 16 c .. 16 c + 15; a masked score gives
-                    // 2^-inf = 0).  The row sum takes the rounded P the PV MMA uses, in
-                    // two independent f32x2 accumulators.
+                    // P = 2^(s scale log2e - max) as bf16 pairs: key column c goes to P
+                    // column c / 2 (chunk ci to columns c_base / 2 + 8 ci .. + 7; a
+                    // masked score gives 2^-inf = 0).  The row sum takes the rounded P
+                    // the PV MMA uses, in two independent f32x2 accumulators.
                     const uint64_t sc2 = f2_make(p.scale_log2, p.scale_log2);
                     const uint64_t nb2 = f2_make(-mb, -mb);
                     uint64_t acc2[2] = {f2_make(0.f, 0.f), f2_make(0.f, 0.f)};
 #pragma unroll
                     for (int ci = 0; ci < kChunks; ++ci) {
-                        if (ci < nch) {
-                            uint32_t pk[16];
+                        if (c_base + ci * 16 < n) {
+                            uint32_t pk[8];
 #pragma unroll
-                            for (int c = 0; c < 16; ++c) {
+                            for (int c = 0; c < 8; ++c) {
                                 const uint64_t x2 = f2_fma(f2_make(__uint_as_float(sr[ci][2 * c]),
                                                                    __uint_as_float(sr[ci][2 * c + 1])),
                                                            sc2, nb2);
@@ -506,54 +536,56 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 pk[c] = pack_bf16(fast_exp2(x0), fast_exp2(x1));
                                 acc2[c & 1] = f2_add(acc2[c & 1], f2_make(bf16_lo(pk[c]), bf16_hi(pk[c])));
                             }
-                            tmem_st16(base + ci * 16, pk);
+                            tmem_st8(base + c_base / 2 + ci * 8, pk);
                         }
                     }
                     float a0, a1, b0, b1;
                     f2_split(acc2[0], a0, a1);
                     f2_split(acc2[1], b0, b1);
-                    l = (a0 + a1) + (b0 + b1);
+                    tmem_st1(base + kColSum + half, __float_as_uint((a0 + a1) + (b0 + b1)));
                     tmem_wait_st();
                 }
                 tc_fence_before();
                 mbar_arrive(&sh.p_full[s]);
             }
-            // ---- epilogue of tile k - 1: O / l -> bf16 ---------------------------
+            // ---- epilogue of tile k - 1: O / l -> bf16, this half's 64 columns ----
+            // (the other half's row sum of tile k - 1 was written before it reached
+            // this iteration's pair barrier)
             if (k > 0) {
                 const int j = k - 1;
                 const int s = j & 1;
-                if (!mbar_wait_sleep(&sh.o_full[s], (j >> 1) & 1)) {
-                    ok = false;
-                    break;
+                if (!__all_sync(0xffffffffu, mbar_wait_sleep(&sh.o_full[s], (j >> 1) & 1))) {
+                    ok = false;  // left at the next pair barrier, by both warps
+                    continue;
                 }
                 tc_fence_after();
                 if (prev.valid) {
                     const int i = prev.i0 + u;
                     const bool row_ok = i < prev.C;
-                    const float inv = prev_l > 0.f ? 1.f / prev_l : 0.f;
-                    const uint32_t base = lane_addr + s * kSlotCols + kColO;
+                    uint32_t l0, l1;
+                    tmem_ld2(lane_addr + s * kSlotCols + kColSum, l0, l1);
+                    tmem_wait_ld();
+                    const float l = __uint_as_float(l0) + __uint_as_float(l1);
+                    const float inv = l > 0.f ? 1.f / l : 0.f;
+                    const uint32_t base = lane_addr + s * kSlotCols + kColO + half * 64;
                     __nv_bfloat16 *dst =
-                        p.out + ((int64_t)(prev.row_base + i) * p.Hq + prev.h * p.G + g) * kD;
-                    // two halves of 64 columns (128 at once would share the registers
-                    // the softmax holds and spill)
+                        p.out + ((int64_t)(prev.row_base + i) * p.Hq + prev.h * p.G + g) * kD +
+                        half * 64;
+                    uint32_t o32[2][32];
+                    tmem_ld32(base, o32[0]);
+                    tmem_ld32(base + 32, o32[1]);
+                    tmem_wait_ld();
+                    if (row_ok) {
 #pragma unroll
-                    for (int hf = 0; hf < 2; ++hf) {
-                        uint32_t o32[2][32];
-                        tmem_ld32(base + hf * 64, o32[0]);
-                        tmem_ld32(base + hf * 64 + 32, o32[1]);
-                        tmem_wait_ld();
-                        if (row_ok) {
+                        for (int c2 = 0; c2 < 2; ++c2) {
 #pragma unroll
-                            for (int c2 = 0; c2 < 2; ++c2) {
-#pragma unroll
-                                for (int c = 0; c < 32; c += 8) {
-                                    uint4 w;
-                                    w.x = pack_bf16(__uint_as_float(o32[c2][c + 0]) * inv, __uint_as_float(o32[c2][c + 1]) * inv);
-                                    w.y = pack_bf16(__uint_as_float(o32[c2][c + 2]) * inv, __uint_as_float(o32[c2][c + 3]) * inv);
-                                    w.z = pack_bf16(__uint_as_float(o32[c2][c + 4]) * inv, __uint_as_float(o32[c2][c + 5]) * inv);
-                                    w.w = pack_bf16(__uint_as_float(o32[c2][c + 6]) * inv, __uint_as_float(o32[c2][c + 7]) * inv);
-                                    *reinterpret_cast<uint4 *>(dst + hf * 64 + c2 * 32 + c) = w;
-                                }
+                            for (int c = 0; c < 32; c += 8) {
+                                uint4 w;
+                                w.x = pack_bf16(__uint_as_float(o32[c2][c + 0]) * inv, __uint_as_float(o32[c2][c + 1]) * inv);
+                                w.y = pack_bf16(__uint_as_float(o32[c2][c + 2]) * inv, __uint_as_float(o32[c2][c + 3]) * inv);
+                                w.z = pack_bf16(__uint_as_float(o32[c2][c + 4]) * inv, __uint_as_float(o32[c2][c + 5]) * inv);
+                                w.w = pack_bf16(__uint_as_float(o32[c2][c + 6]) * inv, __uint_as_float(o32[c2][c + 7]) * inv);
+                                *reinterpret_cast<uint4 *>(dst + c2 * 32 + c) = w;
                             }
                         }
                     }
@@ -562,7 +594,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(&sh.t_free[s]);
             }
             prev = inf;
-            prev_l = l;
         }
         if (!ok)
             set_err(p.dev_err, HSA_DEVERR_TIMEOUT);
