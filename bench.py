@@ -833,8 +833,8 @@ TRAFFIC = {
     ("prefill", "sliding"): ("prefill_swa.cu", "487bd58bef03179b", 809082368),
     # append_kernel, full-size launches (writes still held in L2 at the kernel's end
     # reach DRAM after it)
-    ("prefill", "append_full"): ("append.cu", "5b0ffb5eddb0d066", 146275328),
-    ("prefill", "append_sliding"): ("append.cu", "5b0ffb5eddb0d066", 2109184),
+    ("prefill", "append_full"): ("append.cu", "436d89e400666e68", 143246080),
+    ("prefill", "append_sliding"): ("append.cu", "436d89e400666e68", 2110464),
 }
 
 

@@ -30,19 +30,20 @@
 //    chain of N <= 160 columns and each row's softmax is exact: the row maximum is
 //    known before any exponential, no running max, no rescale of O.
 //  * Two shared-memory stages (q + K, and V, of one tile, each freed as soon as the
-//    MMA that reads it has run) and two TMEM slots (S, P, O of one tile); tile n uses
-//    stage and slot n mod 2.  Warp 0 = TMA producer; warp 1 = TMEM owner and
+//    MMA that reads it has run), two TMEM S slots (S, then P over it) and one O
+//    region; tile n uses stage and slot n mod 2.  Warp 0 = TMA producer; warp 1 = TMEM owner and
 //    single-thread MMA issuer (S(n), then PV(n-1)); warps 2-9 = softmax and epilogue,
 //    two warps per TMEM lane quarter (TMEM lane = query row), each taking half of
 //    the row's key columns and half of its output columns, so that every SM
 //    sub-partition has two softmax warps to interleave: the softmax of tile n reads
 //    the half-row's scores from TMEM once and keeps them in registers for both
-//    passes, the pair combines the row max and sum through shared memory, then the
-//    epilogue of tile n - 1 runs while PV(n) is on the tensor cores.
-//  * TMEM slot (256 columns): S at [0, N); P as bf16 pairs over S's first N/2
-//    columns; O at [128, 256), written by the PV MMA once the softmax has read all of
-//    S.  The epilogue divides O by the row sum (of the bf16 P the MMA used) and
-//    writes bf16.
+//    passes, the pair combines the row max and sum through TMEM, then the epilogue
+//    of tile n - 1 reads O, after which PV(n) runs while the softmax of tile n + 1
+//    does -- whose S the tensor cores computed during tile n's softmax.
+//  * TMEM: S slots at columns [0, N) and [192, 192 + N), P as bf16 pairs over the
+//    slot's first N/2 columns, O at [384, 512), written by PV(n) once the epilogue
+//    of tile n - 1 has read it.  The epilogue divides O by the row sum (of the bf16 P
+//    the MMA used) and writes bf16.
 #include "hsa_device.cuh"
 #include "hsa_internal.h"
 
@@ -56,15 +57,20 @@ constexpr int kBox = 16;                   // rows per K / V TMA box
 constexpr int kQHalf = kBM * 128;          // 128 rows x 64 bf16 (one swizzle column block)
 constexpr int kKvHalf = kKvRows * 128;
 constexpr int kThreads = 320;
+// TMEM: two S slots of kKvRows columns (tile n in slot n mod 2; P as bf16 pairs over
+// S's first columns) 192 columns apart, and one O region that every tile's PV
+// accumulates into in turn: S(n + 2) can then run while the epilogue of tile n
+// still reads O -- only PV(n + 1) waits for it.
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kSlotCols = 256;
-constexpr uint32_t kColO = 128;
-// Columns of a TMEM slot the two halves of a row pass values through (per lane, so
-// per row): the halves' maxima of tile n sit in O's columns past S (O is written
-// only by PV(n), after the softmax), their row sums in S's columns past P (free
-// once both halves have read S, until S(n + 2) -- after tile n's epilogue).
+constexpr uint32_t kSlotCols = 192;
+constexpr uint32_t kColO = 2 * kSlotCols;
+static_assert(kColO + 128 <= kTmemCols, "two S slots and O fit in TMEM");
+// Columns of an S slot past S (never written by an MMA) through which the two
+// halves of a row pass values (per lane, so per row): the halves' maxima of the
+// slot's tile, then their row sums, read by the tile's epilogue.
 constexpr uint32_t kColMax = kKvRows;         // + half
-constexpr uint32_t kColSum = kKvRows / 2;     // + half
+constexpr uint32_t kColSum = kKvRows + 2;     // + half
+static_assert(kColSum + 2 <= kSlotCols, "exchange columns inside the slot");
 
 struct TileInfo {
     int32_t valid;     // 0: a bad request -- nothing loaded, nothing written
@@ -82,12 +88,14 @@ struct SwaSmem {
     alignas(1024) uint8_t v[2][2 * kKvHalf];
     // stage s: q + K loaded / free (free once S has read them), V loaded / free
     alignas(8) uint64_t full_qk[2], empty_qk[2], full_v[2], empty_v[2];
-    uint64_t s_full[2], p_full[2], o_full[2], t_free[2];  // per TMEM slot
+    uint64_t s_full[2], p_full[2];  // per S slot
+    uint64_t o_full, o_free;        // O holds PV(n) / O read by the epilogue of tile n
     // description of tile k in info[k mod 4], published by info_full[k mod 4]: the
     // producer writes tile k + 4's once stage k mod 2 frees for it, i.e. after
-    // S(k + 2), which waits for tile k's epilogue -- so no slot is overwritten while
-    // its tile's warps may still read it, and its barrier cannot complete the next
-    // phase before they have waited on this one.  (The softmax warps must not wait on
+    // S(k + 2), which the MMA thread issues after PV(k), which waits for every
+    // softmax warp's P of tile k -- so no slot is overwritten while its tile's warps
+    // may still read it, and its barrier cannot complete the next phase before they
+    // have waited on this one.  (The softmax warps must not wait on
     // full_qk for this: that barrier completes again for tile k + 2 as soon as S(k)
     // has read stage k mod 2, possibly before a late waiter looks, and a parity wait
     // cannot tell two completions from none.)
@@ -232,9 +240,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&sh.empty_v[s], 1);
             mbar_init(&sh.s_full[s], 1);
             mbar_init(&sh.p_full[s], 8 * 32);
-            mbar_init(&sh.o_full[s], 1);
-            mbar_init(&sh.t_free[s], 8 * 32);
         }
+        mbar_init(&sh.o_full, 1);
+        mbar_init(&sh.o_free, 8 * 32);
         for (int j = 0; j < 4; ++j)
             mbar_init(&sh.info_full[j], 1);
         fence_barrier_init();
@@ -357,24 +365,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                 v_lo[s] = smem_desc_sw128_lo(smem_u32(sh.v[s]), kKvHalf);
             }
             int n_prev = 0;  // keys of the previous tile (0: invalid, no PV)
-            // O_s = P_s V_s over n keys: P from TMEM over S (k-step ks: 16 keys = 8
-            // columns of bf16 pairs), V the MN-major tile (16 key rows = 2048 bytes)
+            // O = P V over n keys: P from TMEM over S of slot s (k-step ks: 16 keys =
+            // 8 columns of bf16 pairs), V the MN-major tile (16 key rows = 2048 bytes)
             auto issue_pv = [&](int s, int n) {
                 const uint32_t base = tmem + s * kSlotCols;
                 if (n > 0) {
-                    tc_mma_ts_k<0>(base + kColO, base, desc_join(v_lo[s], dhi), id_pv);
+                    tc_mma_ts_k<0>(tmem + kColO, base, desc_join(v_lo[s], dhi), id_pv);
                     for (int ks = 1; ks < n / 16; ++ks)
-                        tc_mma_ts_k<1>(base + kColO, base + ks * 8,
+                        tc_mma_ts_k<1>(tmem + kColO, base + ks * 8,
                                        desc_join(v_lo[s] + ks * (2048 >> 4), dhi), id_pv);
                 }
-                tc_commit(&sh.o_full[s]);
+                tc_commit(&sh.o_full);
                 tc_commit(&sh.empty_v[s]);
+            };
+            // PV(j) waits for its P, its V and the epilogue of tile j - 1 (O free)
+            auto wait_pv = [&](int j) -> bool {
+                const int sp = j & 1;
+                const uint32_t php = (j >> 1) & 1;
+                return mbar_wait_sleep(&sh.p_full[sp], php) && mbar_wait_sleep(&sh.full_v[sp], php) &&
+                       mbar_wait_sleep(&sh.o_free, (j & 1) ^ 1);
             };
             bool ok = true;
             for (int k = 0; k < n_my && ok; ++k) {
                 const int s = k & 1;
                 const uint32_t ph = (k >> 1) & 1;
-                if (!mbar_wait_sleep(&sh.full_qk[s], ph) || !mbar_wait_sleep(&sh.t_free[s], ph ^ 1)) {
+                // slot s last held tile k - 2, whose P PV(k - 2) -- issued earlier by
+                // this thread, so run earlier -- has read
+                if (!mbar_wait_sleep(&sh.full_qk[s], ph)) {
                     ok = false;
                     break;
                 }
@@ -398,24 +415,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_commit(&sh.s_full[s]);
                 tc_commit(&sh.empty_qk[s]);  // q and K of stage s are free once S has run
                 if (k > 0) {
-                    const int sp = (k - 1) & 1;
-                    const uint32_t php = ((k - 1) >> 1) & 1;
-                    if (!mbar_wait_sleep(&sh.p_full[sp], php) ||
-                        !mbar_wait_sleep(&sh.full_v[sp], php)) {
+                    if (!wait_pv(k - 1)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    issue_pv(sp, n_prev);
+                    issue_pv((k - 1) & 1, n_prev);
                 }
                 n_prev = n;
             }
             if (ok) {
-                const int sp = (n_my - 1) & 1;
-                const uint32_t php = ((n_my - 1) >> 1) & 1;
-                if (mbar_wait_sleep(&sh.p_full[sp], php) && mbar_wait_sleep(&sh.full_v[sp], php)) {
+                if (wait_pv(n_my - 1)) {
                     tc_fence_after();
-                    issue_pv(sp, n_prev);
+                    issue_pv((n_my - 1) & 1, n_prev);
                 } else {
                     ok = false;
                 }
@@ -430,8 +442,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // half 1 (warps 6-9) key columns [80, 160) and output columns [64, 128); the
         // two warps of a quarter meet at a 64-thread barrier of their own to combine
         // the row max (every tile) and the row sum (for the epilogue).  Every tile in
-        // turn: the softmax of tile k, then the epilogue of tile k - 1 while PV(k)
-        // runs on the tensor cores.
+        // turn: the softmax of tile k, then the epilogue of tile k - 1, which frees O
+        // for PV(k).
         const int wq = warp & 3;             // TMEM lane quarter of this warp
         const int half = (warp - 2) >> 2;    // key / output column half
         const int m = wq * 32 + lane;        // query row of the tile: position m / G, head m % G
@@ -554,7 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (k > 0) {
                 const int j = k - 1;
                 const int s = j & 1;
-                if (!__all_sync(0xffffffffu, mbar_wait_sleep(&sh.o_full[s], (j >> 1) & 1))) {
+                if (!__all_sync(0xffffffffu, mbar_wait_sleep(&sh.o_full, j & 1))) {
                     ok = false;  // left at the next pair barrier, by both warps
                     continue;
                 }
@@ -567,7 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_wait_ld();
                     const float l = __uint_as_float(l0) + __uint_as_float(l1);
                     const float inv = l > 0.f ? 1.f / l : 0.f;
-                    const uint32_t base = lane_addr + s * kSlotCols + kColO + half * 64;
+                    const uint32_t base = lane_addr + kColO + half * 64;
                     __nv_bfloat16 *dst =
                         p.out + ((int64_t)(prev.row_base + i) * p.Hq + prev.h * p.G + g) * kD +
                         half * 64;
@@ -591,7 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 tc_fence_before();
-                mbar_arrive(&sh.t_free[s]);
+                mbar_arrive(&sh.o_free);
             }
             prev = inf;
         }
