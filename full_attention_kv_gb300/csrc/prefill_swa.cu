@@ -147,7 +147,7 @@ struct Cursor {
 // Describe tile t (the cursor only moves forward): its request, rows and the two key
 // regions; reports a bad request once (on its first tile) and marks it invalid.
 __device__ __forceinline__ void describe(const PrefillParams &p, int ppt, int t, Cursor &cur,
-                                         TileInfo &inf, int &rr)
+                                         TileInfo &inf, int &rr, bool may_report)
 {
     while (t >= cur.acc + cur.tr) {
         cur.acc += cur.tr;
@@ -163,7 +163,7 @@ __device__ __forceinline__ void describe(const PrefillParams &p, int ppt, int t,
     inf.C = __ldg(p.cu_rows + r + 1) - inf.row_base;
     inf.P = __ldg(p.prefix_len + r);
     const int seq = __ldg(p.seq_idx + r);
-    const bool report = inf.h == 0 && blk == 0;  // one report per request
+    const bool report = may_report && inf.h == 0 && blk == 0;  // one report per request
     inf.valid = 1;
     if (inf.row_base < 0 || inf.row_base + inf.C > p.rows) {
         if (report)
@@ -258,93 +258,105 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ================================================================ producer
+        // The whole warp: lane 0 waits for a stage and arms its barrier, then every
+        // lane issues one TMA box (a tile's q + K or V is up to 22 boxes of 16 rows x
+        // 64 columns: 16-row blocks never wrap the ring), so no single thread walks
+        // the boxes one by one.
         if (lane == 0) {
             tma_prefetch_desc(&tmQ);
             tma_prefetch_desc(&tmNK);
             tma_prefetch_desc(&tmNV);
             tma_prefetch_desc(&tmRK);
             tma_prefetch_desc(&tmRV);
-            const uint64_t pol_q = policy_evict_first();  // q is read once
-            const uint64_t pol_kv = policy_evict_last();  // a key serves ~W / ppt tiles
-            // Loads go out in the order their stages free up: q + K of tile k (stage
-            // k mod 2 is free once S(k-2) has read it), then V of tile k-1 (free once
-            // PV(k-3) has); a tile's description is read one tile ahead, so its
-            // global loads overlap the waits.
-            Cursor cur{0, 0, tiles_of(p, 0, ppt)};
-            TileInfo inf_next, inf_prev{};
-            int rr_next = 0, rr_prev = 0;
-            describe(p, ppt, (int)blockIdx.x, cur, inf_next, rr_next);
-            bool ok = true;
-            int k = 0;
-            auto load_v = [&](int j, const TileInfo &inf, int rr) -> bool {
-                const int s = j & 1;
-                if (!mbar_wait_sleep(&sh.empty_v[s], ((j >> 1) & 1) ^ 1))
-                    return false;
-                uint64_t *bar = &sh.full_v[s];
-                if (!inf.valid) {
-                    mbar_arrive(bar);
-                    return true;
+        }
+        const uint64_t pol_q = policy_evict_first();  // q is read once
+        const uint64_t pol_kv = policy_evict_last();  // a key serves ~W / ppt tiles
+        // Loads go out in the order their stages free up: q + K of tile k (stage k mod
+        // 2 is free once S(k-2) has read it), then V of tile k-1 (free once PV(k-3)
+        // has); a tile's description is read one tile ahead (by every lane, so that
+        // each knows the boxes), its global loads overlapping the waits.
+        Cursor cur{0, 0, tiles_of(p, 0, ppt)};
+        TileInfo inf_next, inf_prev{};
+        int rr_next = 0, rr_prev = 0;
+        describe(p, ppt, (int)blockIdx.x, cur, inf_next, rr_next, lane == 0);
+        // box e of a K or V region: e & 1 = 64-column half, e >> 1 = 16-row block
+        // (ring blocks first, then chunk blocks)
+        auto issue_kv = [&](uint8_t *dst, const TileInfo &inf, int rr, const CUtensorMap *ring,
+                            const CUtensorMap *chunk, uint64_t *bar, int e) {
+            const int half = e & 1, b = (e >> 1) * kBox;
+            uint8_t *d = dst + half * kKvHalf + b * 128;
+            if (b < inf.nr) {
+                const int y = (rr * p.Hkv + inf.h) * p.W + (inf.a0 + b) % p.W;
+                tma_load_2d(d, ring, bar, half * 64, y, pol_kv);
+            } else {
+                const int z = inf.row_base + inf.z0 + (b - inf.nr);
+                tma_load_3d(d, chunk, bar, half * 64, inf.h, z, pol_kv);
+            }
+        };
+        auto load_v = [&](int j, const TileInfo &inf, int rr) -> bool {
+            const int s = j & 1;
+            int ok_w = 1;
+            if (lane == 0) {
+                ok_w = mbar_wait_sleep(&sh.empty_v[s], ((j >> 1) & 1) ^ 1);
+                if (ok_w) {
+                    if (inf.valid)
+                        mbar_arrive_expect_tx(&sh.full_v[s], (inf.nr + inf.nc) * 256);
+                    else
+                        mbar_arrive(&sh.full_v[s]);
                 }
-                mbar_arrive_expect_tx(bar, (inf.nr + inf.nc) * 256);
-                for (int b = 0; b < inf.nr; b += kBox) {
-                    const int y = (rr * p.Hkv + inf.h) * p.W + (inf.a0 + b) % p.W;
-                    tma_load_2d(sh.v[s] + b * 128, &tmRV, bar, 0, y, pol_kv);
-                    tma_load_2d(sh.v[s] + kKvHalf + b * 128, &tmRV, bar, 64, y, pol_kv);
+            }
+            ok_w = __shfl_sync(0xffffffffu, ok_w, 0);  // also orders the copies after the arm
+            if (ok_w && inf.valid && lane < 2 * (inf.nr + inf.nc) / kBox)
+                issue_kv(sh.v[s], inf, rr, &tmRV, &tmNV, &sh.full_v[s], lane);
+            return ok_w != 0;
+        };
+        bool ok = true;
+        for (int k = 0; k < n_my; ++k) {
+            const TileInfo inf = inf_next;
+            const int rr = rr_next;
+            if (k + 1 < n_my)
+                describe(p, ppt, (int)blockIdx.x + (k + 1) * (int)gridDim.x, cur, inf_next, rr_next,
+                         lane == 0);
+            const int s = k & 1;
+            uint64_t *bar = &sh.full_qk[s];
+            int ok_w = 1;
+            if (lane == 0) {
+                ok_w = mbar_wait_sleep(&sh.empty_qk[s], ((k >> 1) & 1) ^ 1);
+                if (ok_w) {
+                    sh.info[k & 3] = inf;
+                    mbar_arrive(&sh.info_full[k & 3]);  // publishes it to the softmax warps
+                    if (inf.valid)
+                        mbar_arrive_expect_tx(bar, 2 * kQHalf + (inf.nr + inf.nc) * 256);
+                    else
+                        mbar_arrive(bar);
                 }
-                for (int b = 0; b < inf.nc; b += kBox) {
-                    const int z = inf.row_base + inf.z0 + b;
-                    const int off = (inf.nr + b) * 128;
-                    tma_load_3d(sh.v[s] + off, &tmNV, bar, 0, inf.h, z, pol_kv);
-                    tma_load_3d(sh.v[s] + kKvHalf + off, &tmNV, bar, 64, inf.h, z, pol_kv);
-                }
-                return true;
-            };
-            for (; k < n_my; ++k) {
-                const TileInfo inf = inf_next;
-                const int rr = rr_next;
-                if (k + 1 < n_my)
-                    describe(p, ppt, (int)blockIdx.x + (k + 1) * (int)gridDim.x, cur, inf_next,
-                             rr_next);
-                const int s = k & 1;
-                if (!mbar_wait_sleep(&sh.empty_qk[s], ((k >> 1) & 1) ^ 1)) {
-                    ok = false;
-                    break;
-                }
-                sh.info[k & 3] = inf;
-                mbar_arrive(&sh.info_full[k & 3]);  // publishes it to the softmax warps
-                uint64_t *bar = &sh.full_qk[s];
-                if (!inf.valid) {
-                    mbar_arrive(bar);
-                } else {
-                    mbar_arrive_expect_tx(bar, 2 * kQHalf + (inf.nr + inf.nc) * 256);
+            }
+            if (!__shfl_sync(0xffffffffu, ok_w, 0)) {
+                ok = false;
+                break;
+            }
+            if (inf.valid) {
+                const int nk = 2 * (inf.nr + inf.nc) / kBox;  // K boxes, <= 20
+                if (lane < nk) {
+                    issue_kv(sh.k[s], inf, rr, &tmRK, &tmNK, bar, lane);
+                } else if (lane < nk + 2) {
                     // q: ppt positions x the G query heads of KV head h (rows past the
                     // request are masked; rows past the tensor are zero-filled)
-                    const int qz = inf.row_base + inf.i0;
-                    tma_load_3d(sh.q[s], &tmQ, bar, 0, inf.h * p.G, qz, pol_q);
-                    tma_load_3d(sh.q[s] + kQHalf, &tmQ, bar, 64, inf.h * p.G, qz, pol_q);
-                    // ring region: 16-aligned position blocks -> 16-slot blocks of the ring
-                    for (int b = 0; b < inf.nr; b += kBox) {
-                        const int y = (rr * p.Hkv + inf.h) * p.W + (inf.a0 + b) % p.W;
-                        tma_load_2d(sh.k[s] + b * 128, &tmRK, bar, 0, y, pol_kv);
-                        tma_load_2d(sh.k[s] + kKvHalf + b * 128, &tmRK, bar, 64, y, pol_kv);
-                    }
-                    // chunk region
-                    for (int b = 0; b < inf.nc; b += kBox) {
-                        const int z = inf.row_base + inf.z0 + b;
-                        const int off = (inf.nr + b) * 128;
-                        tma_load_3d(sh.k[s] + off, &tmNK, bar, 0, inf.h, z, pol_kv);
-                        tma_load_3d(sh.k[s] + kKvHalf + off, &tmNK, bar, 64, inf.h, z, pol_kv);
-                    }
+                    const int half = lane - nk;
+                    tma_load_3d(sh.q[s] + half * kQHalf, &tmQ, bar, half * 64, inf.h * p.G,
+                                inf.row_base + inf.i0, pol_q);
                 }
-                if (k > 0 && !load_v(k - 1, inf_prev, rr_prev)) {
-                    ok = false;
-                    break;
-                }
-                inf_prev = inf;
-                rr_prev = rr;
             }
-            if (ok && n_my > 0 && !load_v(n_my - 1, inf_prev, rr_prev))
+            if (k > 0 && !load_v(k - 1, inf_prev, rr_prev)) {
                 ok = false;
+                break;
+            }
+            inf_prev = inf;
+            rr_prev = rr;
+        }
+        if (ok && !load_v(n_my - 1, inf_prev, rr_prev))
+            ok = false;
+        if (lane == 0) {
             if (!ok)
                 set_err(p.dev_err, HSA_DEVERR_TIMEOUT);
             // drain: no TMA write may still be in flight when the CTA exits
@@ -353,6 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_wait_sleep(&sh.full_v[j & 1], (j >> 1) & 1);
             }
         }
+        __syncwarp();
     } else if (warp == 1) {
         // ================================================================ MMA issuer
         if (lane == 0) {
