@@ -12,7 +12,7 @@
 // pinned host row directly over NVLink-C2C (no staging copy) and writing the
 // device ring row of the destination sequence, with four loads in flight per
 // thread.  The caller launches it on a side stream one or more layers ahead of the
-// attention that needs it; it keeps to two CTAs per SM and no shared memory, so it
+// attention that needs it; it keeps to a small grid and no shared memory, so it
 // runs beside the attention kernels.
 #include "hsa_device.cuh"
 #include "hsa_internal.h"
@@ -77,10 +77,12 @@ cudaError_t launch_swa_prefetch(const SwaPrefetchParams &p, cudaStream_t stream)
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    // a small footprint (two CTAs of 8 warps per SM) so that attention CTAs launched
-    // beside it always find room on every SM
+    // about 0.4 CTAs of 8 warps an SM: enough 16-byte loads in flight to fill the host
+    // link (~190 GB/s, reached from 64 CTAs up), few enough to leave the attention
+    // kernels running beside it their SMs (an all-rings decode step took 6.60 ms with
+    // 64 CTAs, 6.84 ms with two an SM; more loads a thread did not help)
     int64_t blocks = (total + 255) / 256;
-    const int64_t cap = (int64_t)(sms > 0 ? sms : 148) * 2;
+    const int64_t cap = (int64_t)(sms > 0 ? sms : 148) * 2 / 5;
     if (blocks > cap)
         blocks = cap;
     swa_prefetch_kernel<<<(unsigned)blocks, 256, 0, stream>>>(p);
