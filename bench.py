@@ -830,7 +830,7 @@ TRAFFIC = {
     # prefill_kernel, full layer: 4.720 GB on 2 requests, scaled by flops
     ("prefill", "full"): ("prefill.cu", "5df8d9b43c75a2fc", 14869832402),
     # prefill_swa_kernel, sliding layer: full-size launch
-    ("prefill", "sliding"): ("prefill_swa.cu", "487bd58bef03179b", 809082368),
+    ("prefill", "sliding"): ("prefill_swa.cu", "9c087b05ca36f8c6", 809227776),
     # append_kernel, full-size launches (writes still held in L2 at the kernel's end
     # reach DRAM after it)
     ("prefill", "append_full"): ("append.cu", "436d89e400666e68", 143246080),
