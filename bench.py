@@ -464,10 +464,13 @@ class PrefillStep:
         self.hsa.hsa_kv_append(self.pool, l, self.k[l], self.v[l], self.cu, self.seq,
                                self.pl, dev_err=self.err, stream=stream)
 
+    def layer(self, l):
+        self.attn(l)
+        self.append(l)
+
     def __call__(self):
         for l in self.layers:
-            self.attn(l)
-            self.append(l)
+            self.layer(l)
 
     def inputs(self):
         return self.q + self.k + self.v
@@ -580,6 +583,66 @@ def _graph_step(step, stream, warmup):
     if int(step.err.item()) != 0:
         raise SystemExit("device error flag set: %d" % int(step.err.item()))
     return graph
+
+
+def _e2e_layered(step, steps, ws):
+    """End to end through the C ABI with host buffers, the copies pipelined by layer:
+    seconds per step, H2D and D2H bytes per step.
+
+    Each step is one captured graph: every layer's q, k_new and v_new go from pinned
+    host memory to the device on one stream, layer l's kernels start once its own
+    inputs are in, and layer l's output goes back to pinned host memory on a third
+    stream as soon as layer l is done.  The copies of a step overlap that step's
+    kernels, so what is left exposed is the first layer's inputs and the last
+    layer's output; everything is inside the timed region."""
+    n = len(step.layers)
+    h_in = [t.cpu().pin_memory() for t in step.inputs()]
+    h_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in step.outputs()]
+    h2d = sum(t.numel() * t.element_size() for t in h_in)
+    d2h = sum(t.numel() * t.element_size() for t in h_out)
+    main, s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(n)]
+    ev_done = [torch.cuda.Event() for _ in range(n)]
+
+    def body():
+        s_in.wait_stream(main)
+        s_out.wait_stream(main)
+        with torch.cuda.stream(s_in):
+            for l in range(n):
+                for h, d in ((h_in[l], step.q[l]), (h_in[n + l], step.k[l]),
+                             (h_in[2 * n + l], step.v[l])):
+                    d.copy_(h, non_blocking=True)
+                ev_in[l].record(s_in)
+        for l in range(n):
+            main.wait_event(ev_in[l])
+            step.layer(l)
+            ev_done[l].record(main)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_done[l])
+                h_out[l].copy_(step.out[l], non_blocking=True)
+        main.wait_stream(s_in)
+        main.wait_stream(s_out)
+
+    with torch.cuda.stream(main):
+        body()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=main):
+        body()
+    torch.cuda.synchronize()
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+    barrier(ws)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        graph.replay()
+    torch.cuda.synchronize()
+    e2e_s = (time.perf_counter() - t0) / steps
+    if int(step.err.item()) != 0:
+        raise SystemExit("device error flag set: %d" % int(step.err.item()))
+    del graph, h_in, h_out
+    return max_over_ranks(e2e_s, ws), h2d, d2h
 
 
 def _e2e(step, graph, stream, steps, ws):
@@ -719,7 +782,10 @@ def measure(args, inst, ws, rank, local, cpu_repeats=None):
             prefetch_info = _prefetch_report(step, args, stream)
     clocks = clk.summary()
     step_ms = max_over_ranks(step_ms, ws)
-    e2e_s, h2d, d2h = _e2e(step, graph, stream, args.steps, ws)
+    if hasattr(step, "layer"):
+        e2e_s, h2d, d2h = _e2e_layered(step, args.steps, ws)
+    else:
+        e2e_s, h2d, d2h = _e2e(step, graph, stream, args.steps, ws)
 
     units = step.units_per_step()
     pk = peaks()

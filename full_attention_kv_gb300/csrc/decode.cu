@@ -775,7 +775,207 @@ __global__ void __launch_bounds__(kThreads, (RING && MT == 1) ? 2 : 1)
                                 p.scale_log2, false, t0 < T, t1 < T, vis_new);
     };
 
-    for (int64_t i = i0, k = 0; i < i1; ++i, ++k) {
+    // Sliding layers at T = 1 with a full ring (c >= W = 128): the new token replaces
+    // the one slot its query no longer sees (position c - W, slot c mod W), so once
+    // that row of the staged tile is overwritten with the new K / V, every one of the
+    // tile pair's 128 keys is visible and no mask or separate new-token tile remains.
+    // Each warp takes 32 keys with the operands swapped -- keys on the MMA's M side,
+    // the unit's (at most 8) query heads on its N side -- which halves the MMAs and
+    // the accumulator registers of the 16-row form; P goes from the S accumulators to
+    // the B operand of P V through an 8x8 transpose.  The warp holding the new slot
+    // also appends the new row, and one shared-memory pass merges the four warps.
+    const bool fold_ok = RING && MT == 1 && p.T == 1 && p.G <= 8 && p.W == 2 * kTileKeys;
+    auto ring_unit_t1 = [&](int64_t k_first, bool last_unit) {
+        const int grp = slice / wt;                    // tile-pair half this warp reads
+        const int my_j = grp ^ (int)(k_first & 1);     // the unit's tile in stage grp
+        const int64_t kk = k_first + my_j;
+        const int c = w.c;
+        const int slot_new = c % p.W;
+        const bool patcher = slot_new / kTileKeys == my_j && (slot_new % kTileKeys) / 32 == slice % wt;
+        // B operand of S^T = K Q^T: column n = query head g of the unit (zero past G)
+        uint32_t qb[kD / 16][2];
+        {
+            const bool ok = g < p.G;
+            const __nv_bfloat16 *qg = p.q + ((int64_t)w.b * Hq + w.h * p.G + (ok ? g : 0)) * kD;
+#pragma unroll
+            for (int ks = 0; ks < kD / 16; ++ks) {
+                qb[ks][0] = ok ? __ldg(reinterpret_cast<const uint32_t *>(qg + ks * 16 + 2 * tq)) : 0u;
+                qb[ks][1] = ok ? __ldg(reinterpret_cast<const uint32_t *>(qg + ks * 16 + 8 + 2 * tq)) : 0u;
+            }
+        }
+        // the new row: lanes 0-15 hold K's sixteen 16-byte chunks, lanes 16-31 V's
+        const int ch = lane & 15;
+        uint4 nrow = make_uint4(0, 0, 0, 0);
+        int rr = -1;
+        if (patcher) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(lane < 16 ? p.k_new : p.v_new);
+            nrow = __ldg(src + ((int64_t)w.b * p.Hkv + w.h) * (kD / 8) + ch);
+            if (p.flags & kDecodeAppend)
+                rr = __ldg(p.ring_row + w.b);
+        }
+        const uint32_t ph = (uint32_t)((kk / NS) & 1);
+        if (!timed_out && !mbar_wait(&sh.full[grp], ph)) {
+            set_err(p.dev_err, HSA_DEVERR_TIMEOUT);
+            timed_out = true;
+        }
+        const bool loaded = !timed_out && sh.tile_ok[grp] != 0;
+        const uint32_t sK = smem_u32(sh.stage + grp * kStageBytes);
+        const uint32_t sV = sK + kTileBytes;
+        if (patcher && loaded) {
+            const int row = slot_new % kTileKeys;
+            *reinterpret_cast<uint4 *>(sh.stage + grp * kStageBytes + (lane < 16 ? 0 : kTileBytes) +
+                                       swz128_offset(row, ch * 8, kTileKeys)) = nrow;
+            if (p.flags & kDecodeAppend) {
+                if (rr >= 0 && rr < p.n_ring_rows) {
+                    const int64_t dst_row = ((int64_t)rr * p.Hkv + w.h) * p.W + slot_new;
+                    (lane < 16 ? p.k_dst : p.v_dst)[dst_row * (kD / 8) + ch] = nrow;
+                } else if (lane == 0) {
+                    set_err(p.dev_err, HSA_DEVERR_BAD_RING);
+                }
+            }
+        }
+        __syncwarp();
+        // this warp's 32 keys: S^T (keys x heads), softmax per head column, O^T += V^T P^T
+        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // heads 2 tq, 2 tq + 1
+        float oT[kD / 16][4];
+#pragma unroll
+        for (int dt = 0; dt < kD / 16; ++dt)
+            oT[dt][0] = oT[dt][1] = oT[dt][2] = oT[dt][3] = 0.f;
+        if (loaded) {
+            const int kb = (slice % wt) * 32;
+            const int mi = lane >> 3, r8 = lane & 7;
+            float sc[2][4];
+#pragma unroll
+            for (int mt2 = 0; mt2 < 2; ++mt2) {
+                sc[mt2][0] = sc[mt2][1] = sc[mt2][2] = sc[mt2][3] = 0.f;
+#pragma unroll
+                for (int ks = 0; ks < kD / 16; ++ks) {
+                    uint32_t a[4];
+                    ldmatrix_x4(sK + swz128_offset(kb + mt2 * 16 + (mi & 1) * 8 + r8,
+                                                   ks * 16 + (mi >> 1) * 8, kTileKeys),
+                                a[0], a[1], a[2], a[3]);
+                    mma_bf16_16816(sc[mt2], a, qb[ks][0], qb[ks][1]);
+                }
+            }
+            float x0 = fmaxf(fmaxf(sc[0][0], sc[0][2]), fmaxf(sc[1][0], sc[1][2]));
+            float x1 = fmaxf(fmaxf(sc[0][1], sc[0][3]), fmaxf(sc[1][1], sc[1][3]));
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {
+                x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, o));
+                x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, o));
+            }
+            m0 = x0 * p.scale_log2;
+            m1 = x1 * p.scale_log2;
+            uint32_t pb[2][2];
+#pragma unroll
+            for (int mt2 = 0; mt2 < 2; ++mt2) {
+                const uint32_t lo = pack_bf16(fast_exp2(fmaf(sc[mt2][0], p.scale_log2, -m0)),
+                                              fast_exp2(fmaf(sc[mt2][1], p.scale_log2, -m1)));
+                const uint32_t hi = pack_bf16(fast_exp2(fmaf(sc[mt2][2], p.scale_log2, -m0)),
+                                              fast_exp2(fmaf(sc[mt2][3], p.scale_log2, -m1)));
+                // the sums take the bf16-rounded P the MMA uses
+                l0 += bf16_lo(lo) + bf16_lo(hi);
+                l1 += bf16_hi(lo) + bf16_hi(hi);
+                pb[mt2][0] = movmatrix_trans(lo);  // keys 0-7 of the 16: B rows 2 tq, +1
+                pb[mt2][1] = movmatrix_trans(hi);  // keys 8-15
+            }
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {
+                l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+                l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+            }
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks) {
+#pragma unroll
+                for (int dt = 0; dt < kD / 16; ++dt) {
+                    uint32_t a[4];
+                    ldmatrix_x4_trans(sV + swz128_offset(kb + ks * 16 + (mi >> 1) * 8 + r8,
+                                                         dt * 16 + (mi & 1) * 8, kTileKeys),
+                                      a[0], a[1], a[2], a[3]);
+                    mma_bf16_16816(oT[dt], a, pb[ks][0], pb[ks][1]);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(&sh.empty[grp]);
+        // merge: per warp m[8], l[8], then O as [head][dim] with a 132-float head stride
+        constexpr int kHs = kD + 4;
+        float *cb = sh.comb[warp];
+        if (g == 0) {
+            cb[2 * tq] = m0;
+            cb[2 * tq + 1] = m1;
+            cb[8 + 2 * tq] = l0;
+            cb[8 + 2 * tq + 1] = l1;
+        }
+        float *co = cb + 16;
+#pragma unroll
+        for (int dt = 0; dt < kD / 16; ++dt) {
+            co[(2 * tq) * kHs + dt * 16 + g] = oT[dt][0];
+            co[(2 * tq + 1) * kHs + dt * 16 + g] = oT[dt][1];
+            co[(2 * tq) * kHs + dt * 16 + g + 8] = oT[dt][2];
+            co[(2 * tq + 1) * kHs + dt * 16 + g + 8] = oT[dt][3];
+        }
+        named_bar_sync(1, kConsumerWarps * 32);
+        {
+            const int head = tid >> 4, d0 = (tid & 15) * 8;
+            if (head < p.G) {
+                float M = -INFINITY;
+#pragma unroll
+                for (int s = 0; s < kConsumerWarps; ++s)
+                    M = fmaxf(M, sh.comb[s][head]);
+                const float base = M == -INFINITY ? 0.f : M;
+                float a[kConsumerWarps], L = 0.f;
+#pragma unroll
+                for (int s = 0; s < kConsumerWarps; ++s) {
+                    a[s] = fast_exp2(sh.comb[s][head] - base);
+                    L += sh.comb[s][8 + head] * a[s];
+                }
+                const float norm = L > 0.f ? 1.f / L : 0.f;
+                float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int s = 0; s < kConsumerWarps; ++s) {
+                    const float4 *src =
+                        reinterpret_cast<const float4 *>(&sh.comb[s][16 + head * kHs + d0]);
+                    const float4 x = src[0], y = src[1];
+                    const float wgt = a[s] * norm;
+                    o[0] += x.x * wgt;
+                    o[1] += x.y * wgt;
+                    o[2] += x.z * wgt;
+                    o[3] += x.w * wgt;
+                    o[4] += y.x * wgt;
+                    o[5] += y.y * wgt;
+                    o[6] += y.z * wgt;
+                    o[7] += y.w * wgt;
+                }
+                uint4 v;
+                v.x = pack_bf16(o[0], o[1]);
+                v.y = pack_bf16(o[2], o[3]);
+                v.z = pack_bf16(o[4], o[5]);
+                v.w = pack_bf16(o[6], o[7]);
+                *reinterpret_cast<uint4 *>(p.out + ((int64_t)w.b * Hq + w.h * p.G + head) * kD + d0) = v;
+            }
+        }
+        if (!last_unit)
+            named_bar_sync(1, kConsumerWarps * 32);  // comb free again
+    };
+
+    int64_t i = i0, k = 0;
+    if constexpr (RING && MT == 1) {
+        // the CTA's leading whole units with a full ring take the path above; from the
+        // first unit that does not (a partial unit, a ring not yet full) the general
+        // loop below takes the rest
+        while (fold_ok && i < i1 && w.j == 0 && w.c >= p.W && unit_start + w.n <= i1) {
+            const int n = w.n;
+            ring_unit_t1(k, unit_start + n == i1);
+            i += n;
+            k += n;
+            unit_start += n;
+            for (int e = 0; e < n; ++e)
+                walk_next(p, w);
+        }
+    }
+    for (; i < i1; ++i, ++k) {
         if (fresh) {
             fresh = false;
             st.m[0] = st.m[1] = -INFINITY;

@@ -234,6 +234,15 @@ __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t &r0, u
                  : "r"(addr));
 }
 
+// Transpose of an 8x8 b16 matrix held in the fragment layout (lane l: row l / 4,
+// elements 2 (l % 4), +1) into the same layout.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x)
+{
+    uint32_t r;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
+    return r;
+}
+
 // D = A(16x16, row) * B(16x8, col) + D, bf16 inputs, fp32 accumulate.
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                                uint32_t b1)

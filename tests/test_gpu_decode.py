@@ -130,6 +130,46 @@ def test_decode_ragged_contexts_and_mtp(T, heads):
         assert err <= TOL, "T=%d heads=%s layer %d: err %g" % (T, heads, l, err)
 
 
+RING_T1_CONTEXTS = (0, 1, 63, 64, 100, 127, 128, 129, 191, 192, 193, 255, 256, 257, 1000, 4097)
+
+
+@pytest.mark.parametrize("heads", [(16, 2), (8, 2)])
+@pytest.mark.parametrize("max_ctas", [0, 40])
+def test_ring_t1_whole_units(heads, max_ctas):
+    """Sliding layer at T = 1 with whole (sequence, KV head) units per CTA: 96
+    sequences x 2 KV heads is enough units for one CTA each (max_ctas=0), or several
+    whole units and a split one per CTA (max_ctas=40).  Full rings (c >= W) take the
+    path with the new token written over the slot its query no longer sees; the
+    contexts put that slot at the start, middle and end of both 64-key tiles, and
+    mix in rings not yet full.  8 query heads per KV head, and 4 (padding columns).
+    Attention against the oracle; the fused append's rings bit-exact."""
+    hsa = _cuda()
+    Hq, Hkv = heads
+    ctx = tuple(RING_T1_CONTEXTS[i % len(RING_T1_CONTEXTS)] + 128 * (i // len(RING_T1_CONTEXTS))
+                for i in range(96))
+    cfg = dataclasses.replace(workload.CONFIGS["tiny"], Hq=Hq, Hkv=Hkv, T=1, contexts=ctx,
+                              B=len(ctx), index=90 + Hq)
+    inst = workload.draw(cfg)
+    pool = harness.make_pool(inst, [0])
+    q, k, v, cl = harness.decode_inputs(inst, 0)
+    ref = _oracle_layer(inst, 0)
+    out = hsa.hsa_decode_attn(pool, 0, q, k, v, cl, cfg.scale, max_ctas=max_ctas)
+    torch.cuda.synchronize()
+    err = np.max(np.abs(out.float().cpu().numpy().reshape(ref.shape) - ref))
+    assert err <= TOL, "heads=%s max_ctas=%d: err %g" % (heads, max_ctas, err)
+    ek, ev = _bits(pool.k[0]).copy(), _bits(pool.v[0]).copy()
+    dev_err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out2 = hsa.hsa_decode_attn_append(pool, 0, q, k, v, cl, cfg.scale, max_ctas=max_ctas,
+                                      dev_err=dev_err)
+    torch.cuda.synchronize()
+    assert int(dev_err.item()) == 0
+    assert torch.equal(out2, out)
+    B = inst.R
+    oracle.append(ek, ev, np.arange(B + 1), np.arange(B), inst.prefix,
+                  k.view(B, Hkv, cfg.d), v.view(B, Hkv, cfg.d), ring_row=inst.ring_row)
+    assert np.array_equal(_bits(pool.k[0]), ek) and np.array_equal(_bits(pool.v[0]), ev)
+
+
 def test_split_count_and_page_permutation_invariance():
     hsa = _cuda()
     cfg = dataclasses.replace(workload.CONFIGS["tiny"], Hq=32, Hkv=4, T=4,
