@@ -589,12 +589,12 @@ def _e2e_layered(step, steps, ws):
     """End to end through the C ABI with host buffers, the copies pipelined by layer:
     seconds per step, H2D and D2H bytes per step.
 
-    Each step is one captured graph: every layer's q, k_new and v_new go from pinned
-    host memory to the device on one stream, layer l's kernels start once its own
-    inputs are in, and layer l's output goes back to pinned host memory on a third
-    stream as soon as layer l is done.  The copies of a step overlap that step's
-    kernels, so what is left exposed is the first layer's inputs and the last
-    layer's output; everything is inside the timed region."""
+    A serving loop issued eagerly on three streams: every layer's q, k_new and v_new
+    go from pinned host memory to the device on one stream, layer l's kernels start
+    once its own inputs are in (and the previous step's read-back of its output is
+    done), and layer l's output goes back to pinned host memory on a third stream as
+    soon as layer l ends.  A step's copies overlap its own kernels and the
+    neighbouring steps'; everything is inside the timed region."""
     n = len(step.layers)
     h_in = [t.cpu().pin_memory() for t in step.inputs()]
     h_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in step.outputs()]
@@ -603,45 +603,39 @@ def _e2e_layered(step, steps, ws):
     main, s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     ev_in = [torch.cuda.Event() for _ in range(n)]
     ev_done = [torch.cuda.Event() for _ in range(n)]
+    ev_out = [torch.cuda.Event() for _ in range(n)]
 
-    def body():
-        s_in.wait_stream(main)
-        s_out.wait_stream(main)
-        with torch.cuda.stream(s_in):
-            for l in range(n):
-                for h, d in ((h_in[l], step.q[l]), (h_in[n + l], step.k[l]),
-                             (h_in[2 * n + l], step.v[l])):
-                    d.copy_(h, non_blocking=True)
-                ev_in[l].record(s_in)
-        for l in range(n):
-            main.wait_event(ev_in[l])
-            step.layer(l)
-            ev_done[l].record(main)
+    def serve(k):
+        for _ in range(k):
+            with torch.cuda.stream(s_in):
+                for l in range(n):
+                    s_in.wait_event(ev_done[l])  # the previous step's layer l has read them
+                    for h, d in ((h_in[l], step.q[l]), (h_in[n + l], step.k[l]),
+                                 (h_in[2 * n + l], step.v[l])):
+                        d.copy_(h, non_blocking=True)
+                    ev_in[l].record(s_in)
+            with torch.cuda.stream(main):
+                for l in range(n):
+                    main.wait_event(ev_in[l])
+                    main.wait_event(ev_out[l])  # the previous step's output l is read back
+                    step.layer(l)
+                    ev_done[l].record(main)
             with torch.cuda.stream(s_out):
-                s_out.wait_event(ev_done[l])
-                h_out[l].copy_(step.out[l], non_blocking=True)
-        main.wait_stream(s_in)
-        main.wait_stream(s_out)
+                for l in range(n):
+                    s_out.wait_event(ev_done[l])
+                    h_out[l].copy_(step.out[l], non_blocking=True)
+                    ev_out[l].record(s_out)
 
-    with torch.cuda.stream(main):
-        body()
-    torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=main):
-        body()
-    torch.cuda.synchronize()
-    for _ in range(2):
-        graph.replay()
+    serve(2)
     torch.cuda.synchronize()
     barrier(ws)
     t0 = time.perf_counter()
-    for _ in range(steps):
-        graph.replay()
+    serve(steps)
     torch.cuda.synchronize()
     e2e_s = (time.perf_counter() - t0) / steps
     if int(step.err.item()) != 0:
         raise SystemExit("device error flag set: %d" % int(step.err.item()))
-    del graph, h_in, h_out
+    del h_in, h_out
     return max_over_ranks(e2e_s, ws), h2d, d2h
 
 

@@ -47,12 +47,19 @@ constexpr int kTileKeys = 64;
 constexpr int kD = 128;
 constexpr int kStages = 4;
 constexpr int kConsumerWarps = 4;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
+// FP8 full layers at T = 1 with at most 8 query heads a KV head run eight consumer
+// warps (operands swapped, fewer registers a thread: see the consumer loop)
+constexpr int kSwWarps = 8;
+constexpr int kMaxThreads = (kSwWarps + 1) * 32;
 constexpr int kTileBytes = kTileKeys * kD * 2;  // 16 KB: one K or V tile
 constexpr int kStageBytes = 2 * kTileBytes;
 constexpr int kMaxRows = 32;                    // G * T
 constexpr int kNewRows = 16;                    // new-token tile (T <= 4 used)
 constexpr int kCombFloats = 16 + 16 + 16 * kD;  // per warp: m, l, o[16][128]
+constexpr int kHs = kD + 4;                     // swapped layouts: o[head][dim] row stride
+constexpr int kSwFloats = 16 + 8 * kHs;         // swapped layouts, per warp: m[8], l[8], o[8][132]
+constexpr int kCombStride = (kSwWarps * kSwFloats + kConsumerWarps - 1) / kConsumerWarps;
+static_assert(kCombStride >= kCombFloats && kCombStride % 4 == 0, "merge buffer layout");
 constexpr int kPartFloats = kMaxRows * (kD + 2);
 // FP8 full layers (fp8_kv.cuh): a stage holds the tile's E4M3 K (64 x 128 B,
 // 128-byte swizzle), transposed V (128 x 64 B, 64-byte swizzle) and the two rows
@@ -82,13 +89,13 @@ struct SharedStorageT {
     alignas(1024) uint8_t stage[kRegion];  // bf16: [K lo|K hi|V lo|V hi] per stage
     alignas(16) uint8_t new_k[kNewRows * kD * 2];
     alignas(16) uint8_t new_v[kNewRows * kD * 2];
-    alignas(16) float comb[kConsumerWarps][kCombFloats];
+    alignas(16) float comb[kConsumerWarps][kCombStride];  // also kSwWarps x kSwFloats
     float mscale[kMaxRows][kConsumerWarps];  // merge: each slice's weight per row
     float mrow[kMaxRows][2];                 // merge: each row's combined max and sum
     alignas(8) uint64_t full[kMaxStages];
     alignas(8) uint64_t empty[kMaxStages];
     int32_t tile_ok[kMaxStages];  // the producer loaded the stage's tile (else: masked)
-    int32_t scan[kThreads];
+    int32_t scan[kMaxThreads];
     int32_t first_b;
     int32_t first_items_before;  // items of all units of sequences < first_b (per KV head)
     int32_t total_items;         // per KV head sum
@@ -460,6 +467,120 @@ __device__ __forceinline__ void run_tile_fp8(RowState &st, const uint32_t (&qa)[
     st.l[1] += sum1;
 }
 
+// One 64-key page of an FP8 full layer at T = 1 with the operands swapped: S^T =
+// K Q^T with the page's keys on the MMA's M side (four 16-key m-tiles) and the
+// unit's query heads on its N side (column n = head g, heads past G are zero), then
+// O^T += V^T P^T with the output dimensions on M (eight m-tiles).  The shared-memory
+// words are the ones run_tile_fp8 reads (K: four codes of one key, V transposed:
+// four codes of one dimension), now taken for two keys / two dimensions an MMA.  P
+// reaches the B operand of the second product through an 8x8 transpose.  State per
+// thread: heads 2 tq and 2 tq + 1 (m, l in log2 units) and oT[dt] = O^T rows
+// dt * 16 + g, + 8.  Keys >= `valid` are masked (a partly filled last page).
+template <bool E5M2>
+__device__ __forceinline__ void tile_fp8_sw(float (&m)[2], float (&l)[2], float (&oT)[kD / 16][4],
+                                            const uint32_t (&qb)[kD / 16][2], const uint8_t *sK,
+                                            const uint8_t *sV, const float *k_scale,
+                                            const float *v_scale, int valid, float scale_log2)
+{
+    const int lane = threadIdx.x & 31;
+    const int g = lane >> 2, tq = lane & 3;
+    float s[4][4], s2[4][4];
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt)
+        s[mt][0] = s[mt][1] = s[mt][2] = s[mt][3] = s2[mt][0] = s2[mt][1] = s2[mt][2] = s2[mt][3] = 0.f;
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt) {
+        // keys mt * 16 + g and + 8 share (key & 7) = g, so one swizzle serves both rows
+        const uint8_t *ra = sK + (mt * 16 + g) * 128 + 4 * tq;
+        const uint8_t *rb = ra + 8 * 128;
+#pragma unroll
+        for (int ks = 0; ks < kD / 16; ++ks) {
+            const int off = (ks ^ g) << 4;
+            const uint32_t wa = *reinterpret_cast<const uint32_t *>(ra + off);
+            const uint32_t wb = *reinterpret_cast<const uint32_t *>(rb + off);
+            const uint32_t a[4] = {fp8x2_lo<E5M2>(wa), fp8x2_lo<E5M2>(wb), fp8x2_hi<E5M2>(wa),
+                                   fp8x2_hi<E5M2>(wb)};
+            mma_f16_16816((ks & 1) ? s2[mt] : s[mt], a, qb[ks][0], qb[ks][1]);
+        }
+    }
+    float x0 = -INFINITY, x1 = -INFINITY;
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt) {
+        const int ka = mt * 16 + g, kb = ka + 8;
+        const float sa = ka < valid ? k_scale[ka] : 0.f, sb = kb < valid ? k_scale[kb] : 0.f;
+        s[mt][0] = ka < valid ? (s[mt][0] + s2[mt][0]) * sa : -INFINITY;
+        s[mt][1] = ka < valid ? (s[mt][1] + s2[mt][1]) * sa : -INFINITY;
+        s[mt][2] = kb < valid ? (s[mt][2] + s2[mt][2]) * sb : -INFINITY;
+        s[mt][3] = kb < valid ? (s[mt][3] + s2[mt][3]) * sb : -INFINITY;
+        x0 = fmaxf(x0, fmaxf(s[mt][0], s[mt][2]));
+        x1 = fmaxf(x1, fmaxf(s[mt][1], s[mt][3]));
+    }
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+        x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, o));
+        x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, o));
+    }
+    x0 *= scale_log2;
+    x1 *= scale_log2;
+    // running max raised lazily, as in run_tile (the lanes of a column agree)
+    const bool up0 = x0 != -INFINITY && (m[0] == -INFINITY || x0 > m[0] + kRescaleSlack);
+    const bool up1 = x1 != -INFINITY && (m[1] == -INFINITY || x1 > m[1] + kRescaleSlack);
+    if (__any_sync(0xffffffffu, up0 || up1)) {
+        const float a0 = up0 ? fast_exp2(m[0] - x0) : 1.f;
+        const float a1 = up1 ? fast_exp2(m[1] - x1) : 1.f;
+        if (up0)
+            m[0] = x0;
+        if (up1)
+            m[1] = x1;
+        l[0] *= a0;
+        l[1] *= a1;
+#pragma unroll
+        for (int dt = 0; dt < kD / 16; ++dt) {
+            oT[dt][0] *= a0;
+            oT[dt][1] *= a1;
+            oT[dt][2] *= a0;
+            oT[dt][3] *= a1;
+        }
+    }
+    const float base0 = m[0] == -INFINITY ? 0.f : m[0];
+    const float base1 = m[1] == -INFINITY ? 0.f : m[1];
+    constexpr float f = E5M2 ? 256.f : 1.f;  // an E5M2 V scale is folded in times 256
+    float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+        const int ka = ks * 16 + g, kb = ka + 8;
+        const float p0 = fast_exp2(fmaf(s[ks][0], scale_log2, -base0));
+        const float p1 = fast_exp2(fmaf(s[ks][1], scale_log2, -base1));
+        const float p2 = fast_exp2(fmaf(s[ks][2], scale_log2, -base0));
+        const float p3 = fast_exp2(fmaf(s[ks][3], scale_log2, -base1));
+        sum0 += p0 + p2;
+        sum1 += p1 + p3;
+        const float va = (ka < valid ? v_scale[ka] : 0.f) * f;
+        const float vb = (kb < valid ? v_scale[kb] : 0.f) * f;
+        // P^T rows ka (keys 0-7 of the 16) and kb (8-15), columns heads 2 tq, +1
+        const uint32_t b0 = movmatrix_trans(pack_f16(p0 * va, p1 * va));
+        const uint32_t b1 = movmatrix_trans(pack_f16(p2 * vb, p3 * vb));
+#pragma unroll
+        for (int dt = 0; dt < kD / 16; ++dt) {
+            const int da = dt * 16 + g, db = da + 8;
+            const uint32_t wa = *reinterpret_cast<const uint32_t *>(
+                sV + da * 64 + ((ks ^ ((da >> 1) & 3)) << 4) + 4 * tq);
+            const uint32_t wb = *reinterpret_cast<const uint32_t *>(
+                sV + db * 64 + ((ks ^ ((db >> 1) & 3)) << 4) + 4 * tq);
+            const uint32_t a[4] = {fp8x2_lo<E5M2>(wa), fp8x2_lo<E5M2>(wb), fp8x2_hi<E5M2>(wa),
+                                   fp8x2_hi<E5M2>(wb)};
+            mma_f16_16816(oT[dt], a, b0, b1);
+        }
+    }
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+        sum0 += __shfl_xor_sync(0xffffffffu, sum0, o);
+        sum1 += __shfl_xor_sync(0xffffffffu, sum1, o);
+    }
+    l[0] += sum0;
+    l[1] += sum1;
+}
+
 // Append of unit (b, h) into an FP8 full layer: one warp per new K or V row.
 __device__ __forceinline__ void append_unit_fp8(const DecodeParams &p, int b, int h, int c, int warp,
                                                 int lane, int nwarps, bool e5m2)
@@ -542,6 +663,66 @@ __device__ __forceinline__ void append_unit(const DecodeParams &p, int b, int h,
     }
 }
 
+// A unit split across CTAs: count this CTA's part in (its (m, l, o) partial is in
+// the workspace already); the last CTA to arrive (atomic counter, no waiting)
+// merges every part into `out`, appends the unit's new rows and resets the counter.
+// Called by the nwarps consumer warps of the CTA, named barrier 1.
+template <int FP8>
+__device__ __forceinline__ void finish_split_unit(const DecodeParams &p, int32_t &is_last,
+                                                  const Walk &cur, int64_t unit_start,
+                                                  int64_t unit_end, int64_t N, int64_t C, int tid,
+                                                  int warp, int lane, int nwarps)
+{
+    int32_t *const ws_cnt = reinterpret_cast<int32_t *>(p.ws);
+    const float *const ws_part =
+        reinterpret_cast<const float *>(p.ws + decode_counter_bytes(p.B, p.Hkv));
+    const int nthreads = nwarps * 32;
+    const int Hq = p.G * p.Hkv;
+    const int unit = cur.b * p.Hkv + cur.h;
+    const int64_t c_lo = ((unit_start + 1) * C - 1) / N;
+    const int64_t c_hi = (unit_end * C - 1) / N;
+    named_bar_sync(1, nthreads);
+    if (tid == 0) {
+        __threadfence();
+        const int prev = atomicAdd(ws_cnt + unit, 1);
+        is_last = (prev == (int)(c_hi - c_lo));
+    }
+    named_bar_sync(1, nthreads);
+    if (!is_last)
+        return;
+    __threadfence();
+    for (int e = tid; e < p.G * p.T * kD; e += nthreads) {
+        const int rr = e / kD, dim = e % kD;
+        float M = -INFINITY;
+        for (int64_t cc = c_lo; cc <= c_hi; ++cc) {
+            const int64_t start_cc = cc * N / C;
+            const int sl = 2 * (int)cc + (start_cc < unit_start ? 1 : 0);
+            M = fmaxf(M, __ldcg(ws_part + (int64_t)sl * kPartFloats + rr));
+        }
+        const float base = M == -INFINITY ? 0.f : M;
+        float L = 0.f, O = 0.f;
+        for (int64_t cc = c_lo; cc <= c_hi; ++cc) {
+            const int64_t start_cc = cc * N / C;
+            const int sl = 2 * (int)cc + (start_cc < unit_start ? 1 : 0);
+            const float *pp = ws_part + (int64_t)sl * kPartFloats;
+            const float a = fast_exp2(__ldcg(pp + rr) - base);
+            L += __ldcg(pp + kMaxRows + rr) * a;
+            O += __ldcg(pp + 2 * kMaxRows + rr * kD + dim) * a;
+        }
+        const int t = rr / p.G, hh = rr % p.G;
+        p.out[((int64_t)(cur.b * p.T + t) * Hq + cur.h * p.G + hh) * kD + dim] =
+            __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
+    }
+    if (p.flags & kDecodeAppend) {
+        if constexpr (FP8)
+            append_unit_fp8(p, cur.b, cur.h, cur.c, warp, lane, nwarps, FP8 == 2);
+        else
+            append_unit(p, cur.b, cur.h, cur.c, tid, nthreads);
+    }
+    if (tid == 0)
+        ws_cnt[unit] = 0;
+}
+
 template <bool RING>
 using SharedStorage = SharedStorageT<RING ? kRingStageRegion : kStageRegion>;
 
@@ -549,12 +730,16 @@ using SharedStorage = SharedStorageT<RING ? kRingStageRegion : kStageRegion>;
 // layer; RING: a sliding layer (its own instantiation with two stages; at MT = 1 it
 // is held to 168 registers so that two CTAs fit on an SM -- at MT = 2 that limit
 // spilled ~170 bytes a thread, so MTP rings keep one CTA an SM).
-template <int MT, int FP8, bool RING>
-__global__ void __launch_bounds__(kThreads, (RING && MT == 1) ? 2 : 1)
+// CW: consumer warps (kConsumerWarps, or kSwWarps for the swapped FP8 loop).
+template <int MT, int FP8, bool RING, int CW>
+__global__ void __launch_bounds__((CW + 1) * 32, (RING && MT == 1) ? 2 : 1)
     decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const DecodeParams p)
 {
     static_assert(!(FP8 && RING), "the rings stay bf16");
+    static_assert(CW == kConsumerWarps || (CW == kSwWarps && FP8 && MT == 1 && !RING),
+                  "eight consumer warps: FP8 full layers at T = 1 only");
+    constexpr int kThr = (CW + 1) * 32;
     constexpr int NS = RING ? kRingStages : (FP8 ? kFp8Stages : kStages);
     extern __shared__ uint8_t smem_raw[];
     SharedStorage<RING> &sh = *reinterpret_cast<SharedStorage<RING> *>(
@@ -570,7 +755,7 @@ __global__ void __launch_bounds__(kThreads, (RING && MT == 1) ? 2 : 1)
         }
         fence_barrier_init();
     }
-    if (warp == kConsumerWarps && lane == 0) {
+    if (warp == CW && lane == 0) {
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
     }
@@ -587,7 +772,7 @@ __global__ void __launch_bounds__(kThreads, (RING && MT == 1) ? 2 : 1)
 
     // ---- locate this CTA's contiguous range of items ------------------------
     {
-        const int per = (p.B + kThreads - 1) / kThreads;
+        const int per = (p.B + kThr - 1) / kThr;
         const int b_lo = min(p.B, tid * per), b_hi = min(p.B, b_lo + per);
         int local = 0;
         for (int b = b_lo; b < b_hi; ++b)
@@ -595,8 +780,8 @@ __global__ void __launch_bounds__(kThreads, (RING && MT == 1) ? 2 : 1)
         sh.scan[tid] = local;
         __syncthreads();
         if (warp == 0) {
-            // exclusive scan of kThreads entries: kThreads / 32 consecutive entries per lane
-            constexpr int kPer = kThreads / 32;
+            // exclusive scan of kThr entries: kThr / 32 consecutive entries per lane
+            constexpr int kPer = kThr / 32;
             int v[kPer];
             int sum = 0;
 #pragma unroll
@@ -633,7 +818,7 @@ __global__ void __launch_bounds__(kThreads, (RING && MT == 1) ? 2 : 1)
     const int64_t i1 = ((int64_t)blockIdx.x + 1) * N / C;
     {
         // the thread whose chunk of sequences holds item i0 records it
-        const int per = (p.B + kThreads - 1) / kThreads;
+        const int per = (p.B + kThr - 1) / kThr;
         const int b_lo = min(p.B, tid * per), b_hi = min(p.B, b_lo + per);
         int before = sh.scan[tid];
         for (int b = b_lo; b < b_hi; ++b) {
@@ -656,7 +841,7 @@ __global__ void __launch_bounds__(kThreads, (RING && MT == 1) ? 2 : 1)
     }
     const int64_t w0_unit_start = i0 - w0.j;  // item index of tile 0 of the first unit
 
-    if (warp == kConsumerWarps) {
+    if (warp == CW) {
         // ---------------------------------------------------------------- producer
 #ifdef HSA_TEST_WITHHOLD_LOADS
         // Test-only builds (never the product library): the producer issues no load
@@ -727,6 +912,163 @@ __global__ void __launch_bounds__(kThreads, (RING && MT == 1) ? 2 : 1)
         return;
     }
 
+    if constexpr (CW == kSwWarps) {
+        // ------------------------------------------ consumers: FP8 full layer, T = 1
+        // Eight warps; warp w runs the tiles k = w mod 8 of the CTA's range (stage k
+        // mod 8) with tile_fp8_sw.  At the end of a unit the warps' states merge
+        // through shared memory, warp h taking query head h and each lane four output
+        // dimensions; the CTA that owns the unit's last tile adds the new token there
+        // as one more key (its score q . k_new from the bf16 rows, weight and value
+        // exact).  Split units go through the workspace as in the general loop.
+        constexpr bool kE5 = FP8 == 2;
+        const int g = lane >> 2, tq = lane & 3;
+        const int Hq = p.G * p.Hkv;
+        float *const ws_part = reinterpret_cast<float *>(p.ws + decode_counter_bytes(p.B, p.Hkv));
+        float *const comb = &sh.comb[0][0];
+        uint32_t qb[kD / 16][2];
+        float m[2], l[2], oT[kD / 16][4];
+        Walk w = w0;
+        int64_t unit_start = w0_unit_start;
+        bool fresh = true, timed_out = false;
+        for (int64_t i = i0, k = 0; i < i1; ++i, ++k) {
+            if (fresh) {
+                fresh = false;
+                m[0] = m[1] = -INFINITY;
+                l[0] = l[1] = 0.f;
+#pragma unroll
+                for (int dt = 0; dt < kD / 16; ++dt)
+                    oT[dt][0] = oT[dt][1] = oT[dt][2] = oT[dt][3] = 0.f;
+                // B operand of S^T = K Q^T in fp16: column g = query head g of the unit
+                const bool ok = g < p.G;
+                const __nv_bfloat16 *qg = p.q + ((int64_t)w.b * Hq + w.h * p.G + (ok ? g : 0)) * kD;
+#pragma unroll
+                for (int ks = 0; ks < kD / 16; ++ks) {
+                    const uint32_t *q32 = reinterpret_cast<const uint32_t *>(qg + ks * 16 + 2 * tq);
+                    qb[ks][0] = ok ? bf16x2_to_f16x2(__ldg(q32)) : 0u;
+                    qb[ks][1] = ok ? bf16x2_to_f16x2(__ldg(q32 + 4)) : 0u;
+                }
+            }
+            if ((int)(k % kSwWarps) == warp) {
+                const int stg = (int)(k % NS);
+                if (!timed_out && !mbar_wait(&sh.full[stg], (uint32_t)((k / NS) & 1))) {
+                    set_err(p.dev_err, HSA_DEVERR_TIMEOUT);
+                    timed_out = true;
+                }
+                const int valid = w.c - w.j * kTileKeys;  // cached keys on this page
+                if (!timed_out && sh.tile_ok[stg] != 0 && valid > 0) {
+                    const uint8_t *base = sh.stage + stg * kFp8StageStride;
+                    const float *ksc = reinterpret_cast<const float *>(base + 2 * kFp8TileBytes);
+                    tile_fp8_sw<kE5>(m, l, oT, qb, base, base + kFp8TileBytes, ksc, ksc + 64,
+                                     valid < kTileKeys ? valid : kTileKeys, p.scale_log2);
+                }
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&sh.empty[stg]);
+            }
+            const bool unit_last_tile = (w.j == w.n - 1);
+            const Walk cur = w;
+            walk_next(p, w);
+            if (!(unit_last_tile || i == i1 - 1))
+                continue;
+
+            // ---- end of this CTA's share of unit (cur.b, cur.h) --------------
+            const int64_t unit_end = unit_start + cur.n;
+            if constexpr (kE5) {  // the E5M2 tiles accumulate 256 O
+#pragma unroll
+                for (int dt = 0; dt < kD / 16; ++dt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        oT[dt][e] *= 1.f / 256.f;
+            }
+            {
+                float *cb = comb + warp * kSwFloats;
+                if (g == 0) {
+                    cb[2 * tq] = m[0];
+                    cb[2 * tq + 1] = m[1];
+                    cb[8 + 2 * tq] = l[0];
+                    cb[8 + 2 * tq + 1] = l[1];
+                }
+                float *co = cb + 16;
+#pragma unroll
+                for (int dt = 0; dt < kD / 16; ++dt) {
+                    co[(2 * tq) * kHs + dt * 16 + g] = oT[dt][0];
+                    co[(2 * tq + 1) * kHs + dt * 16 + g] = oT[dt][1];
+                    co[(2 * tq) * kHs + dt * 16 + g + 8] = oT[dt][2];
+                    co[(2 * tq + 1) * kHs + dt * 16 + g + 8] = oT[dt][3];
+                }
+            }
+            named_bar_sync(1, kSwWarps * 32);
+            const bool whole = unit_start >= i0 && unit_end <= i1;
+            const bool has_new = unit_end <= i1;  // this CTA owns the unit's last tile
+            const int head = warp;
+            if (head < p.G) {
+                const int d0 = lane * 4;
+                float sn = -INFINITY, vn[4] = {0.f, 0.f, 0.f, 0.f};
+                if (has_new) {
+                    const uint2 qv = __ldg(reinterpret_cast<const uint2 *>(
+                        p.q + ((int64_t)cur.b * Hq + cur.h * p.G + head) * kD + d0));
+                    const int64_t rk = ((int64_t)cur.b * p.Hkv + cur.h) * kD + d0;
+                    const uint2 kv = __ldg(reinterpret_cast<const uint2 *>(p.k_new + rk));
+                    const uint2 vv = __ldg(reinterpret_cast<const uint2 *>(p.v_new + rk));
+                    float dot = bf16_lo(qv.x) * bf16_lo(kv.x) + bf16_hi(qv.x) * bf16_hi(kv.x) +
+                                bf16_lo(qv.y) * bf16_lo(kv.y) + bf16_hi(qv.y) * bf16_hi(kv.y);
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1)
+                        dot += __shfl_xor_sync(0xffffffffu, dot, o);
+                    sn = dot * p.scale_log2;
+                    vn[0] = bf16_lo(vv.x);
+                    vn[1] = bf16_hi(vv.x);
+                    vn[2] = bf16_lo(vv.y);
+                    vn[3] = bf16_hi(vv.y);
+                }
+                float M = sn;
+#pragma unroll
+                for (int s = 0; s < kSwWarps; ++s)
+                    M = fmaxf(M, comb[s * kSwFloats + head]);
+                const float base = M == -INFINITY ? 0.f : M;
+                const float an = has_new ? fast_exp2(sn - base) : 0.f;
+                float L = an;
+                float o[4] = {an * vn[0], an * vn[1], an * vn[2], an * vn[3]};
+#pragma unroll
+                for (int s = 0; s < kSwWarps; ++s) {
+                    const float *cs = comb + s * kSwFloats;
+                    const float a = fast_exp2(cs[head] - base);
+                    L += cs[8 + head] * a;
+                    const float4 x = *reinterpret_cast<const float4 *>(cs + 16 + head * kHs + d0);
+                    o[0] += x.x * a;
+                    o[1] += x.y * a;
+                    o[2] += x.z * a;
+                    o[3] += x.w * a;
+                }
+                if (whole) {
+                    const float norm = L > 0.f ? 1.f / L : 0.f;
+                    *reinterpret_cast<uint2 *>(
+                        p.out + ((int64_t)cur.b * Hq + cur.h * p.G + head) * kD + d0) =
+                        make_uint2(pack_bf16(o[0] * norm, o[1] * norm),
+                                   pack_bf16(o[2] * norm, o[3] * norm));
+                } else {
+                    const int slot = 2 * (int)blockIdx.x + (i0 < unit_start ? 1 : 0);
+                    float *part = ws_part + (int64_t)slot * kPartFloats;
+                    if (lane == 0) {
+                        __stcg(part + head, M);
+                        __stcg(part + kMaxRows + head, L);
+                    }
+                    __stcg(reinterpret_cast<float4 *>(part + 2 * kMaxRows + head * kD + d0),
+                           make_float4(o[0], o[1], o[2], o[3]));
+                }
+            }
+            if (whole && (p.flags & kDecodeAppend))
+                append_unit_fp8(p, cur.b, cur.h, cur.c, warp, lane, kSwWarps, kE5);
+            if (!whole)
+                finish_split_unit<FP8>(p, sh.is_last, cur, unit_start, unit_end, N, C, tid, warp,
+                                       lane, kSwWarps);
+            named_bar_sync(1, kSwWarps * 32);  // merge buffer free again
+            unit_start = unit_end;
+            fresh = true;
+        }
+        return;
+    }
+
     // -------------------------------------------------------------------- consumers
     const int mt = warp % MT;
     const int slice = warp / MT;
@@ -753,7 +1095,6 @@ __global__ void __launch_bounds__(kThreads, (RING && MT == 1) ? 2 : 1)
     const int t0 = r0 / p.G, t1 = r1 / p.G;
     const int rows_valid = p.G * p.T;
     const int Hq = p.G * p.Hkv;
-    int32_t *const ws_cnt = reinterpret_cast<int32_t *>(p.ws);
     float *const ws_part = reinterpret_cast<float *>(p.ws + decode_counter_bytes(p.B, p.Hkv));
 
     RowState st;
@@ -900,7 +1241,6 @@ __global__ void __launch_bounds__(kThreads, (RING && MT == 1) ? 2 : 1)
         if (lane == 0)
             mbar_arrive(&sh.empty[grp]);
         // merge: per warp m[8], l[8], then O as [head][dim] with a 132-float head stride
-        constexpr int kHs = kD + 4;
         float *cb = sh.comb[warp];
         if (g == 0) {
             cb[2 * tq] = m0;
@@ -1210,53 +1550,9 @@ __global__ void __launch_bounds__(kThreads, (RING && MT == 1) ? 2 : 1)
             else
                 append_unit(p, cur.b, cur.h, cur.c, tid, kConsumerWarps * 32, sh.new_k, sh.new_v);
         }
-        if (!whole) {
-            // count this part in; the last CTA of the unit merges every part
-            const int unit = cur.b * p.Hkv + cur.h;
-            const int64_t c_lo = ((unit_start + 1) * C - 1) / N;
-            const int64_t c_hi = (unit_end * C - 1) / N;
-            named_bar_sync(1, kConsumerWarps * 32);
-            if (tid == 0) {
-                __threadfence();
-                const int prev = atomicAdd(ws_cnt + unit, 1);
-                sh.is_last = (prev == (int)(c_hi - c_lo));
-            }
-            named_bar_sync(1, kConsumerWarps * 32);
-            if (sh.is_last) {
-                __threadfence();
-                for (int e = tid; e < rows_valid * kD; e += kConsumerWarps * 32) {
-                    const int rr = e / kD, dim = e % kD;
-                    float M = -INFINITY;
-                    for (int64_t cc = c_lo; cc <= c_hi; ++cc) {
-                        const int64_t start_cc = cc * N / C;
-                        const int sl = 2 * (int)cc + (start_cc < unit_start ? 1 : 0);
-                        M = fmaxf(M, __ldcg(ws_part + (int64_t)sl * kPartFloats + rr));
-                    }
-                    const float base = M == -INFINITY ? 0.f : M;
-                    float L = 0.f, O = 0.f;
-                    for (int64_t cc = c_lo; cc <= c_hi; ++cc) {
-                        const int64_t start_cc = cc * N / C;
-                        const int sl = 2 * (int)cc + (start_cc < unit_start ? 1 : 0);
-                        const float *pp = ws_part + (int64_t)sl * kPartFloats;
-                        const float a = fast_exp2(__ldcg(pp + rr) - base);
-                        L += __ldcg(pp + kMaxRows + rr) * a;
-                        O += __ldcg(pp + 2 * kMaxRows + rr * kD + dim) * a;
-                    }
-                    const int t = rr / p.G, hh = rr % p.G;
-                    p.out[((int64_t)(cur.b * p.T + t) * Hq + cur.h * p.G + hh) * kD + dim] =
-                        __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
-                }
-                if (p.flags & kDecodeAppend) {
-                    if constexpr (FP8)
-                        append_unit_fp8(p, cur.b, cur.h, cur.c, warp, lane, kConsumerWarps,
-                                        FP8 == 2);
-                    else
-                        append_unit(p, cur.b, cur.h, cur.c, tid, kConsumerWarps * 32);
-                }
-                if (tid == 0)
-                    ws_cnt[unit] = 0;
-            }
-        }
+        if (!whole)
+            finish_split_unit<FP8>(p, sh.is_last, cur, unit_start, unit_end, N, C, tid, warp, lane,
+                                   kConsumerWarps);
         named_bar_sync(1, kConsumerWarps * 32);  // comb / new-token buffers free again
         unit_start = unit_end;
         fresh = true;
@@ -1281,20 +1577,28 @@ cudaError_t launch_decode(const CUtensorMap &tmK, const CUtensorMap &tmV, const 
     const size_t smem = (ring ? sizeof(SharedStorage<true>) : sizeof(SharedStorage<false>)) + 1024;
     // the opt-in shared-memory size is set once per process (the API is not a stream
     // operation, but setting it once keeps graph capture free of extra calls)
-    static bool attr_set[8] = {false, false, false, false, false, false, false, false};
+    static bool attr_set[10] = {false, false, false, false, false,
+                                false, false, false, false, false};
     void (*kern)(CUtensorMap, CUtensorMap, DecodeParams);
     int which;
+    constexpr int C4 = kConsumerWarps;
+    // FP8 full layers at T = 1 with <= 8 query heads a KV head: the eight-warp loop
+    const bool sw = fp8 && !ring && p.T == 1 && p.G <= 8;
     if (ring) {
-        kern = MT == 1 ? decode_kernel<1, 0, true> : decode_kernel<2, 0, true>;
+        kern = MT == 1 ? decode_kernel<1, 0, true, C4> : decode_kernel<2, 0, true, C4>;
         which = 4 + MT - 1;
+    } else if (sw) {
+        kern = (p.flags & kDecodeE5M2) ? decode_kernel<1, 2, false, kSwWarps>
+                                       : decode_kernel<1, 1, false, kSwWarps>;
+        which = (p.flags & kDecodeE5M2) ? 9 : 8;
     } else if (fp8 && (p.flags & kDecodeE5M2)) {
-        kern = MT == 1 ? decode_kernel<1, 2, false> : decode_kernel<2, 2, false>;
+        kern = MT == 1 ? decode_kernel<1, 2, false, C4> : decode_kernel<2, 2, false, C4>;
         which = 6 + MT - 1;
     } else if (fp8) {
-        kern = MT == 1 ? decode_kernel<1, 1, false> : decode_kernel<2, 1, false>;
+        kern = MT == 1 ? decode_kernel<1, 1, false, C4> : decode_kernel<2, 1, false, C4>;
         which = 2 + MT - 1;
     } else {
-        kern = MT == 1 ? decode_kernel<1, 0, false> : decode_kernel<2, 0, false>;
+        kern = MT == 1 ? decode_kernel<1, 0, false, C4> : decode_kernel<2, 0, false, C4>;
         which = MT - 1;
     }
     if (!attr_set[which]) {
@@ -1306,7 +1610,7 @@ cudaError_t launch_decode(const CUtensorMap &tmK, const CUtensorMap &tmV, const 
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)ctas);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(((sw ? kSwWarps : kConsumerWarps) + 1) * 32);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];

@@ -181,23 +181,29 @@ def test_fp8_layers_are_decode_only():
 
 
 @pytest.mark.parametrize("fmt", FORMATS)
-@pytest.mark.parametrize("T", [1, 2, 4])
-def test_fp8_ragged_contexts(T, fmt):
-    """Empty, one-token, page-edge and partial-page contexts with 1, 2 and 4 new
-    tokens on an FP8 full layer, every row against the oracle; the fused append's
-    codes bit-exact."""
+@pytest.mark.parametrize("T,heads,max_ctas", [(1, (16, 2), 0), (2, (16, 2), 0), (4, (16, 2), 0),
+                                              (1, (16, 2), 3), (1, (8, 2), 0), (1, (8, 2), 5)])
+def test_fp8_ragged_contexts(T, heads, max_ctas, fmt):
+    """Empty, one-token, page-edge, partial-page and multi-page contexts with 1, 2
+    and 4 new tokens on an FP8 full layer, every row against the oracle; the fused
+    append's codes bit-exact.  T = 1 with at most 8 query heads a KV head runs the
+    eight-warp loop: 8 and 4 heads (padding columns), units split across CTAs
+    (max_ctas=0: one CTA per SM) and whole units, several a CTA (max_ctas=3, 5)."""
     import dataclasses
     hsa = _cuda()
-    contexts = (0, 1, 63, 64, 65, 127, 200)
-    cfg = dataclasses.replace(workload.CONFIGS["tiny"], T=T, contexts=contexts, B=len(contexts),
-                              index=70 + T)
+    contexts = (0, 1, 63, 64, 65, 127, 200, 1000, 4097)
+    cfg = dataclasses.replace(workload.CONFIGS["tiny"], T=T, Hq=heads[0], Hkv=heads[1],
+                              contexts=contexts, B=len(contexts), index=70 + T + heads[0])
     inst = workload.draw(cfg)
     l = 6
     pool = harness.make_pool(inst, [l], fp8=fmt)
     q, k, v, cl = harness.decode_inputs(inst, l)
     ws = hsa.decode_workspace(pool, inst.R, T)
-    out = hsa.hsa_decode_attn_append(pool, 0, q, k, v, cl, cfg.scale, workspace=ws)
+    err_t = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = hsa.hsa_decode_attn_append(pool, 0, q, k, v, cl, cfg.scale, workspace=ws,
+                                     max_ctas=max_ctas, dev_err=err_t)
     torch.cuda.synchronize()
+    assert int(err_t.item()) == 0
     ref = oracle.attention_fp8hist(scale=cfg.scale, **_fp8_case(inst, l, range(inst.R), fmt))
     got = out.view(-1, cfg.Hq, cfg.d).float().cpu().numpy()
     err = float(np.max(np.abs(got - ref)))
