@@ -873,20 +873,20 @@ def _ctx_desc(cfg):
 # kernel whose source has changed since reports None.  Captures of fewer
 # sequences / requests are scaled to the full launch by the units processed.
 TRAFFIC = {
-    # decode_kernel, full layer: 388.9 MB on 4 sequences, scaled by units
-    ("decode", "full"): ("decode.cu", "053937bc5c4fa8b2", 2827638725),
+    # decode_kernel, full layer: 389.4 MB on 4 sequences, scaled by units
+    ("decode", "full"): ("decode.cu", "07b58d6539e4e363", 2831041157),
     # decode_kernel, sliding layer: full-size launch (32 sequences)
-    ("decode", "sliding"): ("decode.cu", "053937bc5c4fa8b2", 8854528),
-    # decode_kernel, FP8 full layer: 202.5 MB (E4M3) / 202.1 MB (E5M2) on 4
+    ("decode", "sliding"): ("decode.cu", "07b58d6539e4e363", 8851968),
+    # decode_kernel, FP8 full layer: 202.1 MB (E4M3) / 202.2 MB (E5M2) on 4
     # sequences, scaled by units
-    ("decode", "full_fp8"): ("decode.cu", "053937bc5c4fa8b2", 1471985925),
-    ("decode", "full_e5m2"): ("decode.cu", "053937bc5c4fa8b2", 1469482449),
+    ("decode", "full_fp8"): ("decode.cu", "07b58d6539e4e363", 1469743034),
+    ("decode", "full_e5m2"): ("decode.cu", "07b58d6539e4e363", 1470353547),
     # decode_kernel, full layer: 1.608 GB on 1 sequence, scaled by units
-    ("long", "full"): ("decode.cu", "053937bc5c4fa8b2", 5674756107),
-    ("long", "sliding"): ("decode.cu", "053937bc5c4fa8b2", 1181184),
+    ("long", "full"): ("decode.cu", "07b58d6539e4e363", 5674792247),
+    ("long", "sliding"): ("decode.cu", "07b58d6539e4e363", 1188096),
     # decode_kernel, full layer, T = 4: 1.658 GB on 8 sequences, scaled by units
-    ("mtp", "full"): ("decode.cu", "053937bc5c4fa8b2", 11699352313),
-    ("mtp", "sliding"): ("decode.cu", "053937bc5c4fa8b2", 14617344),
+    ("mtp", "full"): ("decode.cu", "07b58d6539e4e363", 11698687581),
+    ("mtp", "sliding"): ("decode.cu", "07b58d6539e4e363", 14617344),
     # prefill_kernel, full layer: 4.720 GB on 2 requests, scaled by flops
     ("prefill", "full"): ("prefill.cu", "5df8d9b43c75a2fc", 14869832402),
     # prefill_swa_kernel, sliding layer: full-size launch

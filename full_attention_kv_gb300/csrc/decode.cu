@@ -27,6 +27,11 @@
 //    groups of MT warps, a group taking every (4 / MT)-th tile with all 64 keys, so
 //    several tiles are in flight.  Rings: two groups, one per tile of a unit.  Online
 //    softmax in registers (exp2, quad shuffles).
+//  * T = 1 special cases with the operands swapped (keys on the MMA's M side, the
+//    unit's <= 8 query heads on N): a sliding layer's whole unit with a full ring
+//    (the new token overwrites the staged row of the one slot its query no longer
+//    sees, so no mask and no new-token tile remain), and FP8 full layers (eight
+//    consumer warps, a 64-key tile each, the new token merged as one more key).
 //  * At the end of a unit the warps merge their softmax states through shared
 //    memory.  A unit covered by one CTA is written straight to `out`; a unit split
 //    across CTAs leaves (m, l, o) partials in the workspace and the last CTA to
@@ -467,31 +472,34 @@ __device__ __forceinline__ void run_tile_fp8(RowState &st, const uint32_t (&qa)[
     st.l[1] += sum1;
 }
 
-// One 64-key page of an FP8 full layer at T = 1 with the operands swapped: S^T =
-// K Q^T with the page's keys on the MMA's M side (four 16-key m-tiles) and the
-// unit's query heads on its N side (column n = head g, heads past G are zero), then
-// O^T += V^T P^T with the output dimensions on M (eight m-tiles).  The shared-memory
-// words are the ones run_tile_fp8 reads (K: four codes of one key, V transposed:
-// four codes of one dimension), now taken for two keys / two dimensions an MMA.  P
-// reaches the B operand of the second product through an 8x8 transpose.  State per
-// thread: heads 2 tq and 2 tq + 1 (m, l in log2 units) and oT[dt] = O^T rows
-// dt * 16 + g, + 8.  Keys >= `valid` are masked (a partly filled last page).
-template <bool E5M2>
+// KM keys (KM / 16 m-tiles) of a 64-key page of an FP8 full layer at T = 1, from
+// key0, with the operands swapped: S^T = K Q^T with the keys on the MMA's M side and
+// the unit's query heads on its N side (column n = head g, heads past G are zero),
+// then O^T += V^T P^T with the output dimensions on M (eight m-tiles).  The
+// shared-memory words are the ones run_tile_fp8 reads (K: four codes of one key, V
+// transposed: four codes of one dimension), now taken for two keys / two dimensions
+// an MMA.  P reaches the B operand of the second product through an 8x8 transpose.
+// State per thread: heads 2 tq and 2 tq + 1 (m, l in log2 units) and oT[dt] = O^T
+// rows dt * 16 + g, + 8.  Keys of the page >= `valid` are masked (a partly filled
+// last page).
+template <int KM, bool E5M2>
 __device__ __forceinline__ void tile_fp8_sw(float (&m)[2], float (&l)[2], float (&oT)[kD / 16][4],
                                             const uint32_t (&qb)[kD / 16][2], const uint8_t *sK,
                                             const uint8_t *sV, const float *k_scale,
-                                            const float *v_scale, int valid, float scale_log2)
+                                            const float *v_scale, int key0, int valid,
+                                            float scale_log2)
 {
+    constexpr int MTS = KM / 16;
     const int lane = threadIdx.x & 31;
     const int g = lane >> 2, tq = lane & 3;
-    float s[4][4], s2[4][4];
+    float s[MTS][4], s2[MTS][4];
 #pragma unroll
-    for (int mt = 0; mt < 4; ++mt)
+    for (int mt = 0; mt < MTS; ++mt)
         s[mt][0] = s[mt][1] = s[mt][2] = s[mt][3] = s2[mt][0] = s2[mt][1] = s2[mt][2] = s2[mt][3] = 0.f;
 #pragma unroll
-    for (int mt = 0; mt < 4; ++mt) {
-        // keys mt * 16 + g and + 8 share (key & 7) = g, so one swizzle serves both rows
-        const uint8_t *ra = sK + (mt * 16 + g) * 128 + 4 * tq;
+    for (int mt = 0; mt < MTS; ++mt) {
+        // keys key0 + mt * 16 + g and + 8 share (key & 7) = g, so one swizzle serves both
+        const uint8_t *ra = sK + (key0 + mt * 16 + g) * 128 + 4 * tq;
         const uint8_t *rb = ra + 8 * 128;
 #pragma unroll
         for (int ks = 0; ks < kD / 16; ++ks) {
@@ -505,8 +513,8 @@ __device__ __forceinline__ void tile_fp8_sw(float (&m)[2], float (&l)[2], float 
     }
     float x0 = -INFINITY, x1 = -INFINITY;
 #pragma unroll
-    for (int mt = 0; mt < 4; ++mt) {
-        const int ka = mt * 16 + g, kb = ka + 8;
+    for (int mt = 0; mt < MTS; ++mt) {
+        const int ka = key0 + mt * 16 + g, kb = ka + 8;
         const float sa = ka < valid ? k_scale[ka] : 0.f, sb = kb < valid ? k_scale[kb] : 0.f;
         s[mt][0] = ka < valid ? (s[mt][0] + s2[mt][0]) * sa : -INFINITY;
         s[mt][1] = ka < valid ? (s[mt][1] + s2[mt][1]) * sa : -INFINITY;
@@ -547,8 +555,9 @@ __device__ __forceinline__ void tile_fp8_sw(float (&m)[2], float (&l)[2], float 
     constexpr float f = E5M2 ? 256.f : 1.f;  // an E5M2 V scale is folded in times 256
     float sum0 = 0.f, sum1 = 0.f;
 #pragma unroll
-    for (int ks = 0; ks < 4; ++ks) {
-        const int ka = ks * 16 + g, kb = ka + 8;
+    for (int ks = 0; ks < MTS; ++ks) {
+        const int ka = key0 + ks * 16 + g, kb = ka + 8;
+        const int grp = (key0 >> 4) + ks;  // 16-key group: the 16-byte chunk of a V row
         const float p0 = fast_exp2(fmaf(s[ks][0], scale_log2, -base0));
         const float p1 = fast_exp2(fmaf(s[ks][1], scale_log2, -base1));
         const float p2 = fast_exp2(fmaf(s[ks][2], scale_log2, -base0));
@@ -564,9 +573,9 @@ __device__ __forceinline__ void tile_fp8_sw(float (&m)[2], float (&l)[2], float 
         for (int dt = 0; dt < kD / 16; ++dt) {
             const int da = dt * 16 + g, db = da + 8;
             const uint32_t wa = *reinterpret_cast<const uint32_t *>(
-                sV + da * 64 + ((ks ^ ((da >> 1) & 3)) << 4) + 4 * tq);
+                sV + da * 64 + ((grp ^ ((da >> 1) & 3)) << 4) + 4 * tq);
             const uint32_t wb = *reinterpret_cast<const uint32_t *>(
-                sV + db * 64 + ((ks ^ ((db >> 1) & 3)) << 4) + 4 * tq);
+                sV + db * 64 + ((grp ^ ((db >> 1) & 3)) << 4) + 4 * tq);
             const uint32_t a[4] = {fp8x2_lo<E5M2>(wa), fp8x2_lo<E5M2>(wb), fp8x2_hi<E5M2>(wa),
                                    fp8x2_hi<E5M2>(wb)};
             mma_f16_16816(oT[dt], a, b0, b1);
@@ -849,60 +858,113 @@ __global__ void __launch_bounds__((CW + 1) * 32, (RING && MT == 1) ? 2 : 1)
         // HSA_WAIT_NS and the kernel must flag HSA_DEVERR_TIMEOUT and return.
         return;
 #endif
-        if (lane == 0) {
-            const uint64_t pol = policy_evict_first();
-            Walk w = w0;
-            int64_t k = 0;
-            const int64_t fp8_cb = fp8_codes_bytes(p.num_blocks, p.Hkv);
-            // the block-table read of the next tile is issued before waiting for its
-            // stage, so its latency hides behind the wait
-            int64_t row = i0 < i1 ? tile_row(p, w, true) : -1;
-            for (int64_t i = i0; i < i1; ++i, ++k) {
-                if (early && (w.j == 0 || i == i0)) {
-                    // before the grid-dependency wait: pull the unit's q rows and new
-                    // K / V rows towards L2 (a hint; the consumers read them after it)
-                    const int Hq = p.G * p.Hkv;
-                    for (int t = 0; t < p.T; ++t) {
-                        const int64_t r = (int64_t)w.b * p.T + t;
-                        prefetch_l2(p.q + (r * Hq + (int64_t)w.h * p.G) * kD, p.G * kD * 2);
-                        prefetch_l2(p.k_new + (r * p.Hkv + w.h) * kD, kD * 2);
-                        prefetch_l2(p.v_new + (r * p.Hkv + w.h) * kD, kD * 2);
+        const uint64_t pol = policy_evict_first();
+        const int64_t fp8_cb = fp8_codes_bytes(p.num_blocks, p.Hkv);
+        // Lane 0: stage k gets item (b, h, j) whose TMA row is r (< 0: nothing to
+        // load; its consumers skip it).  false = the stage never came free.
+        auto issue = [&](int64_t k, int64_t r, int b, int h, int j, bool first) -> bool {
+            if (early && (j == 0 || first)) {
+                // before the grid-dependency wait: pull the unit's q rows and new K / V
+                // rows towards L2 (a hint; the consumers read them after it)
+                const int Hq = p.G * p.Hkv;
+                for (int t = 0; t < p.T; ++t) {
+                    const int64_t rq = (int64_t)b * p.T + t;
+                    prefetch_l2(p.q + (rq * Hq + (int64_t)h * p.G) * kD, p.G * kD * 2);
+                    prefetch_l2(p.k_new + (rq * p.Hkv + h) * kD, kD * 2);
+                    prefetch_l2(p.v_new + (rq * p.Hkv + h) * kD, kD * 2);
+                }
+            }
+            const int st = (int)(k % NS);
+            const uint32_t ph = (uint32_t)((k / NS) & 1);
+            if (!mbar_wait(&sh.empty[st], ph ^ 1)) {
+                set_err(p.dev_err, HSA_DEVERR_TIMEOUT);
+                return false;
+            }
+            // read by the stage's consumers after the full barrier (whose arrive below
+            // releases this write)
+            sh.tile_ok[st] = r >= 0 ? 1 : 0;
+            if (FP8 && r >= 0) {
+                // E4M3 K page (64 rows x 128 B), transposed V page (128 rows x 64 B), and
+                // the page's 64 K and 64 V scales
+                mbar_arrive_expect_tx(&sh.full[st], 2 * kFp8TileBytes + 2 * 256);
+                uint8_t *dst = sh.stage + st * kFp8StageStride;
+                tma_load_2d(dst, &tmK, &sh.full[st], 0, (int32_t)r, pol);
+                tma_load_2d(dst + kFp8TileBytes, &tmV, &sh.full[st], 0, (int32_t)(2 * r), pol);
+                const uint8_t *kb = reinterpret_cast<const uint8_t *>(p.k_dst) + fp8_cb;
+                const uint8_t *vb = reinterpret_cast<const uint8_t *>(p.v_dst) + fp8_cb;
+                bulk_load(dst + 2 * kFp8TileBytes, kb + r * 4, 256, &sh.full[st], pol);
+                bulk_load(dst + 2 * kFp8TileBytes + 256, vb + r * 4, 256, &sh.full[st], pol);
+            } else if (r >= 0) {
+                mbar_arrive_expect_tx(&sh.full[st], kStageBytes);
+                uint8_t *dst = sh.stage + st * kStageBytes;
+                tma_load_2d(dst, &tmK, &sh.full[st], 0, (int32_t)r, pol);
+                tma_load_2d(dst + kTileBytes / 2, &tmK, &sh.full[st], 64, (int32_t)r, pol);
+                tma_load_2d(dst + kTileBytes, &tmV, &sh.full[st], 0, (int32_t)r, pol);
+                tma_load_2d(dst + kTileBytes + kTileBytes / 2, &tmV, &sh.full[st], 64, (int32_t)r,
+                            pol);
+            } else {
+                mbar_arrive(&sh.full[st]);
+            }
+            return true;
+        };
+        int64_t k = 0;
+        if constexpr (FP8 != 0) {
+            // FP8 pages are half the bytes of bf16 ones, and reading the block table one
+            // entry at a time (a dependent L2 access, ~0.5 us, on the producer's path
+            // between stages) bounded the layer.  The rows are read 32 items at a time,
+            // lane l taking item start + l, one batch ahead of the stages they feed; lane
+            // 0 issues the stages, the rows and walk positions reaching it by shuffles.
+            // A lane walks only to items of the CTA's range (past it a walk can cross
+            // many short units, each a dependent read of cached_len).  (Measured on bf16
+            // layers, the same scheme was ~2% slower, so they keep the loop below.)
+            Walk wl = w0;
+            int64_t row = -1;
+            if (i0 + lane < i1) {
+                for (int e = 0; e < lane; ++e)
+                    walk_next(p, wl);
+                row = tile_row(p, wl, true);
+            }
+            for (int64_t ib = i0; ib < i1; ib += 32) {
+                Walk wn = wl;  // this lane's item of the next batch
+                int64_t nrow = -1;
+                if (ib + 32 + lane < i1) {
+                    for (int e = 0; e < 32; ++e)
+                        walk_next(p, wn);
+                    nrow = tile_row(p, wn, true);
+                }
+                const int cnt = (int)(i1 - ib < 32 ? i1 - ib : 32);
+                bool stop = false;
+                for (int e = 0; e < cnt; ++e, ++k) {
+                    const int64_t r = __shfl_sync(0xffffffffu, row, e);
+                    const int eb = __shfl_sync(0xffffffffu, wl.b, e);
+                    const int eh = __shfl_sync(0xffffffffu, wl.h, e);
+                    const int ej = __shfl_sync(0xffffffffu, wl.j, e);
+                    int ok = 1;
+                    if (lane == 0)
+                        ok = issue(k, r, eb, eh, ej, ib + e == i0) ? 1 : 0;
+                    if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                        stop = true;
+                        break;
                     }
                 }
-                const int st = (int)(k % NS);
-                const uint32_t ph = (uint32_t)((k / NS) & 1);
-                if (!mbar_wait(&sh.empty[st], ph ^ 1)) {
-                    set_err(p.dev_err, HSA_DEVERR_TIMEOUT);
+                if (stop)
                     break;
-                }
-                // read by the stage's consumers after the full barrier (whose arrive
-                // below releases this write)
-                sh.tile_ok[st] = row >= 0 ? 1 : 0;
-                if (FP8 && row >= 0) {
-                    // E4M3 K page (64 rows x 128 B), transposed V page (128 rows x 64 B),
-                    // and the page's 64 K and 64 V scales
-                    mbar_arrive_expect_tx(&sh.full[st], 2 * kFp8TileBytes + 2 * 256);
-                    uint8_t *dst = sh.stage + st * kFp8StageStride;
-                    tma_load_2d(dst, &tmK, &sh.full[st], 0, (int32_t)row, pol);
-                    tma_load_2d(dst + kFp8TileBytes, &tmV, &sh.full[st], 0, (int32_t)(2 * row), pol);
-                    const uint8_t *kb = reinterpret_cast<const uint8_t *>(p.k_dst) + fp8_cb;
-                    const uint8_t *vb = reinterpret_cast<const uint8_t *>(p.v_dst) + fp8_cb;
-                    bulk_load(dst + 2 * kFp8TileBytes, kb + row * 4, 256, &sh.full[st], pol);
-                    bulk_load(dst + 2 * kFp8TileBytes + 256, vb + row * 4, 256, &sh.full[st], pol);
-                } else if (row >= 0) {
-                    mbar_arrive_expect_tx(&sh.full[st], kStageBytes);
-                    uint8_t *dst = sh.stage + st * kStageBytes;
-                    tma_load_2d(dst, &tmK, &sh.full[st], 0, (int32_t)row, pol);
-                    tma_load_2d(dst + kTileBytes / 2, &tmK, &sh.full[st], 64, (int32_t)row, pol);
-                    tma_load_2d(dst + kTileBytes, &tmV, &sh.full[st], 0, (int32_t)row, pol);
-                    tma_load_2d(dst + kTileBytes + kTileBytes / 2, &tmV, &sh.full[st], 64,
-                                (int32_t)row, pol);
-                } else {
-                    mbar_arrive(&sh.full[st]);
-                }
+                row = nrow;
+                wl = wn;
+            }
+        } else if (lane == 0) {
+            // the block-table read of the next tile is issued before waiting for its
+            // stage, so its latency hides behind the wait
+            Walk w = w0;
+            int64_t row = i0 < i1 ? tile_row(p, w, true) : -1;
+            for (int64_t i = i0; i < i1; ++i, ++k) {
+                if (!issue(k, row, w.b, w.h, w.j, i == i0))
+                    break;
                 walk_next(p, w);
                 row = i + 1 < i1 ? tile_row(p, w, true) : -1;
             }
+        }
+        if (lane == 0) {
             // drain: no TMA write may still be in flight when the CTA exits
             for (int64_t s = 0; s < NS && s < k; ++s) {
                 const int64_t last = s + ((k - 1 - s) / NS) * NS;
@@ -958,8 +1020,9 @@ __global__ void __launch_bounds__((CW + 1) * 32, (RING && MT == 1) ? 2 : 1)
                 if (!timed_out && sh.tile_ok[stg] != 0 && valid > 0) {
                     const uint8_t *base = sh.stage + stg * kFp8StageStride;
                     const float *ksc = reinterpret_cast<const float *>(base + 2 * kFp8TileBytes);
-                    tile_fp8_sw<kE5>(m, l, oT, qb, base, base + kFp8TileBytes, ksc, ksc + 64,
-                                     valid < kTileKeys ? valid : kTileKeys, p.scale_log2);
+                    tile_fp8_sw<kTileKeys, kE5>(m, l, oT, qb, base, base + kFp8TileBytes, ksc,
+                                                ksc + 64, 0, valid < kTileKeys ? valid : kTileKeys,
+                                                p.scale_log2);
                 }
                 __syncwarp();
                 if (lane == 0)
