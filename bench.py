@@ -344,7 +344,17 @@ class DecodeStep:
             self.host_rows = torch.from_numpy(inst.ring_row[seqs].astype(np.int32)).to(device)
             self.seqs = torch.from_numpy(seqs.astype(np.int32)).to(device)
             self.side = torch.cuda.Stream(device, priority=0)  # below the attention stream
-            self.ready = {i: torch.cuda.Event() for i in self.swa}
+            # one event per run of consecutive sliding layers, recorded once the run's
+            # rings are back: the run's first layer waits on it, and the layers after it
+            # keep their programmatic launch behind the layer before (a wait on another
+            # stream's event before every launch would break that chain)
+            self.runs = []
+            for i in self.swa:
+                if self.runs and self.runs[-1][-1] == i - 1:
+                    self.runs[-1].append(i)
+                else:
+                    self.runs.append([i])
+            self.ready = {r[0]: torch.cuda.Event() for r in self.runs}
             ring_bytes = cfg.Hkv * cfg.W * cfg.d * 2 * 2  # K and V of one sequence's ring
             self.prefetch_bytes = len(seqs) * ring_bytes * len(self.swa)
             self.prefetch_frac = len(seqs) / inst.R
@@ -377,10 +387,11 @@ class DecodeStep:
 
     def prefetch_all(self, stream):
         with torch.cuda.stream(stream):
-            for i in self.swa:
-                self.hsa.hsa_swa_prefetch(self.pool, i, self.host_k[i], self.host_v[i],
-                                          self.host_rows, self.seqs, dev_err=self.err)
-                self.ready[i].record(stream)
+            for r in self.runs:
+                for i in r:
+                    self.hsa.hsa_swa_prefetch(self.pool, i, self.host_k[i], self.host_v[i],
+                                              self.host_rows, self.seqs, dev_err=self.err)
+                self.ready[r[0]].record(stream)
 
     def __call__(self):
         if self.prefetch:
