@@ -884,24 +884,24 @@ def _ctx_desc(cfg):
 # kernel whose source has changed since reports None.  Captures of fewer
 # sequences / requests are scaled to the full launch by the units processed.
 TRAFFIC = {
-    # decode_kernel, full layer: 389.4 MB on 4 sequences, scaled by units
-    ("decode", "full"): ("decode.cu", "07b58d6539e4e363", 2831041157),
+    # decode_kernel, full layer: 389.2 MB on 4 sequences, scaled by units
+    ("decode", "full"): ("decode.cu", "4f3057adad2ada52", 2829665666),
     # decode_kernel, sliding layer: full-size launch (32 sequences)
-    ("decode", "sliding"): ("decode.cu", "07b58d6539e4e363", 8851968),
-    # decode_kernel, FP8 full layer: 202.1 MB (E4M3) / 202.2 MB (E5M2) on 4
+    ("decode", "sliding"): ("decode.cu", "4f3057adad2ada52", 8786944),
+    # decode_kernel, FP8 full layer: 202.1 MB (E4M3 and E5M2) on 4
     # sequences, scaled by units
-    ("decode", "full_fp8"): ("decode.cu", "07b58d6539e4e363", 1469743034),
-    ("decode", "full_e5m2"): ("decode.cu", "07b58d6539e4e363", 1470353547),
+    ("decode", "full_fp8"): ("decode.cu", "4f3057adad2ada52", 1469597851),
+    ("decode", "full_e5m2"): ("decode.cu", "4f3057adad2ada52", 1469201390),
     # decode_kernel, full layer: 1.608 GB on 1 sequence, scaled by units
-    ("long", "full"): ("decode.cu", "07b58d6539e4e363", 5674792247),
-    ("long", "sliding"): ("decode.cu", "07b58d6539e4e363", 1188096),
+    ("long", "full"): ("decode.cu", "4f3057adad2ada52", 5674878985),
+    ("long", "sliding"): ("decode.cu", "4f3057adad2ada52", 1169664),
     # decode_kernel, full layer, T = 4: 1.658 GB on 8 sequences, scaled by units
-    ("mtp", "full"): ("decode.cu", "07b58d6539e4e363", 11698687581),
-    ("mtp", "sliding"): ("decode.cu", "07b58d6539e4e363", 14617344),
-    # prefill_kernel, full layer: 4.720 GB on 2 requests, scaled by flops
-    ("prefill", "full"): ("prefill.cu", "5df8d9b43c75a2fc", 14869832402),
+    ("mtp", "full"): ("decode.cu", "4f3057adad2ada52", 11699016334),
+    ("mtp", "sliding"): ("decode.cu", "4f3057adad2ada52", 14617344),
+    # prefill_kernel, full layer: 4.985 GB on 2 requests, scaled by flops
+    ("prefill", "full"): ("prefill.cu", "7128fc2d6f16d75e", 15703684589),
     # prefill_swa_kernel, sliding layer: full-size launch
-    ("prefill", "sliding"): ("prefill_swa.cu", "9c087b05ca36f8c6", 809227776),
+    ("prefill", "sliding"): ("prefill_swa.cu", "40cbea755aac5f81", 808964352),
     # append_kernel, full-size launches (writes still held in L2 at the kernel's end
     # reach DRAM after it)
     ("prefill", "append_full"): ("append.cu", "436d89e400666e68", 143246080),

@@ -752,7 +752,7 @@ __global__ void __launch_bounds__((CW + 1) * 32, (RING && MT == 1) ? 2 : 1)
     constexpr int NS = RING ? kRingStages : (FP8 ? kFp8Stages : kStages);
     extern __shared__ uint8_t smem_raw[];
     SharedStorage<RING> &sh = *reinterpret_cast<SharedStorage<RING> *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+        align_smem_1024(smem_raw));
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
 

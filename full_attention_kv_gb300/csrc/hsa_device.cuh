@@ -24,6 +24,16 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p)
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// The first 1024-byte boundary (of the shared-memory address) at or after a dynamic
+// shared-memory array, reached by pointer arithmetic on the array itself rather than
+// through an integer, so that the compiler still sees every pointer derived from it
+// as a shared-memory pointer and emits shared loads and stores (not generic ones) for
+// the kernel's plain C++ accesses.
+__device__ __forceinline__ uint8_t *align_smem_1024(uint8_t *base)
+{
+    return base + ((1024u - (smem_u32(base) & 1023u)) & 1023u);
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
 {

@@ -203,7 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 {
     extern __shared__ uint8_t smem_raw[];
     SwaSmem &sh = *reinterpret_cast<SwaSmem *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+        align_smem_1024(smem_raw));
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int ppt = kBM / p.G;  // positions per tile
