@@ -19,11 +19,12 @@
 //    their scales for an FP8 full layer) into a shared-memory stage ring with TMA
 //    (128-byte swizzle), mbarrier-tracked; 4 stages bf16, 8 FP8.  It flags per stage
 //    whether a tile was loaded and reads the next block-table entry before waiting
-//    for a free stage.
-//  * Four consumer warps run tiles on tensor cores (mma.sync m16n8k16, fp32
-//    accumulate).  GQA packing: the G query heads x T tokens that share a KV head
-//    form the M dimension (row = t * G + hh), so each KV byte is read once for all of
-//    them; MT = 1 (T <= 2) or 2 (T = 3, 4) 16-row m-tiles.  Full layers: 4 / MT
+//    for a free stage (FP8 layers: 32 entries at a time, one per lane, a batch ahead).
+//  * Four consumer warps (eight in the FP8 loop below) run tiles on tensor cores
+//    (mma.sync m16n8k16, fp32 accumulate).  GQA packing: the G query heads x T
+//    tokens that share a KV head form the M dimension (row = t * G + hh), so each KV
+//    byte is read once for all of them; MT = 1 (T <= 2) or 2 (T = 3, 4) 16-row
+//    m-tiles.  Full layers: 4 / MT
 //    groups of MT warps, a group taking every (4 / MT)-th tile with all 64 keys, so
 //    several tiles are in flight.  Rings: two groups, one per tile of a unit.  Online
 //    softmax in registers (exp2, quad shuffles).
@@ -39,8 +40,11 @@
 //  * Optionally (hsa_decode_attn_append) the CTA that completes a unit also appends
 //    the unit's new K/V rows to the pool or ring: every read of that unit is done
 //    by then, so even a T > 1 ring write cannot clobber a slot still being read.
+//    (The T = 1 full-ring path appends as soon as its tile is staged: the slot it
+//    writes holds a position no query of the step sees.)
 //  * Launched with programmatic dependent launch: nothing global is read before
-//    griddepcontrol.wait, so the launch and prologue overlap the previous kernel.
+//    griddepcontrol.wait (except, with kDecodeEarly, a sliding layer's item walk and
+//    ring loads), so the launch and prologue overlap the previous kernel.
 #include "fp8_kv.cuh"
 #include "hsa_device.cuh"
 #include "hsa_internal.h"
