@@ -1,6 +1,6 @@
 """Compile the CPU oracle (``hsa_oracle.c``) into ``oracle/_build/liboracle.so``.
 
-Test infrastructure only: this builds the checker, it does not use it.  Plain gcc,
+Test infrastructure only: this compiles the oracle, it does not run it.  Plain gcc,
 -O2 without fast-math so that the double arithmetic stays IEEE; OpenMP if the
 compiler has it.
 """
