@@ -538,7 +538,7 @@ def time_kernel(launch, layers, iters):
 
 
 def _prefetch_report(step, args, stream):
-    """Step time without the prefetch, and the prefetch alone, on the same box."""
+    """Step time without the prefetch, and the prefetch alone, on the same GPU."""
     step.prefetch = False
     g2 = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g2, stream=stream):
