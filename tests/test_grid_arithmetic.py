@@ -2,7 +2,8 @@
 random layouts: the decode kernel's stream-K split and in-kernel merge
 (full_attention_kv_gb300/csrc/decode.cu, including the 1M-token extreme) and the
 prefill kernel's CTA-to-tile-pair map, grid bound and key-tile schedule (csrc/prefill.cu,
-csrc/api.cu), and both kernels' ring-visibility formulas.
+csrc/api.cu), both kernels' ring-visibility formulas, and the slot and owning warp of
+the new token on the sliding decode's T = 1 full-ring path.
 
 Items (64-key tiles) of all units are laid end to end; CTA c takes items
 [c N / C, (c + 1) N / C).  A unit split across CTAs leaves one partial state per
@@ -266,3 +267,45 @@ def test_swa_prefill_tile_walk_matches_the_grid():
         want = [(r, b, h) for r, c in enumerate(C) for b in range((c + ppt - 1) // ppt)
                 for h in range(Hkv)]
         assert sorted(seen) == want
+
+
+def test_ring_t1_new_token_slot_and_owner():
+    """Sliding-layer decode at T = 1 on a full ring (c >= W = 128, decode.cu's
+    leading loop): the kernel writes the new token over the staged row of slot
+    c mod W and then lets the query see all W staged keys.  Against the oracle's ring
+    placement and the window definition: after positions 0 .. c-1 were appended,
+    that slot holds position c - W, the one ring position outside the query's window
+    (c - W, c]; every other slot holds a position inside it, so after the overwrite
+    the W slots hold exactly the window.  And exactly one of the four consumer warps
+    writes the row: warp 2 grp + half reads tile my_j = grp xor (k0 & 1) of the unit
+    (its stage grp, k0 the unit's first item index in the CTA's range), keys
+    32 half .. 32 half + 31 of it."""
+    import numpy as np
+
+    import oracle
+    W = 128
+    ring_row = np.array([0], np.int32)
+    for c in list(range(W, 3 * W + 2)) + [1000, 4097, 65535]:
+        held = [-1] * W
+        for p in range(max(0, c - 2 * W), c):  # older positions are overwritten anyway
+            row, slot = oracle.ring_place(ring_row, 1, W, 0, p)
+            assert row == 0
+            held[slot] = p
+        window = set(range(c - W + 1, c + 1))
+        _, new_slot = oracle.ring_place(ring_row, 1, W, 0, c)
+        assert new_slot == c % W
+        assert held[new_slot] == c - W and (c - W) not in window
+        assert all(held[s] in window for s in range(W) if s != new_slot)
+        after = list(held)
+        after[new_slot] = c
+        assert set(after) == window
+        for k0 in (0, 1, 2, 7):
+            owners = []
+            for warp in range(4):
+                grp, half = warp // 2, warp % 2
+                my_j = grp ^ (k0 & 1)
+                assert (k0 + my_j) % 2 == grp  # the stage of item k0 + my_j is grp
+                if new_slot // 64 == my_j and (new_slot % 64) // 32 == half:
+                    owners.append(warp)
+                    assert my_j * 64 + 32 * half <= new_slot < my_j * 64 + 32 * half + 32
+            assert len(owners) == 1, (c, k0, owners)
