@@ -385,6 +385,8 @@ uint8_t orc_e4m3_encode(float x)
 /* Quantise rows of d bf16 values: codes [rows, d], scales [rows].            */
 void orc_quantize_e4m3(int64_t rows, int d, const uint16_t *x, uint8_t *codes, float *scales)
 {
+    /* rows are independent groups: spread over the host's threads */
+#pragma omp parallel for schedule(static)
     for (int64_t r = 0; r < rows; ++r) {
         float amax = 0.0f;
         for (int c = 0; c < d; ++c) {
@@ -438,6 +440,8 @@ uint8_t orc_e5m2_encode(float x)
 /* Quantise rows of d bf16 values to E5M2: codes [rows, d], scales [rows].     */
 void orc_quantize_e5m2(int64_t rows, int d, const uint16_t *x, uint8_t *codes, float *scales)
 {
+    /* rows are independent groups: spread over the host's threads */
+#pragma omp parallel for schedule(static)
     for (int64_t r = 0; r < rows; ++r) {
         float amax = 0.0f;
         for (int c = 0; c < d; ++c) {
